@@ -1,0 +1,486 @@
+"""Benchmark of the TreeWY verify + commit hot path on GB300.
+
+One step = one speculative round of the wide ragged tree workload: 256
+requests x 32 value heads, dk = dv = 128, one random draft tree per request
+with N uniform in 16..64 nodes and depth <= 8, verified and committed in each
+of 30 GDN layers (30 treewy_verify launches, then 30 treewy_commit launches,
+every layer with its own state pool and inputs, all resident in HBM).
+
+Metric: verified draft nodes per second = (draft nodes in the batch, summed
+over ranks) / (time of one step).  Each layer's inputs (about 1.1 GB) are far
+larger than L2, so no flush is needed between steps.  Also reported: verify
+and commit GB/s on the algorithmic bytes, the roofline fraction of the
+dominant kernel against the measured HBM copy bandwidth, the end-to-end rate
+with host-resident inputs/outputs, the storeall comparator on the same
+inputs, and the CPU oracle on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own independent
+batch (weak scaling, no collective on the data path); ranks meet at a barrier
+around the timed region and rank 0 prints the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from gdn_speculative_tree_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "verified draft nodes/sec (30 GDN layers verify+commit, 256 req x 32 heads, N 16..64)"
+UNIT = "nodes/s"
+CONFIG_NAME = "wide"
+LAYERS = 30
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_tc_wide_traffic.json")
+KERNEL_SOURCES = ["gdn_speculative_tree_gb300/csrc/verify_tc.cu",
+                  "gdn_speculative_tree_gb300/csrc/treewy_device.cuh"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- bytes model
+
+def tree_stats(trees, accepted):
+    """Per-request N, and path length of the accepted node (0 if none)."""
+    Ns, plen = [], []
+    for par, a in zip(trees, accepted):
+        Ns.append(len(par))
+        d = 0
+        cur = int(a)
+        while cur >= 0:
+            d += 1
+            cur = int(par[cur])
+        plen.append(d)
+    return np.array(Ns), np.array(plen)
+
+
+def verify_bytes(Ns, H):
+    # per (request, head): S0 read 64 KiB + per node q,k,v (768 B bf16), alpha,
+    # beta (8 B), o and U written (1024 B fp32), gamma (4 B); parents once per request
+    return int(H * (65536 * len(Ns) + 1804 * Ns.sum()) + 4 * Ns.sum())
+
+
+def commit_bytes(plen, H):
+    # per (request, head) with an accepted node: state read + written (128 KiB)
+    # + per path node u (512 B), k (256 B), alpha (4 B); nothing when a = -1
+    live = plen > 0
+    return int(H * (131072 * live.sum() + 772 * plen.sum()))
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock and throttle reasons)."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(n_requests: int, seed_layer: int = 0):
+    """Time the CPU oracle on the first n_requests of one layer (all heads).
+
+    Returns (nodes in the sample, seconds)."""
+    from oracle import gdn_tree_oracle as orc
+    cfg = wl.CONFIGS[CONFIG_NAME]
+    w = wl.generate(cfg, R=n_requests, layer=seed_layer)
+    node = w.node_offset.numpy()
+    q, k, v = w.q.float().numpy(), w.k.float().numpy(), w.v.float().numpy()
+    alpha, beta, parent = w.alpha.numpy(), w.beta.numpy(), w.parent.numpy()
+    acc = w.accepted.numpy()
+    t0 = time.perf_counter()
+    for r in range(w.R):
+        lo, hi = int(node[r]), int(node[r + 1])
+        S0 = w.state[int(w.state_slot[r])].numpy()
+        res = orc.verify_request(S0, parent[lo:hi], q[lo:hi], k[lo:hi], v[lo:hi], alpha[lo:hi],
+                                 beta[lo:hi])
+        orc.commit_request(S0, res, int(acc[r]))
+    dt = time.perf_counter() - t0
+    return int(node[-1]), dt
+
+
+def cpu_baseline(n_requests: int = 64):
+    nodes, dt = oracle_sample(n_requests)
+    # a full step needs every node through all 30 layers
+    value = nodes / (dt * LAYERS)
+    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, first {n_requests} requests x 32 heads of one layer "
+                      f"({nodes} nodes, {dt:.1f} s single-threaded), scaled to {LAYERS} layers"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    n_req = 8
+    for _ in range(args.warmup):
+        oracle_sample(n_req)
+    times, nodes = [], 0
+    for _ in range(args.steps):
+        nodes, dt = oracle_sample(n_req)
+        times.append(dt)
+    t = sum(times) / len(times)
+    value = nodes / (t * LAYERS)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1000.0 * LAYERS,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "wide ragged trees (256 req x 32 heads, N 16..64, depth<=8, "
+                                   "30 GDN layers); each timed step is a bounded sample",
+                       "sample_requests": n_req},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"first {n_req} requests x 32 heads of one layer per step "
+                                       f"({nodes} nodes), scaled to {LAYERS} layers"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_ours(args, world, rank, local):
+    from gdn_speculative_tree_gb300 import binding
+    from gdn_speculative_tree_gb300 import build as _build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    torch.cuda.set_device(local)
+    _build.build()
+    binding.load()
+    dev = torch.device("cuda", local)
+    cfg = wl.CONFIGS[CONFIG_NAME]
+    layers = args.layers
+
+    # inputs of every layer resident in HBM; trees are shared by the layers
+    work = []
+    for l in range(layers):
+        w = wl.generate(cfg, layer=l + 1000 * rank, device=dev)
+        work.append(binding.TreeVerifier(w))
+    trees, accepted = work[0].wl.trees, work[0].wl.accepted.cpu().numpy()
+    Ns, plen = tree_stats(trees, accepted)
+    H = cfg.H
+    vb, cb = verify_bytes(Ns, H), commit_bytes(plen, H)
+    nodes = int(Ns.sum())
+
+    stream = torch.cuda.current_stream()
+
+    def new_events():
+        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(layers)]
+
+    def step(ev_v=None, ev_c=None):
+        for l, tv in enumerate(work):
+            if ev_v is not None:
+                ev_v[l][0].record(stream)
+            tv.verify(stream)
+            if ev_v is not None:
+                ev_v[l][1].record(stream)
+        for l, tv in enumerate(work):
+            if ev_c is not None:
+                ev_c[l][0].record(stream)
+            tv.commit(None, stream)
+            if ev_c is not None:
+                ev_c[l][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for tv in work:
+        if tv.status.any().item():
+            raise SystemExit(f"device status bits set: {tv.status.unique().tolist()}")
+
+    # timed region: kernel launches on `stream`, inputs resident in HBM; the
+    # per-launch events sit on the same stream and are read after the region
+    events = [(new_events(), new_events()) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for ev_v, ev_c in events:
+            step(ev_v, ev_c)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    v_ms = [a.elapsed_time(b) for ev_v, _ in events for a, b in ev_v]
+    c_ms = [a.elapsed_time(b) for _, ev_c in events for a, b in ev_c]
+    ms_per_step = max_over_ranks(total_ms / args.steps, world)
+    all_nodes = sum_over_ranks(nodes, world)
+    value = all_nodes / (ms_per_step / 1e3)
+
+    peak, peak_kind = read_peaks()
+    v_avg = sum(v_ms) / len(v_ms)
+    c_avg = sum(c_ms) / len(c_ms)
+    v_gbs = vb / (v_avg * 1e-3) / 1e9
+    c_gbs = cb / (c_avg * 1e-3) / 1e9
+    traffic = None
+    if os.path.exists(PROFILE_TRAFFIC):
+        with open(PROFILE_TRAFFIC) as f:
+            prof = json.load(f)
+        if prof.get("kernel_hash") == kernel_hash():
+            traffic = prof.get("traffic_bytes_per_launch")
+
+    # end to end through the public API: per step, pinned host inputs of all
+    # layers copied in, verify + commit, outputs o of all layers copied out
+    e2e = run_e2e(args, work, stream, world)
+
+    storeall = run_storeall(work[0], stream) if rank == 0 and not args.no_storeall else None
+    cpu = cpu_baseline(args.cpu_requests) if rank == 0 and args.cpu_requests > 0 else None
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, shapes of the pages' workloads)",
+        "config": {"workload": "wide ragged trees: 256 requests x 32 value heads per GPU, dk=dv=128, "
+                               "N~U{16..64}, depth<=8, fp32 state, bf16 q/k/v, 30 GDN layers per step",
+                   "R": cfg.R, "H": H, "layers": layers, "nodes_per_layer": nodes,
+                   "l2": "no flush: each layer's inputs (~1.1 GB) exceed the 129 MB L2"},
+        "roofline": {"bound": "hbm", "achieved": v_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": v_gbs / peak, "traffic": traffic,
+                     "kernel": "verify_tc_kernel<64>", "algorithmic_bytes_per_launch": vb,
+                     "avg_launch_ms": v_avg, "peak_kind": f"{peak_kind} hbm_gbs"},
+        "commit": {"achieved_gbs": c_gbs, "frac": c_gbs / peak, "avg_launch_ms": c_avg,
+                   "algorithmic_bytes_per_launch": cb},
+        "verify_nodes_per_s_per_layer": nodes / (v_avg * 1e-3),
+        "head_verifies_per_s": cfg.R * H / (v_avg * 1e-3),
+        "head_node_verifies_per_s": nodes * H / (v_avg * 1e-3),
+        "gpu_launches": 2 * layers * args.steps,
+        "e2e": e2e,
+        "storeall": storeall,
+        "cpu_baseline": cpu,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, work, stream, world):
+    from gdn_speculative_tree_gb300 import binding
+    hosts = []
+    h2d = d2h = 0
+    for tv in work:
+        w = tv.wl
+        ins = {name: getattr(w, name).cpu().pin_memory()
+               for name in ("node_offset", "parent", "q", "k", "v", "alpha", "beta", "accepted")}
+        out = torch.empty(tv.o.shape, dtype=tv.o.dtype).pin_memory()
+        hosts.append((ins, out))
+        h2d += sum(x.numel() * x.element_size() for x in ins.values())
+        d2h += out.numel() * out.element_size()
+
+    def step():
+        for tv, (ins, _) in zip(work, hosts):
+            w = tv.wl
+            for name, x in ins.items():
+                getattr(w, name).copy_(x, non_blocking=True)
+            binding.treewy_verify(tv.batch, stream)
+        for tv, (_, out) in zip(work, hosts):
+            binding.treewy_commit(tv.batch, tv.wl.accepted, stream)
+            out.copy_(tv.o, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    steps = max(2, min(args.steps, 5))
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    dt = max_over_ranks((time.perf_counter() - t0) / steps, world)
+    nodes = sum_over_ranks(int(work[0].wl.node_offset[-1]), world)
+    return {"value": nodes / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": dt * 1e3, "steps": steps,
+            "note": "pinned host inputs (q,k,v,alpha,beta,tree,accepted) of all layers copied in and "
+                    "o of all layers copied out each step; the state pool is model state and stays "
+                    "resident on the device"}
+
+
+def run_storeall(tv, stream):
+    """storeall comparator on layer 0's inputs: snapshot-per-node verify and
+    rollback, timed with CUDA events (state restored afterwards)."""
+    from gdn_speculative_tree_gb300 import binding
+    w = tv.wl
+    T, H = w.T, w.H
+    need = T * H * w.dv * w.dk * 4
+    free, _ = torch.cuda.mem_get_info()
+    if need > 0.8 * free:
+        return {"skipped": f"snapshots need {need / 1e9:.1f} GB, free {free / 1e9:.1f} GB"}
+    snaps = torch.empty(T, H, w.dv, w.dk, device=w.q.device, dtype=torch.float32)
+    S_save = w.state.clone()
+    o = torch.empty_like(tv.o)
+    status = torch.zeros_like(tv.status)
+    b = binding.make_batch(node_offset=w.node_offset, parent=w.parent, q=w.q, k=w.k, v=w.v,
+                           alpha=w.alpha, beta=w.beta, state=w.state, state_slot=w.state_slot,
+                           o=o, U=o, status=status, max_nodes=w.max_nodes)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    vt, ct = [], []
+    for i in range(4):
+        ev[0].record(stream)
+        binding.treewy_storeall_verify(b, snaps, stream)
+        ev[1].record(stream)
+        binding.treewy_storeall_commit(b, snaps, w.accepted, stream)
+        ev[2].record(stream)
+        ev[2].synchronize()
+        w.state.copy_(S_save)
+        if i:
+            vt.append(ev[0].elapsed_time(ev[1]))
+            ct.append(ev[1].elapsed_time(ev[2]))
+    torch.cuda.synchronize()
+    Ns = np.diff(w.node_offset.cpu().numpy())
+    snap_bytes = int(Ns.sum()) * H * w.dv * w.dk * 4
+    v_bytes = snap_bytes + verify_bytes(Ns, H) - int(Ns.sum()) * H * 516
+    del snaps
+    return {"verify_ms_per_layer": statistics.median(vt), "commit_ms_per_layer": statistics.median(ct),
+            "snapshot_bytes_per_layer": snap_bytes, "verify_bytes_per_layer": v_bytes,
+            "verify_gbs": v_bytes / (statistics.median(vt) * 1e-3) / 1e9,
+            "state_blocks_per_request": "N+1 (treewy: 1)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--cpu-requests", type=int, default=64)
+    ap.add_argument("--no-storeall", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+// treewy_api.cu -- the C ABI entry points: argument validation, tensor-map
+// construction for the tensor-core path, kernel dispatch and error reporting.
+// No device memory is allocated here and the host never synchronises.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "treewy_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+treewy_status fail(treewy_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+treewy_status cuda_fail(cudaError_t err, const char* what) {
+  return fail(TREEWY_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-visible checks common to every entry point.
+treewy_status validate(const treewy_batch* b, bool need_qv, bool need_outputs, bool need_k,
+                       bool need_tree = true) {
+  if (b == nullptr) return fail(TREEWY_ERR_INVALID_ARG, "batch is NULL");
+  if (b->R < 0) return fail(TREEWY_ERR_INVALID_ARG, "R = %d is negative", b->R);
+  if (b->H < 1) return fail(TREEWY_ERR_INVALID_ARG, "H = %d must be >= 1", b->H);
+  if (b->dk < 1 || b->dv < 1)
+    return fail(TREEWY_ERR_INVALID_ARG, "dk = %d, dv = %d must be >= 1", b->dk, b->dv);
+  if (b->dk > 128 || b->dv > 128)
+    return fail(TREEWY_ERR_UNSUPPORTED, "dk = %d, dv = %d: head sizes above 128 are not supported",
+                b->dk, b->dv);
+  if (b->max_nodes < 1 || b->max_nodes > TREEWY_MAX_NODES)
+    return fail(TREEWY_ERR_UNSUPPORTED, "max_nodes = %d outside [1, %d]", b->max_nodes,
+                TREEWY_MAX_NODES);
+  if (b->qkv_dtype != TREEWY_DTYPE_BF16 && b->qkv_dtype != TREEWY_DTYPE_F32)
+    return fail(TREEWY_ERR_INVALID_ARG, "qkv_dtype = %d is not TREEWY_DTYPE_BF16/F32", b->qkv_dtype);
+  if (b->T < 0 || b->T > (int64_t(1) << 31) - 1)
+    return fail(TREEWY_ERR_INVALID_ARG, "T = %lld outside [0, 2^31)", (long long)b->T);
+  if (b->num_slots < 1) return fail(TREEWY_ERR_INVALID_ARG, "num_slots = %lld must be >= 1",
+                                    (long long)b->num_slots);
+  if (b->num_slots * b->H * int64_t(b->dv) > (int64_t(1) << 31) - 1)
+    return fail(TREEWY_ERR_UNSUPPORTED, "state pool rows num_slots*H*dv exceed 2^31");
+  if (b->T * b->H * int64_t(b->dv > b->dk ? b->dv : b->dk) > (int64_t(1) << 40))
+    return fail(TREEWY_ERR_UNSUPPORTED, "per-node arrays too large");
+  if (b->R == 0) return TREEWY_OK;
+  if (!b->node_offset || !b->state || !b->state_slot || !b->status)
+    return fail(TREEWY_ERR_INVALID_ARG,
+                "node_offset, state, state_slot and status must be non-NULL");
+  if (need_tree && (!b->parent || !b->alpha))
+    return fail(TREEWY_ERR_INVALID_ARG, "parent and alpha must be non-NULL");
+  if (need_k && !b->k) return fail(TREEWY_ERR_INVALID_ARG, "k is NULL");
+  if (need_qv && (!b->q || !b->v || !b->beta))
+    return fail(TREEWY_ERR_INVALID_ARG, "q, v and beta must be non-NULL");
+  if (need_outputs && (!b->o || !b->U)) return fail(TREEWY_ERR_INVALID_ARG, "o and U must be non-NULL");
+  if (!aligned16(b->state)) return fail(TREEWY_ERR_INVALID_ARG, "state must be 16-byte aligned");
+  if (need_k && !aligned16(b->k)) return fail(TREEWY_ERR_INVALID_ARG, "k must be 16-byte aligned");
+  if (need_qv && (!aligned16(b->q) || !aligned16(b->v)))
+    return fail(TREEWY_ERR_INVALID_ARG, "q and v must be 16-byte aligned");
+  return TREEWY_OK;
+}
+
+bool use_tensor_cores(const treewy_batch* b) {
+  return b->dk == 128 && b->dv == 128 && b->qkv_dtype == TREEWY_DTYPE_BF16 &&
+         (b->flags & TREEWY_FLAG_FORCE_GENERIC) == 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+  });
+  return fn;
+}
+
+treewy_status make_maps(const treewy_batch* b, treewy::VerifyMaps* m) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return fail(TREEWY_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint32_t ones[3] = {1, 1, 1};
+  {
+    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(b->num_slots) * b->H * 128};
+    const cuuint64_t strides[1] = {128 * sizeof(float)};
+    const cuuint32_t box[2] = {32, 128};
+    CUresult rc = enc(&m->s0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, b->state, dims, strides, box,
+                      ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rc != CUDA_SUCCESS) return fail(TREEWY_ERR_CUDA, "tensor map for state failed (%d)", (int)rc);
+  }
+  const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(b->H), static_cast<cuuint64_t>(b->T)};
+  const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(b->H) * 128 * 2};
+  const cuuint32_t box[3] = {64, 1, 8};
+  const void* ptrs[2] = {b->k, b->q};
+  CUtensorMap* maps[2] = {&m->k, &m->q};
+  for (int i = 0; i < 2; ++i) {
+    CUresult rc = enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptrs[i]), dims,
+                      strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rc != CUDA_SUCCESS)
+      return fail(TREEWY_ERR_CUDA, "tensor map for %s failed (%d)", i ? "q" : "k", (int)rc);
+  }
+  return TREEWY_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* treewy_last_error(void) { return g_last_error.c_str(); }
+
+const char* treewy_version(void) { return "treewy-gb300 0.1 (sm_103a)"; }
+
+treewy_status treewy_verify(const treewy_batch* batch, cudaStream_t stream) {
+  g_last_error.clear();
+  treewy_status st = validate(batch, true, true, true);
+  if (st != TREEWY_OK || batch->R == 0) return st;
+  cudaError_t err;
+  if (use_tensor_cores(batch)) {
+    if (batch->T == 0) return TREEWY_OK;
+    treewy::VerifyMaps maps;
+    st = make_maps(batch, &maps);
+    if (st != TREEWY_OK) return st;
+    err = treewy::launch_verify_tc(*batch, maps, batch->max_nodes, stream);
+  } else {
+    err = treewy::launch_verify_generic(*batch, stream);
+  }
+  return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_verify launch");
+}
+
+treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted, cudaStream_t stream) {
+  g_last_error.clear();
+  treewy_status st = validate(batch, false, false, true);
+  if (st != TREEWY_OK || batch->R == 0) return st;
+  if (!batch->U) return fail(TREEWY_ERR_INVALID_ARG, "U is NULL");
+  if (!accepted) return fail(TREEWY_ERR_INVALID_ARG, "accepted is NULL");
+  cudaError_t err = treewy::launch_commit(*batch, accepted, stream);
+  return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_commit launch");
+}
+
+treewy_status treewy_storeall_verify(const treewy_batch* batch, float* snapshots, cudaStream_t stream) {
+  g_last_error.clear();
+  treewy_status st = validate(batch, true, false, true);
+  if (st != TREEWY_OK || batch->R == 0) return st;
+  if (!batch->o) return fail(TREEWY_ERR_INVALID_ARG, "o is NULL");
+  if (!snapshots || !aligned16(snapshots))
+    return fail(TREEWY_ERR_INVALID_ARG, "snapshots must be non-NULL and 16-byte aligned");
+  cudaError_t err = treewy::launch_storeall_verify(*batch, snapshots, stream);
+  return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_storeall_verify launch");
+}
+
+treewy_status treewy_storeall_commit(const treewy_batch* batch, const float* snapshots,
+                                     const int32_t* accepted, cudaStream_t stream) {
+  g_last_error.clear();
+  treewy_status st = validate(batch, false, false, false, false);
+  if (st == TREEWY_OK && batch->R > 0 && !batch->parent)
+    return fail(TREEWY_ERR_INVALID_ARG, "parent is NULL");
+  if (st != TREEWY_OK || batch->R == 0) return st;
+  if (!snapshots || !aligned16(snapshots))
+    return fail(TREEWY_ERR_INVALID_ARG, "snapshots must be non-NULL and 16-byte aligned");
+  if (!accepted) return fail(TREEWY_ERR_INVALID_ARG, "accepted is NULL");
+  cudaError_t err = treewy::launch_storeall_commit(*batch, snapshots, accepted, stream);
+  return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_storeall_commit launch");
+}
+
+}  // extern "C"

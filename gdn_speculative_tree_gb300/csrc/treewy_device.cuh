@@ -1,0 +1,322 @@
+// treewy_device.cuh -- device-side helpers shared by the TreeWY kernels:
+// inline-PTX wrappers for mbarrier, TMA and tcgen05 (sm_103a), bounded waits,
+// and the per-(request, head) draft-tree preparation (decays, ancestor lists).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "treewy.h"
+
+namespace treewy {
+
+constexpr int kMaxNodes = TREEWY_MAX_NODES;
+// Status bits beyond the public ones: an internal wait gave up (outputs of
+// that request/head were not written).  Public in treewy.h as well.
+constexpr int kStatusTimeout = 16;
+constexpr int kStatusBadSlot = 8;
+// Longest a kernel waits on an mbarrier before it gives up (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// ---------------------------------------------------------------- basics
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Load element i of a q/k/v row as float (bf16 or fp32 storage).
+__device__ __forceinline__ float load_qkv(const void* base, int64_t idx, bool is_bf16) {
+  if (is_bf16) {
+    return bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(base) + idx));
+  }
+  return __ldg(reinterpret_cast<const float*>(base) + idx);
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for the phase with the given parity to complete; false after
+// kWaitLimitNs without completion (the caller records a timeout and skips).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 31u) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- TMA
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tensor-core operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* holder, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(holder)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D(tmem) (+)= A(smem desc) * B(smem desc)^T, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on an mbarrier once all previously issued tcgen05.mma of this thread
+// have completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): K-major operand with a
+// 128-byte swizzle, rows 128 bytes apart, 8-row groups `sbo` bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);        // start address
+  d |= static_cast<uint64_t>(1u) << 16;                       // leading byte offset (unused)
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;     // stride byte offset
+  d |= static_cast<uint64_t>(1u) << 46;                       // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;                       // swizzle: 128B
+  return d;
+}
+
+// Instruction descriptor: kind::f16, A and B bf16 K-major, D fp32, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
+  return (1u << 4)             // D format: f32
+         | (1u << 7)           // A format: bf16
+         | (1u << 10)          // B format: bf16
+         | ((N >> 3) << 17)    // N / 8
+         | ((M >> 4) << 24);   // M / 16
+}
+
+// ---------------------------------------------------------------- tree prep
+
+// Per-CTA draft-tree data in shared memory for one (request, head).
+struct TreeSmem {
+  int parent[kMaxNodes];
+  float alpha[kMaxNodes];
+  float beta[kMaxNodes];
+  float gamma[kMaxNodes];
+  int nanc[kMaxNodes];        // number of strict ancestors
+  int aoff[kMaxNodes + 1];    // CSR offsets of the strict-ancestor lists
+  int tok0, N, slot, flags;   // broadcast request data
+};
+
+// Maximum number of strict-ancestor entries of a tree with n nodes.
+__host__ __device__ constexpr int max_anc_entries(int n) { return n * (n - 1) / 2; }
+
+// Load parents and gates of nodes 0..N-1 of this request/head, validate the
+// parents (every parent in [-1, n)), and form the path decays
+// gamma_n = prod of alpha over root..n (the review's Algorithm step 1) and
+// the strict-ancestor counts.  Must be called by all threads; returns false
+// (uniformly) when the tree is invalid.  Requires blockDim.x >= 64.
+__device__ __forceinline__ bool tree_prepare(TreeSmem& ts, const int32_t* __restrict__ parent_g,
+                                             const float* __restrict__ alpha_g,
+                                             const float* __restrict__ beta_g, int H, int h) {
+  const int t = threadIdx.x;
+  const int N = ts.N;
+  bool bad = false;
+  if (t < N) {
+    const int64_t row = static_cast<int64_t>(ts.tok0) + t;
+    const int p = __ldg(parent_g + row);
+    bad = !(p >= -1 && p < t);
+    ts.parent[t] = bad ? -1 : p;
+    ts.alpha[t] = __ldg(alpha_g + row * H + h);
+    ts.beta[t] = __ldg(beta_g + row * H + h);
+  }
+  if (__syncthreads_or(bad)) return false;
+  if (t < N) {
+    // walk towards the root: gamma_t = alpha_t * alpha_p * ...
+    float g = ts.alpha[t];
+    int cnt = 0;
+    int p = ts.parent[t];
+    while (p >= 0) {
+      g *= ts.alpha[p];
+      ++cnt;
+      p = ts.parent[p];
+    }
+    ts.gamma[t] = g;
+    ts.nanc[t] = cnt;
+  }
+  __syncthreads();
+  if (t < 32) {
+    // exclusive scan of nanc over up to 64 nodes, two per lane
+    const int i0 = 2 * t, i1 = 2 * t + 1;
+    const int a0 = i0 < N ? ts.nanc[i0] : 0;
+    const int a1 = i1 < N ? ts.nanc[i1] : 0;
+    int s = a0 + a1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (t >= o) s += y;
+    }
+    const int excl = s - a0 - a1;
+    ts.aoff[i0] = excl;
+    ts.aoff[i1] = excl + a0;
+    if (t == 31) ts.aoff[kMaxNodes] = s;
+  }
+  __syncthreads();
+  return true;
+}
+
+// Walk node n's strict ancestors, nearest first, calling f(j, i, c) for the
+// j-th ancestor i with decay ratio c = gamma_n / gamma_i formed as the
+// product of alpha over the path segment (i, n] (no division).
+template <typename F>
+__device__ __forceinline__ void for_each_ancestor(const TreeSmem& ts, int n, F&& f) {
+  float c = 1.0f;
+  int cur = n;
+  int j = 0;
+  int p = ts.parent[n];
+  while (p >= 0) {
+    c *= ts.alpha[cur];
+    f(j, p, c);
+    ++j;
+    cur = p;
+    p = ts.parent[p];
+  }
+}
+
+// Column-parallel forward substitution of (I + A) U = W for the thread's
+// column d (one unit-lower-triangular solve, TreeWY paper §3 Eq. (2)): Us
+// holds W on entry (row pitch `pitch` floats) and U on exit.  Row n only
+// subtracts its strict ancestors' rows, A[n, idx[e]] = coefA[e].
+__device__ __forceinline__ void solve_inplace(const TreeSmem& ts, float* Us, int pitch, int d,
+                                              const uint8_t* idx, const float* coefA) {
+  const int N = ts.N;
+  for (int n = 0; n < N; ++n) {
+    float acc = Us[n * pitch + d];
+    const int e0 = ts.aoff[n], e1 = ts.aoff[n + 1];
+    for (int e = e0; e < e1; ++e) acc = fmaf(-coefA[e], Us[idx[e] * pitch + d], acc);
+    Us[n * pitch + d] = acc;
+  }
+}
+
+// Output of node n in column d (review §3.1 Eq. (5) restricted to ancestors):
+// o_n = gamma_n (S0 q_n) + (k_n.q_n) u_n + sum_{strict ancestors i} M[n,i] u_i.
+__device__ __forceinline__ float readout_node(const TreeSmem& ts, int n, float s0q,
+                                              const float* Us, int pitch, int d,
+                                              const uint8_t* idx, const float* coefM,
+                                              const float* qk_self) {
+  float acc = ts.gamma[n] * s0q;
+  acc = fmaf(qk_self[n], Us[n * pitch + d], acc);
+  const int e0 = ts.aoff[n], e1 = ts.aoff[n + 1];
+  for (int e = e0; e < e1; ++e) acc = fmaf(coefM[e], Us[idx[e] * pitch + d], acc);
+  return acc;
+}
+
+}  // namespace treewy

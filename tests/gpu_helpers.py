@@ -1,0 +1,83 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the C ABI
+and run the oracle on the same seeded inputs, then compare element by element.
+
+Tolerances: max-abs error of o at most 2e-3 x max|o_ref| and of the committed
+state at most 1e-3 x max|S_ref|, both taken over the compared set; the
+pseudo-values U at most 2e-3 x max|U_ref|; path decays gamma to 1e-5
+relative.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from gdn_speculative_tree_gb300 import binding
+from oracle import gdn_tree_oracle as orc
+
+O_TOL = 2e-3
+S_TOL = 1e-3
+U_TOL = 2e-3
+G_TOL = 1e-5
+
+
+def np32(x: torch.Tensor) -> np.ndarray:
+    return x.detach().to("cpu").to(torch.float32).numpy()
+
+
+class GpuRun:
+    """Verify + commit of one Workload on the GPU (Workload tensors on cuda).
+
+    Keeps a CPU copy of the state pool as it was before the in-place commit.
+    """
+
+    def __init__(self, wl, flags: int = 0, accepted=None, max_nodes=None, commit=True):
+        self.S0_pool = wl.state.cpu()
+        self.tv = binding.TreeVerifier(wl, flags=flags, max_nodes=max_nodes)
+        self.tv.verify()
+        if commit:
+            self.tv.commit(accepted)
+        torch.cuda.synchronize()
+        self.o = np32(self.tv.o)
+        self.U = np32(self.tv.U)
+        self.gamma = np32(self.tv.gamma)
+        self.status = self.tv.status.cpu().numpy()
+        self.S_after = wl.state
+
+
+def oracle_request(wl, r, S0_pool):
+    node = wl.node_offset.cpu().numpy()
+    lo, hi = int(node[r]), int(node[r + 1])
+    S0 = np32(S0_pool[int(wl.state_slot[r])])
+    parent = wl.parent[lo:hi].cpu().numpy()
+    res = orc.verify_request(S0, parent, np32(wl.q[lo:hi]), np32(wl.k[lo:hi]), np32(wl.v[lo:hi]),
+                             np32(wl.alpha[lo:hi]), np32(wl.beta[lo:hi]))
+    return lo, hi, S0, res
+
+
+def compare(wl, run: GpuRun, requests, accepted=None, check_commit=True):
+    """Error ratios of o, U, gamma and the committed state over `requests`."""
+    acc = (wl.accepted if accepted is None else accepted).cpu().numpy()
+    slot = wl.state_slot.cpu().numpy()
+    o_err = o_max = u_err = u_max = g_err = s_err = s_max = 0.0
+    for r in requests:
+        lo, hi, S0, ref = oracle_request(wl, r, run.S0_pool)
+        o_err = max(o_err, float(np.abs(run.o[lo:hi] - ref.o).max(initial=0)))
+        o_max = max(o_max, float(np.abs(ref.o).max(initial=0)))
+        u_err = max(u_err, float(np.abs(run.U[lo:hi] - ref.U).max(initial=0)))
+        u_max = max(u_max, float(np.abs(ref.U).max(initial=0)))
+        if hi > lo:
+            g_err = max(g_err, float((np.abs(run.gamma[lo:hi] - ref.gamma) / ref.gamma).max()))
+        if check_commit:
+            S_ref = orc.commit_request(S0, ref, int(acc[r]))
+            S_gpu = np32(run.S_after[int(slot[r])])
+            s_err = max(s_err, float(np.abs(S_gpu - S_ref).max()))
+            s_max = max(s_max, float(np.abs(S_ref).max()))
+    return {"o": o_err / max(o_max, 1e-30), "U": u_err / max(u_max, 1e-30), "gamma": g_err,
+            "S": s_err / max(s_max, 1e-30) if check_commit else 0.0, "o_abs": o_err, "S_abs": s_err}
+
+
+def assert_within(res, label=""):
+    assert res["o"] <= O_TOL, (label, res)
+    assert res["S"] <= S_TOL, (label, res)
+    assert res["U"] <= U_TOL, (label, res)
+    assert res["gamma"] <= G_TOL, (label, res)

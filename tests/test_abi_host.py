@@ -1,0 +1,108 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads, exports
+every symbol include/treewy.h declares, the ctypes structure matches the C
+layout, and host-side validation rejects bad arguments before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gdn_speculative_tree_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "treewy.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    try:
+        build.nvcc_path()
+    except RuntimeError:
+        pytest.skip("no CUDA toolkit")
+    path = build.build()
+    return binding.load(path)
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(treewy_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in binding.ENTRY_POINTS:
+        assert n in names
+    assert set(names) <= set(binding.ENTRY_POINTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert b"sm_103a" in lib.treewy_version()
+
+
+def test_struct_layout_matches_c():
+    # int32 x6, int64 x2, 13 pointers, uint32 x2 on an LP64 ABI
+    assert ctypes.sizeof(binding.TreewyBatch) == 6 * 4 + 2 * 8 + 13 * 8 + 2 * 4
+    assert binding.TreewyBatch.T.offset == 24
+    assert binding.TreewyBatch.node_offset.offset == 40
+    assert binding.TreewyBatch.flags.offset == 40 + 13 * 8
+
+
+def _valid_batch():
+    b = binding.TreewyBatch()
+    b.R, b.H, b.dk, b.dv, b.max_nodes, b.qkv_dtype = 2, 4, 128, 128, 64, binding.DTYPE_BF16
+    b.T, b.num_slots = 10, 2
+    fake = 0x10000  # never dereferenced: these calls fail validation first
+    for f in ("node_offset", "parent", "q", "k", "v", "alpha", "beta", "state", "state_slot",
+              "o", "U", "status"):
+        setattr(b, f, fake)
+    return b
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("R", -1, binding.TREEWY_ERR_INVALID_ARG),
+    ("H", 0, binding.TREEWY_ERR_INVALID_ARG),
+    ("dk", 0, binding.TREEWY_ERR_INVALID_ARG),
+    ("dk", 256, binding.TREEWY_ERR_UNSUPPORTED),
+    ("dv", 129, binding.TREEWY_ERR_UNSUPPORTED),
+    ("max_nodes", 65, binding.TREEWY_ERR_UNSUPPORTED),
+    ("max_nodes", 0, binding.TREEWY_ERR_UNSUPPORTED),
+    ("qkv_dtype", 7, binding.TREEWY_ERR_INVALID_ARG),
+    ("T", -5, binding.TREEWY_ERR_INVALID_ARG),
+    ("num_slots", 0, binding.TREEWY_ERR_INVALID_ARG),
+    ("q", None, binding.TREEWY_ERR_INVALID_ARG),
+    ("status", None, binding.TREEWY_ERR_INVALID_ARG),
+    ("state", 0x10004, binding.TREEWY_ERR_INVALID_ARG),
+    ("k", 0x10008, binding.TREEWY_ERR_INVALID_ARG),
+])
+def test_verify_rejects_bad_arguments(lib, field, value, code):
+    b = _valid_batch()
+    setattr(b, field, value)
+    rc = lib.treewy_verify(ctypes.byref(b), None)
+    assert rc == code
+    assert lib.treewy_last_error().decode()
+
+
+def test_null_batch_and_null_accepted(lib):
+    assert lib.treewy_verify(None, None) == binding.TREEWY_ERR_INVALID_ARG
+    b = _valid_batch()
+    assert lib.treewy_commit(ctypes.byref(b), None, None) == binding.TREEWY_ERR_INVALID_ARG
+    assert b"accepted" in lib.treewy_last_error()
+    assert lib.treewy_storeall_verify(ctypes.byref(b), None, None) == binding.TREEWY_ERR_INVALID_ARG
+    assert lib.treewy_storeall_commit(ctypes.byref(b), 0x10000, None, None) == \
+        binding.TREEWY_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(lib):
+    b = binding.TreewyBatch()
+    b.R, b.H, b.dk, b.dv, b.max_nodes, b.qkv_dtype, b.T, b.num_slots = 0, 1, 128, 128, 64, 0, 0, 1
+    assert lib.treewy_verify(ctypes.byref(b), None) == binding.TREEWY_OK
+    assert lib.treewy_commit(ctypes.byref(b), None, None) == binding.TREEWY_OK
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        binding.load(str(tmp_path / "nope.so"))
