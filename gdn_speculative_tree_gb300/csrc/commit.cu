@@ -24,7 +24,9 @@ constexpr int kMaxVec = 16;          // float4 per thread for a 128 x 128 state
 __device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(float4* p, float4 v) { __stcs(p, v); }
 
-__global__ void __launch_bounds__(kThreads)
+// Three resident blocks per SM (at most 85 registers a thread) keep three 64 KB
+// state blocks in flight per SM while the blocks' path walks overlap.
+__global__ void __launch_bounds__(kThreads, 3)
     commit_kernel(const treewy_batch b, const int32_t* __restrict__ accepted) {
   __shared__ int s_parent[kMaxNodes];
   __shared__ float s_alpha[kMaxNodes];
