@@ -2,22 +2,31 @@
 // (tcgen05, TMEM accumulators, TMA staging) for dk = dv = 128, bf16 q/k/v,
 // fp32 committed state.
 //
-// One CTA (128 threads, one per value row d = TMEM lane) per (request, head):
+// One CTA (256 threads, two warpgroups; thread t owns TMEM lane t % 128 =
+// value row d) per (request, head).  With Np = N rounded up to 16:
 //
-//  TMA     S0 (64 KB fp32, 4 boxes of 128 rows x 32 columns, 128B swizzle) and
-//          the K and Q rows of the tree (bf16, 8-row boxes) into shared memory.
-//  convert each thread turns its own 128-byte S0 row segment in place into
-//          [hi | lo] bf16 halves, S0 ~= hi + lo (16 significant bits), so the
-//          fp32 state goes through bf16 MMAs without tf32-level rounding.
-//  MMA     D1 = S0 [K;Q]^T  (M = dv = 128, N = 2*Np, K = dk = 128; hi and lo
-//          accumulate into the same fp32 TMEM columns): column n holds
-//          S0 k_n, column Np + n holds S0 q_n  (TreeWY paper §3 Eq. (2) R term,
-//          review §3.2 Algorithm step 3 and the read-out of step 5);
-//          D2 = [K;Q] K^T  (M = 128, N = Np): the Gram rows k_m.k_i, q_m.k_i
-//          (Eq. (2) G, review Algorithm step 2).
-//  solve   thread d: W = beta (v - gamma S0 k), forward substitution over the
-//          ancestor lists, read-out o_n (review Eq. (5) restricted to
-//          ancestors), coalesced stores of o and U.
+//  TMA      S0 (64 KB fp32 as 4 boxes of 128 rows x 32 columns, 128B swizzle)
+//           and the tree's K and Q rows (bf16, 8-row boxes).
+//  split    each thread turns its own 128-byte S0 row segments in place into
+//           [hi | lo] bf16 halves, S0 ~= hi + lo (16 significant bits).
+//  MMA 1    D1 = S0 [K;Q]^T   (M = 128, N = 2Np, K = 128; hi and lo accumulate
+//           into one fp32 accumulator): column n = S0 k_n, column Np+n = S0 q_n
+//           (TreeWY paper §3 Eq. (2), R term; review §3.2 Algorithm steps 3, 5).
+//           D2 = [K;Q] K^T    (M = 128, N = Np): Gram rows k_m.k_i and q_m.k_i
+//           (paper Eq. (2) G; review Algorithm step 2).
+//  coeffs   per node n with root-to-n path p_0 = n, p_1 = parent(n), ...:
+//             A[n, p_k] = beta_n (gamma_n/gamma_{p_k}) k_{p_k}.k_n  (k >= 1)
+//             M[n, p_k] = (gamma_n/gamma_{p_k}) k_{p_k}.q_n         (k >= 0)
+//           then the rows of T = (I + A)^-1 and B = M T restricted to the path,
+//           each by its own O(depth^2) recurrence, since T (I + A) = I and
+//           B (I + A) = M: row n solves x_q = r_q - sum_{a<q} x_a A[p_a, p_q]
+//           with r = e_0 for T and r_q = M[n, p_q] for B.
+//  MMA 2    U = T W and O = B W with W = diag(beta)(V - diag(gamma)(S0 K^T)^T),
+//           as D = W^T [T;B]^T on the tensor cores (bf16 hi/lo splits of W, T
+//           and B; three accumulating products), so the triangular solve of
+//           paper Eq. (2) needs no per-column recurrence.
+//  store    U[n] and o_n = gamma_n S0 q_n + O[n] (review Eq. (5) restricted to
+//           ancestors), coalesced, thread d writing column d.
 //
 // Nothing per node is kept beyond U (N x dv), the object that replaces the
 // per-node snapshots (paper §3 "Reconstruct on commit").
@@ -27,27 +36,103 @@
 namespace treewy {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kDim = 128;
-constexpr uint32_t kS0ChunkBytes = 128u * 128u;          // 128 rows x 32 fp32
-constexpr uint32_t kS0Bytes = 4u * kS0ChunkBytes;        // 64 KB
-constexpr uint32_t kKQChunkBytes = 128u * 128u;          // 128 rows x 64 bf16
-constexpr uint32_t kKQBytes = 2u * kKQChunkBytes;        // 32 KB
-constexpr uint32_t kDynSmem = kS0Bytes + kKQBytes + 1024u;  // + alignment slack
+constexpr uint32_t kS0ChunkBytes = 128u * 128u;     // 128 rows x 32 fp32
+constexpr uint32_t kS0Bytes = 4u * kS0ChunkBytes;   // 64 KB: S0, then W^T and [T;B]
+constexpr uint32_t kKQChunkBytes = 128u * 128u;     // 128 rows x 64 bf16
+constexpr uint32_t kKQBytes = 2u * kKQChunkBytes;   // 32 KB: K,Q, then coefficient lists
+// Operands of the second MMA, placed in the S0 region once the first is done:
+// each is 128 rows x 128 bytes (K-major, 128B swizzle, K <= 64 bf16).
+constexpr uint32_t kWhiOff = 0, kWloOff = 16384, kThiOff = 32768, kTloOff = 49152;
+constexpr int kRegPath = 8;  // paths up to this length keep T/B rows in registers
 
 template <int NPM>
 struct TcCfg {
   static constexpr uint32_t kCols = (3 * NPM <= 64) ? 64u : (3 * NPM <= 128 ? 128u : 256u);
-  static constexpr int kGramPitch = NPM + 1;
-  static constexpr int kE = max_anc_entries(NPM);
-  static constexpr uint32_t kGramBytes = 128u * kGramPitch * 4u;
-  static constexpr uint32_t kIdxOff = kGramBytes;
-  static constexpr uint32_t kCoefAOff = kIdxOff + ((kE + 15u) & ~15u);
-  static constexpr uint32_t kCoefMOff = kCoefAOff + 4u * kE;
-  static constexpr uint32_t kQksOff = kCoefMOff + 4u * kE;
-  static_assert(kQksOff + 4u * NPM <= kS0Bytes, "post-MMA scratch must fit the S0 region");
-  static_assert(NPM * kDim * 4u <= kKQBytes, "U staging must fit the K/Q region");
+  static constexpr int kE = NPM * (NPM + 1) / 2;              // path-list entries, worst case
+  static constexpr uint32_t kListBytes = 4u * kE;
+  static constexpr uint32_t kPidxBytes = (kE + 15u) & ~15u;
+  static constexpr uint32_t kR2Bytes = kPidxBytes + kListBytes;  // pidx + (pc | B scratch)
+  static constexpr uint32_t kDynSmem = kS0Bytes + kKQBytes + kR2Bytes + 1024u;
+  static_assert(3u * kListBytes <= kKQBytes, "A, M and T-scratch lists must fit the K/Q region");
 };
+
+// Per-CTA tree data for one (request, head).
+struct TreeTC {
+  int parent[kMaxNodes];
+  float alpha[kMaxNodes];
+  float gamma[kMaxNodes];
+  float2 bbg[kMaxNodes];                // (beta_n, beta_n * gamma_n)
+  int D[kMaxNodes];                     // path length root..n, n included
+  int off[kMaxNodes + 1];               // CSR offsets of the path lists
+  unsigned long long amask[kMaxNodes];  // strict ancestors as a bit set
+  int tok0, N, slot, flags;
+};
+
+// Load parents and gates, validate the tree, and build every node's path list
+// p_0 = n, p_1, ... with the decay products c_k = gamma_n / gamma_{p_k} formed
+// as products of alpha along the path (no division).  All threads must call
+// it; returns false uniformly when a parent index is out of range.
+__device__ __forceinline__ bool prepare_tree(TreeTC& ts, uint8_t* pidx, float* pc,
+                                             const treewy_batch& b, int h) {
+  const int t = threadIdx.x;
+  const int N = ts.N;
+  const int H = b.H;
+  bool bad = false;
+  float beta = 0.f;
+  if (t < N) {
+    const int64_t row = static_cast<int64_t>(ts.tok0) + t;
+    const int p = __ldg(b.parent + row);
+    bad = !(p >= -1 && p < t);
+    ts.parent[t] = bad ? -1 : p;
+    ts.alpha[t] = __ldg(b.alpha + row * H + h);
+    beta = __ldg(b.beta + row * H + h);
+  }
+  if (__syncthreads_or(bad)) return false;
+  if (t < N) {
+    float g = ts.alpha[t];
+    int D = 1;
+    unsigned long long mask = 0ull;
+    for (int p = ts.parent[t]; p >= 0; p = ts.parent[p]) {
+      g *= ts.alpha[p];
+      ++D;
+      mask |= 1ull << p;
+    }
+    ts.gamma[t] = g;
+    ts.bbg[t] = make_float2(beta, beta * g);
+    ts.D[t] = D;
+    ts.amask[t] = mask;
+  }
+  __syncthreads();
+  if (t < 32) {
+    const int i0 = 2 * t, i1 = 2 * t + 1;
+    const int a0 = i0 < N ? ts.D[i0] : 0;
+    const int a1 = i1 < N ? ts.D[i1] : 0;
+    int s = a0 + a1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (t >= o) s += y;
+    }
+    const int excl = s - a0 - a1;
+    ts.off[i0] = excl;
+    ts.off[i1] = excl + a0;
+    if (t == 31) ts.off[kMaxNodes] = s;
+  }
+  __syncthreads();
+  if (t < N) {
+    const int o = ts.off[t];
+    float c = 1.0f;
+    int k = 0;
+    for (int cur = t; cur >= 0; cur = ts.parent[cur], ++k) {
+      pidx[o + k] = static_cast<uint8_t>(cur);
+      pc[o + k] = c;
+      c *= ts.alpha[cur];
+    }
+  }
+  return true;
+}
 
 // Thread-private in-place conversion of one 128-byte swizzled row segment:
 // 32 fp32 values become 64 bf16 values [hi(32) | lo(32)] with
@@ -64,20 +149,76 @@ __device__ __forceinline__ void convert_row_hilo(unsigned char* row, int sw) {
   }
   uint32_t hi[16], lo[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const __nv_bfloat16 h0 = __float2bfloat16_rn(f[2 * j]);
-    const __nv_bfloat16 h1 = __float2bfloat16_rn(f[2 * j + 1]);
-    const __nv_bfloat16 l0 = __float2bfloat16_rn(f[2 * j] - __bfloat162float(h0));
-    const __nv_bfloat16 l1 = __float2bfloat16_rn(f[2 * j + 1] - __bfloat162float(h1));
-    hi[j] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
-            (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
-    lo[j] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
-            (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
-  }
+  for (int j = 0; j < 16; ++j) split_pair(f[2 * j], f[2 * j + 1], hi[j], lo[j]);
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
     const uint32_t* src = (g < 4) ? (hi + 4 * g) : (lo + 4 * (g - 4));
     *reinterpret_cast<uint4*>(row + ((g ^ sw) << 4)) = make_uint4(src[0], src[1], src[2], src[3]);
+  }
+}
+
+// Zero row `row` of the hi and lo halves of a K-major 128B-swizzled operand.
+__device__ __forceinline__ void zero_operand_row(unsigned char* hi, unsigned char* lo, int row) {
+  unsigned char* rh = hi + row * 128;
+  unsigned char* rl = lo + row * 128;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {  // swizzled order: conflict-free across rows
+    *reinterpret_cast<uint4*>(rh + ((g ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(rl + ((g ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Store x (hi/lo bf16) at column `col` of row `row` of a K-major 128B-swizzled operand.
+__device__ __forceinline__ void put_operand(unsigned char* hi, unsigned char* lo, int row, int col,
+                                            float x) {
+  const __nv_bfloat16 xh = __float2bfloat16_rn(x);
+  const __nv_bfloat16 xl = __float2bfloat16_rn(x - __bfloat162float(xh));
+  const int byte = row * 128 + (((col >> 3) ^ (row & 7)) << 4) + ((col & 7) << 1);
+  *reinterpret_cast<__nv_bfloat16*>(hi + byte) = xh;
+  *reinterpret_cast<__nv_bfloat16*>(lo + byte) = xl;
+}
+
+// Row of T = (I + A)^-1 (rhs = nullptr: r = e_0) or of B = M T (rhs = node n's
+// M coefficients along its path) on node n's path p_0 = n, p_1, ...: solves
+// x_q = r_q - sum_{a<q} x_a A[p_a, p_q], where A[p_a, p_q] is the entry of
+// p_a's strict-ancestor list at position q - a, and writes x_q (hi/lo bf16) at
+// column p_q of operand row `row`.  `scratch` holds x for paths longer than
+// kRegPath (registers otherwise).
+__device__ __forceinline__ void build_path_row(const TreeTC& ts, int n, int row,
+                                               const uint8_t* pidx, const float* aco,
+                                               const float* rhs, float* scratch,
+                                               unsigned char* thi, unsigned char* tlo) {
+  const int Dn = ts.D[n], o = ts.off[n];
+  zero_operand_row(thi, tlo, row);
+  if (Dn <= kRegPath) {
+    int col[kRegPath], opa[kRegPath];
+    float x[kRegPath];
+#pragma unroll
+    for (int a = 0; a < kRegPath; ++a) {
+      const int c = (a < Dn) ? pidx[o + a] : 0;
+      col[a] = c;
+      opa[a] = ts.off[c];
+      x[a] = rhs ? ((a < Dn) ? rhs[o + a] : 0.f) : (a == 0 ? 1.0f : 0.f);
+    }
+#pragma unroll
+    for (int q = 1; q < kRegPath; ++q) {
+#pragma unroll
+      for (int a = 0; a < q; ++a) {
+        const float A = (q < Dn) ? aco[opa[a] + (q - a)] : 0.f;
+        x[q] = fmaf(-x[a], A, x[q]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kRegPath; ++q)
+      if (q < Dn) put_operand(thi, tlo, row, col[q], x[q]);
+  } else {
+    for (int q = 0; q < Dn; ++q) scratch[o + q] = rhs ? rhs[o + q] : (q == 0 ? 1.0f : 0.f);
+    for (int a = 0; a + 1 < Dn; ++a) {
+      const float xa = scratch[o + a];
+      const int opa = ts.off[pidx[o + a]];
+      for (int q = a + 1; q < Dn; ++q) scratch[o + q] = fmaf(-xa, aco[opa + (q - a)], scratch[o + q]);
+    }
+    for (int q = 0; q < Dn; ++q) put_operand(thi, tlo, row, pidx[o + q], scratch[o + q]);
   }
 }
 
@@ -88,8 +229,9 @@ __global__ void __launch_bounds__(kThreads)
                      const __grid_constant__ CUtensorMap map_q, const treewy_batch b) {
   using C = TcCfg<NPM>;
   extern __shared__ unsigned char smem_raw[];
-  __shared__ TreeSmem ts;
-  __shared__ __align__(8) uint64_t bars[6];  // 0-3: S0 chunks, 4: K/Q, 5: MMA done
+  __shared__ TreeTC ts;
+  // 0-3: S0 chunks, 4: K/Q, 5: S0 [K;Q]^T done, 6: second MMA done, 7: Gram done
+  __shared__ __align__(8) uint64_t bars[8];
   __shared__ uint32_t tmem_holder;
   __shared__ int s_fail;
 
@@ -97,17 +239,29 @@ __global__ void __launch_bounds__(kThreads)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
   unsigned char* s0 = base;
   unsigned char* kq = base + kS0Bytes;
+  uint8_t* pidx = base + kS0Bytes + kKQBytes;
+  float* pc = reinterpret_cast<float*>(pidx + C::kPidxBytes);
+  float* xB = pc;  // long-path B rows reuse the decay products once consumed
+  float* aco = reinterpret_cast<float*>(kq);
+  float* mco = aco + C::kE;
+  float* xT = mco + C::kE;
+  unsigned char* thi = s0 + kThiOff;
+  unsigned char* tlo = s0 + kTloOff;
 
   const int H = b.H;
   const int r = blockIdx.x / H;
   const int h = blockIdx.x - r * H;
   const int t = threadIdx.x;
+  const int lane = t & 127;  // TMEM lane = value row d
+  const int wg = t >> 7;
   const int warp = t >> 5;
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
   bool mma_issued = false;
+  bool mma2_issued = false;
 
   if (t == 0) {
 #pragma unroll
-    for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
     fence_mbarrier_init();
     s_fail = 0;
     const int lo = b.node_offset[r], hi = b.node_offset[r + 1];
@@ -150,150 +304,222 @@ __global__ void __launch_bounds__(kThreads)
   tc_fence_after_sync();
   const uint32_t tmem = tmem_holder;
   const int N = ts.N;
+  const int Np = (N + 15) & ~15;
+  const int nch = Np / 16;
   const bool issued = (ts.flags == 0 && N > 0);
   const int64_t tok0 = ts.tok0;
 
-  // Prefetch this thread's column of V (one bf16 per node) into registers;
-  // consumed after the MMA.
+  // Column `lane` of V (one bf16 per node) for the warpgroup that builds W.
   uint32_t vpk[NPM / 2];
   {
     const unsigned short* vg = reinterpret_cast<const unsigned short*>(b.v);
+    const bool mine = issued && wg == 1;
 #pragma unroll
     for (int i = 0; i < NPM / 2; ++i) {
       uint32_t v0 = 0, v1 = 0;
-      if (issued && 2 * i < N) v0 = __ldg(vg + ((tok0 + 2 * i) * H + h) * kDim + t);
-      if (issued && 2 * i + 1 < N) v1 = __ldg(vg + ((tok0 + 2 * i + 1) * H + h) * kDim + t);
+      if (mine && 2 * i < N) v0 = __ldg(vg + ((tok0 + 2 * i) * H + h) * kDim + lane);
+      if (mine && 2 * i + 1 < N) v1 = __ldg(vg + ((tok0 + 2 * i + 1) * H + h) * kDim + lane);
       vpk[i] = v0 | (v1 << 16);
     }
   }
 
   bool bad_tree = false;
-  if (issued) bad_tree = !tree_prepare(ts, b.parent, b.alpha, b.beta, H, h);
+  if (issued) bad_tree = !prepare_tree(ts, pidx, pc, b, h);
 
-  // S0 chunks -> [hi | lo] bf16, each thread converting its own row d = t.
+  // S0 chunks -> [hi | lo] bf16: warpgroup wg converts chunks 2wg, 2wg+1 of row `lane`.
   int fail = 0;
   if (issued) {
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
       if (!mbar_wait(&bars[c], 0)) {
         fail = 1;
         break;
       }
-      if (!bad_tree) convert_row_hilo(s0 + c * kS0ChunkBytes + t * 128, t & 7);
+      if (!bad_tree) convert_row_hilo(s0 + c * kS0ChunkBytes + lane * 128, lane & 7);
     }
     fence_proxy_async_smem();
   }
   fail = __syncthreads_or(fail);
 
-  const int Np = (N + 15) & ~15;
-  if (issued && !bad_tree && !fail && t == 0) {
+  const bool work = issued && !bad_tree;
+  if (work && !fail && t == 0) {
     if (!mbar_wait(&bars[4], 0)) {
       s_fail = 1;
     } else {
       tc_fence_after_sync();
-      const uint32_t a0 = smem_addr(s0);
-      const uint32_t b0 = smem_addr(kq);
+      const uint64_t da = smem_desc_sw128(smem_addr(s0), 1024);
+      const uint64_t db = smem_desc_sw128(smem_addr(kq), 1024);
+      // S0 [K;Q]^T first: its completion frees the S0 region for W^T while the
+      // Gram still runs; the Gram's commit covers both products, after which
+      // the K/Q region and the rest of the S0 region are free.
       const uint32_t id1 = idesc_bf16_f32(128, 2 * Np);
-      const uint32_t id2 = idesc_bf16_f32(128, Np);
-      // D1 = S0 [K;Q]^T over dk in 8 steps of 16, hi then lo part of S0.
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
-          const uint64_t bd = smem_desc_sw128(b0 + (c >> 1) * kKQChunkBytes + (c & 1) * 64 + s * 32, 1024);
-          const uint64_t ahi = smem_desc_sw128(a0 + c * kS0ChunkBytes + s * 32, 1024);
-          const uint64_t alo = smem_desc_sw128(a0 + c * kS0ChunkBytes + 64 + s * 32, 1024);
+          const uint64_t bd = db + (((c >> 1) * kKQChunkBytes + (c & 1) * 64 + s * 32) >> 4);
+          const uint64_t ahi = da + ((c * kS0ChunkBytes + s * 32) >> 4);
+          const uint64_t alo = da + ((c * kS0ChunkBytes + 64 + s * 32) >> 4);
           mma_bf16(tmem, ahi, bd, id1, (c | s) ? 1u : 0u);
           mma_bf16(tmem, alo, bd, id1, 1u);
         }
       }
-      // D2 = [K;Q] K^T (rows past 2*Np are don't-care lanes).
+      mma_commit(&bars[5]);
+      const uint32_t id2 = idesc_bf16_f32(128, Np);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const uint64_t dsc = smem_desc_sw128(b0 + (s >> 2) * kKQChunkBytes + (s & 3) * 32, 1024);
+        const uint64_t dsc = db + (((s >> 2) * kKQChunkBytes + (s & 3) * 32) >> 4);
         mma_bf16(tmem + 2 * NPM, dsc, dsc, id2, s ? 1u : 0u);
       }
-      mma_commit(&bars[5]);
+      mma_commit(&bars[7]);
       mma_issued = true;
     }
   }
   __syncthreads();
   fail |= s_fail;
-  if (issued && !bad_tree && !fail) {
-    if (!mbar_wait(&bars[5], 0)) fail = 1;
-  }
-  fail = __syncthreads_or(fail);
 
-  if (issued && !bad_tree && !fail) {
+  if (work && !fail) {
+    // warpgroup 1 (W^T) waits for S0 [K;Q]^T, warpgroup 0 for the Gram (both products)
+    if (!mbar_wait(&bars[wg ? 5 : 7], 0)) fail = 1;
+    fail = wg ? named_bar_or<2, 128>(fail) : named_bar_or<1, 128>(fail);
     tc_fence_after_sync();
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    float* gram = reinterpret_cast<float*>(s0);
-    uint8_t* idx = s0 + C::kIdxOff;
-    float* coefA = reinterpret_cast<float*>(s0 + C::kCoefAOff);
-    float* coefM = reinterpret_cast<float*>(s0 + C::kCoefMOff);
-    float* qks = reinterpret_cast<float*>(s0 + C::kQksOff);
-    float* Us = reinterpret_cast<float*>(kq);
-
-    // Gram row of this lane: k_t.k_i (t < Np) or q_{t-Np}.k_i (t >= Np).
-    for (int c = 0; c < Np / 16; ++c) {
-      float g[16];
-      tmem_ld16(tmem + lane_base + 2 * NPM + 16 * c, g);
+    if (fail) {
+      // skip this warpgroup's work; the join below reports the failure
+    } else if (wg == 0) {
+      // ---- ancestor coefficients from this lane's Gram row
+      const bool isA = lane < N;
+      const int myn = isA ? lane : ((lane >= Np && lane < Np + N) ? lane - Np : -1);
+      if ((lane >= N && lane < Np) || (lane >= Np + N && lane < 2 * Np))
+        zero_operand_row(thi, tlo, lane);  // padding rows of [T;B]
+      unsigned long long mask = 0ull;
+      int Dn = 0, offn = 0;
+      float scale = 0.f;
+      if (myn >= 0) {
+        mask = ts.amask[myn] | (isA ? 0ull : (1ull << myn));
+        Dn = ts.D[myn];
+        offn = ts.off[myn];
+        scale = isA ? ts.bbg[myn].x : 1.0f;
+      }
+      float* dst = isA ? aco : mco;
+      uint32_t ga[16], gb[16];
+      tmem_ld16_async(tmem + lane_base + 2 * NPM, ga);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) gram[t * C::kGramPitch + 16 * c + j] = g[j];
-    }
-    // ancestor-masked coefficients from the thread's own Gram row
-    if (t < N) {
-      const int n = t;
-      const float bn = ts.beta[n];
-      for_each_ancestor(ts, n, [&](int j, int i, float c) {
-        const int e = ts.aoff[n] + j;
-        idx[e] = static_cast<uint8_t>(i);
-        coefA[e] = bn * c * gram[t * C::kGramPitch + i];
-      });
-    }
-    if (t >= Np && t < Np + N) {
-      const int n = t - Np;
-      for_each_ancestor(ts, n, [&](int j, int i, float c) {
-        coefM[ts.aoff[n] + j] = c * gram[t * C::kGramPitch + i];
-      });
-      qks[n] = gram[t * C::kGramPitch + n];
-    }
-    // W[n][d] = beta_n (v_n[d] - gamma_n (S0 k_n)[d])
+      for (int c = 0; c < NPM / 16; ++c) {
+        if (c < nch) {
+          uint32_t(&cur)[16] = (c & 1) ? gb : ga;
+          uint32_t(&nxt)[16] = (c & 1) ? ga : gb;
+          tmem_wait16(cur);
+          if (c + 1 < nch) tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * (c + 1), nxt);
+          const unsigned int bits = static_cast<unsigned int>(mask >> (16 * c)) & 0xFFFFu;
+          if (bits) {
 #pragma unroll
-    for (int c = 0; c < NPM / 16; ++c) {
-      if (16 * c < N) {
-        float p[16];
-        tmem_ld16(tmem + lane_base + 16 * c, p);
+            for (int j = 0; j < 16; ++j) {
+              if ((bits >> j) & 1u) {
+                const int k = Dn - ts.D[16 * c + j];
+                dst[offn + k] = scale * pc[offn + k] * __uint_as_float(cur[j]);
+              }
+            }
+          }
+        }
+      }
+    } else {
+      // ---- row `lane` of W^T: W[n][d] = beta_n v_n[d] - beta_n gamma_n (S0 k_n)[d]
+      unsigned char* whi = s0 + kWhiOff + lane * 128;
+      unsigned char* wlo = s0 + kWloOff + lane * 128;
+      const int sw = lane & 7;
+      uint32_t pa[16], pb[16];
+      tmem_ld16_async(tmem + lane_base, pa);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int n = 16 * c + j;
-          if (n < N) {
+      for (int c = 0; c < NPM / 16; ++c) {
+        if (c < nch) {
+          uint32_t(&cur)[16] = (c & 1) ? pb : pa;
+          uint32_t(&nxt)[16] = (c & 1) ? pa : pb;
+          tmem_wait16(cur);
+          if (c + 1 < nch) tmem_ld16_async(tmem + lane_base + 16 * (c + 1), nxt);
+          float w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = 16 * c + j;
             const uint32_t pair = vpk[n >> 1];
             const float vv = bf16_bits_to_float(static_cast<uint16_t>((n & 1) ? (pair >> 16) : pair));
-            Us[n * kDim + t] = ts.beta[n] * (vv - ts.gamma[n] * p[j]);
+            const float2 bb = ts.bbg[n];
+            w[j] = (n < N) ? fmaf(-bb.y, __uint_as_float(cur[j]), bb.x * vv) : 0.f;
+          }
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) split_pair(w[2 * j], w[2 * j + 1], hi[j], lo[j]);
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            const int gg = 2 * c + g;
+            *reinterpret_cast<uint4*>(whi + ((gg ^ sw) << 4)) =
+                make_uint4(hi[4 * g], hi[4 * g + 1], hi[4 * g + 2], hi[4 * g + 3]);
+            *reinterpret_cast<uint4*>(wlo + ((gg ^ sw) << 4)) =
+                make_uint4(lo[4 * g], lo[4 * g + 1], lo[4 * g + 2], lo[4 * g + 3]);
           }
         }
       }
     }
-    __syncthreads();
-
-    solve_inplace(ts, Us, kDim, t, idx, coefA);
+    if (wg == 0 && !fail) {
+      named_bar_sync<1, 128>();
+      // ---- T rows (threads 0..N-1) and B rows (threads 64..64+N-1) together
+      if (t < N) build_path_row(ts, t, t, pidx, aco, nullptr, xT, thi, tlo);
+      if (t >= 64 && t - 64 < N) build_path_row(ts, t - 64, Np + t - 64, pidx, aco, mco, xB, thi, tlo);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    fail = __syncthreads_or(fail);
+    if (!fail && t == 0) {
+      tc_fence_after_sync();
+      const uint64_t da = smem_desc_sw128(smem_addr(s0), 1024);
+      const uint32_t id = idesc_bf16_f32(128, Np);
 #pragma unroll
-    for (int c = 0; c < NPM / 16; ++c) {
-      if (16 * c < N) {
-        float pq[16];
-        tmem_ld16(tmem + lane_base + Np + 16 * c, pq);
+      for (int part = 0; part < 2; ++part) {
+        const uint32_t d = tmem + (part ? 2 * NPM : 0);
+        const uint32_t brow = part ? Np * 128 : 0;
+#pragma unroll
+        for (int s = 0; s < NPM / 16; ++s) {
+          if (s < nch) {
+            const uint32_t ko = s * 32;
+            const uint64_t whi = da + ((kWhiOff + ko) >> 4);
+            const uint64_t wlo = da + ((kWloOff + ko) >> 4);
+            const uint64_t thd = da + ((kThiOff + brow + ko) >> 4);
+            const uint64_t tld = da + ((kTloOff + brow + ko) >> 4);
+            mma_bf16(d, whi, thd, id, s ? 1u : 0u);
+            mma_bf16(d, wlo, thd, id, 1u);
+            mma_bf16(d, whi, tld, id, 1u);
+          }
+        }
+      }
+      mma_commit(&bars[6]);
+      mma2_issued = true;
+    }
+    if (!fail && !mbar_wait(&bars[6], 0)) fail = 1;
+    fail = __syncthreads_or(fail);
+    if (!fail) {
+      tc_fence_after_sync();
+      // ---- U[n] and o_n = gamma_n S0 q_n + O[n], column d = lane; warpgroups
+      //      take alternate 16-node chunks
+      float* og = b.o + (tok0 * H + h) * kDim + lane;
+      float* ug = b.U + (tok0 * H + h) * kDim + lane;
+      const int64_t stride = static_cast<int64_t>(H) * kDim;
+      for (int c = wg; c < nch; c += 2) {
+        uint32_t u[16], oo[16], pq[16];
+        tmem_ld16_async(tmem + lane_base + 16 * c, u);
+        tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * c, oo);
+        tmem_ld16_async(tmem + lane_base + Np + 16 * c, pq);
+        tmem_wait16(u);
+        tmem_regs_ready(oo);
+        tmem_regs_ready(pq);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int n = 16 * c + j;
           if (n < N) {
-            const float o = readout_node(ts, n, pq[j], Us, kDim, t, idx, coefM, qks);
-            b.o[((tok0 + n) * H + h) * kDim + t] = o;
+            ug[n * stride] = __uint_as_float(u[j]);
+            og[n * stride] = fmaf(ts.gamma[n], __uint_as_float(pq[j]), __uint_as_float(oo[j]));
           }
         }
       }
+      if (b.gamma != nullptr && t < N) b.gamma[(tok0 + t) * H + h] = ts.gamma[t];
     }
-    for (int n = 0; n < N; ++n) b.U[((tok0 + n) * H + h) * kDim + t] = Us[n * kDim + t];
-    if (b.gamma != nullptr && t < N) b.gamma[(tok0 + t) * H + h] = ts.gamma[t];
   }
 
   if (t == 0) {
@@ -303,7 +529,11 @@ __global__ void __launch_bounds__(kThreads)
     if (issued) {
       // No async copy or MMA may still target this CTA's memory at exit.
       for (int i = 0; i < 5; ++i) mbar_wait(&bars[i], 0);
-      if (mma_issued) mbar_wait(&bars[5], 0);
+      if (mma_issued) {
+        mbar_wait(&bars[5], 0);
+        mbar_wait(&bars[7], 0);
+      }
+      if (mma2_issued) mbar_wait(&bars[6], 0);
     }
   }
   tc_fence_before_sync();
@@ -317,16 +547,21 @@ __global__ void __launch_bounds__(kThreads)
 template <int NPM>
 cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, cudaStream_t stream) {
   static cudaError_t attr = cudaFuncSetAttribute(
-      verify_tc_kernel<NPM>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kDynSmem));
+      verify_tc_kernel<NPM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      static_cast<int>(TcCfg<NPM>::kDynSmem));
   if (attr != cudaSuccess) return attr;
   const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
-  verify_tc_kernel<NPM><<<grid, kThreads, kDynSmem, stream>>>(m.s0, m.k, m.q, b);
+  verify_tc_kernel<NPM><<<grid, kThreads, TcCfg<NPM>::kDynSmem, stream>>>(m.s0, m.k, m.q, b);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t verify_tc_smem(int) { return kDynSmem; }
+size_t verify_tc_smem(int npm) {
+  if (npm <= 16) return TcCfg<16>::kDynSmem;
+  if (npm <= 32) return TcCfg<32>::kDynSmem;
+  return TcCfg<64>::kDynSmem;
+}
 
 cudaError_t launch_verify_tc(const treewy_batch& b, const VerifyMaps& maps, int npm,
                              cudaStream_t stream) {
