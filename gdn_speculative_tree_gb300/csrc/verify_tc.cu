@@ -309,22 +309,41 @@ __global__ void __launch_bounds__(kThreads)
   const bool issued = (ts.flags == 0 && N > 0);
   const int64_t tok0 = ts.tok0;
 
-  // Column `lane` of V (one bf16 per node) for the warpgroup that builds W.
+  // Column `lane` of V for the warpgroup that builds W.  Each thread loads the
+  // bf16 pair of columns (lane & ~1, lane | 1) of every other node (half the
+  // load requests of one 2-byte load per node), and neighbouring lanes swap
+  // halves after the tree is prepared.
   uint32_t vpk[NPM / 2];
   {
-    const unsigned short* vg = reinterpret_cast<const unsigned short*>(b.v);
+    const uint32_t* vg = reinterpret_cast<const uint32_t*>(b.v);
     const bool mine = issued && wg == 1;
+    const int par = lane & 1;
 #pragma unroll
     for (int i = 0; i < NPM / 2; ++i) {
-      uint32_t v0 = 0, v1 = 0;
-      if (mine && 2 * i < N) v0 = __ldg(vg + ((tok0 + 2 * i) * H + h) * kDim + lane);
-      if (mine && 2 * i + 1 < N) v1 = __ldg(vg + ((tok0 + 2 * i + 1) * H + h) * kDim + lane);
-      vpk[i] = v0 | (v1 << 16);
+      const int n = 2 * i + par;
+      uint32_t x = 0;
+      if (mine && n < N) x = __ldg(vg + (((tok0 + n) * H + h) * kDim + (lane & ~1)) / 2);
+      vpk[i] = x;  // pair of columns for node 2i+par
     }
   }
 
   bool bad_tree = false;
   if (issued) bad_tree = !prepare_tree(ts, pidx, pc, b, h);
+  if (wg == 1) {
+    const int par = lane & 1;
+#pragma unroll
+    for (int i = 0; i < NPM / 2; ++i) {
+      // this lane holds a column pair of node 2i+par, its neighbour of node 2i+1-par
+      const uint32_t mine2 = vpk[i];
+      const uint32_t other = __shfl_xor_sync(0xffffffffu, mine2, 1);
+      // node 2i: from the even lane's load; node 2i+1: from the odd lane's load
+      const uint32_t n0 = par ? other : mine2;   // node 2i columns pair
+      const uint32_t n1 = par ? mine2 : other;   // node 2i+1 columns pair
+      const uint32_t v0 = par ? (n0 >> 16) : (n0 & 0xFFFFu);
+      const uint32_t v1 = par ? (n1 >> 16) : (n1 & 0xFFFFu);
+      vpk[i] = v0 | (v1 << 16);
+    }
+  }
 
   // S0 chunks -> [hi | lo] bf16: warpgroup wg converts chunks 2wg, 2wg+1 of row `lane`.
   int fail = 0;
