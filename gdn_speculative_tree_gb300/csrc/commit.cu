@@ -144,19 +144,40 @@ __global__ void __launch_bounds__(kThreads, 3)
         kf[j][x] = (x < dk) ? load_qkv(b.k, row * dk + x, bf16) : 0.f;
       }
       __syncthreads();
+      if (dk == 128) {
+        // float4 f = t + 256 m covers row d = t/32 + 8m, columns x..x+3 with
+        // x = 4 (t % 32): the k chunk of a path node is loaded once per node
+        const int x = (t & 31) << 2;
+        const int d0 = t >> 5;
+        for (int j = 0; j < ns; ++j) {
+          const float4 kk = *reinterpret_cast<const float4*>(&kf[j][x]);
 #pragma unroll
-      for (int m = 0; m < kMaxVec; ++m) {
-        const int f = t + m * kThreads;
-        if (f < nvec) {
-          const int e = f << 2;
-          const int d = e / dk, x = e - d * dk;
-          for (int j = 0; j < ns; ++j) {
-            const float u = cu[j][d];
-            const float4 kk = *reinterpret_cast<const float4*>(&kf[j][x]);
-            acc[m].x = fmaf(u, kk.x, acc[m].x);
-            acc[m].y = fmaf(u, kk.y, acc[m].y);
-            acc[m].z = fmaf(u, kk.z, acc[m].z);
-            acc[m].w = fmaf(u, kk.w, acc[m].w);
+          for (int m = 0; m < kMaxVec; ++m) {
+            const int d = d0 + 8 * m;
+            if (d < dv) {
+              const float u = cu[j][d];
+              acc[m].x = fmaf(u, kk.x, acc[m].x);
+              acc[m].y = fmaf(u, kk.y, acc[m].y);
+              acc[m].z = fmaf(u, kk.z, acc[m].z);
+              acc[m].w = fmaf(u, kk.w, acc[m].w);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int m = 0; m < kMaxVec; ++m) {
+          const int f = t + m * kThreads;
+          if (f < nvec) {
+            const int e = f << 2;
+            const int d = e / dk, x = e - d * dk;
+            for (int j = 0; j < ns; ++j) {
+              const float u = cu[j][d];
+              const float4 kk = *reinterpret_cast<const float4*>(&kf[j][x]);
+              acc[m].x = fmaf(u, kk.x, acc[m].x);
+              acc[m].y = fmaf(u, kk.y, acc[m].y);
+              acc[m].z = fmaf(u, kk.z, acc[m].z);
+              acc[m].w = fmaf(u, kk.w, acc[m].w);
+            }
           }
         }
       }

@@ -22,9 +22,9 @@
 //           B (I + A) = M: row n solves x_q = r_q - sum_{a<q} x_a A[p_a, p_q]
 //           with r = e_0 for T and r_q = M[n, p_q] for B.
 //  MMA 2    U = T W and O = B W with W = diag(beta)(V - diag(gamma)(S0 K^T)^T),
-//           as D = W^T [T;B]^T on the tensor cores (bf16 hi/lo splits of W, T
-//           and B; three accumulating products), so the triangular solve of
-//           paper Eq. (2) needs no per-column recurrence.
+//           as one product [U | O] = W^T [T;B]^T (M = 128, N = 2Np, K = Np;
+//           bf16 hi/lo splits of W, T and B, three accumulating terms), so the
+//           triangular solve of paper Eq. (2) needs no per-column recurrence.
 //  store    U[n] and o_n = gamma_n S0 q_n + O[n] (review Eq. (5) restricted to
 //           ancestors), coalesced, thread d writing column d.
 //
@@ -49,7 +49,9 @@ constexpr int kRegPath = 8;  // paths up to this length keep T/B rows in registe
 
 template <int NPM>
 struct TcCfg {
-  static constexpr uint32_t kCols = (3 * NPM <= 64) ? 64u : (3 * NPM <= 128 ? 128u : 256u);
+  // D1 = [S0k | S0q] in columns [0, 2NPM); the Gram, then [U | O], from 2NPM
+  static constexpr uint32_t kCols = 4u * NPM;
+  static_assert(NPM == 16 || NPM == 32 || NPM == 64, "tree capacity bucket");
   static constexpr int kE = NPM * (NPM + 1) / 2;              // path-list entries, worst case
   static constexpr uint32_t kListBytes = 4u * kE;
   static constexpr uint32_t kPidxBytes = (kE + 15u) & ~15u;
@@ -66,7 +68,6 @@ struct TreeTC {
   float2 bbg[kMaxNodes];                // (beta_n, beta_n * gamma_n)
   int D[kMaxNodes];                     // path length root..n, n included
   int off[kMaxNodes + 1];               // CSR offsets of the path lists
-  unsigned long long amask[kMaxNodes];  // strict ancestors as a bit set
   int tok0, N, slot, flags;
 };
 
@@ -93,16 +94,13 @@ __device__ __forceinline__ bool prepare_tree(TreeTC& ts, uint8_t* pidx, float* p
   if (t < N) {
     float g = ts.alpha[t];
     int D = 1;
-    unsigned long long mask = 0ull;
     for (int p = ts.parent[t]; p >= 0; p = ts.parent[p]) {
       g *= ts.alpha[p];
       ++D;
-      mask |= 1ull << p;
     }
     ts.gamma[t] = g;
     ts.bbg[t] = make_float2(beta, beta * g);
     ts.D[t] = D;
-    ts.amask[t] = mask;
   }
   __syncthreads();
   if (t < 32) {
@@ -314,16 +312,15 @@ __global__ void __launch_bounds__(kThreads)
   // load requests of one 2-byte load per node), and neighbouring lanes swap
   // halves after the tree is prepared.
   uint32_t vpk[NPM / 2];
-  {
+#pragma unroll
+  for (int i = 0; i < NPM / 2; ++i) vpk[i] = 0u;
+  if (issued && wg == 1) {
     const uint32_t* vg = reinterpret_cast<const uint32_t*>(b.v);
-    const bool mine = issued && wg == 1;
     const int par = lane & 1;
 #pragma unroll
     for (int i = 0; i < NPM / 2; ++i) {
       const int n = 2 * i + par;
-      uint32_t x = 0;
-      if (mine && n < N) x = __ldg(vg + (((tok0 + n) * H + h) * kDim + (lane & ~1)) / 2);
-      vpk[i] = x;  // pair of columns for node 2i+par
+      if (n < N) vpk[i] = __ldg(vg + (((tok0 + n) * H + h) * kDim + (lane & ~1)) / 2);
     }
   }
 
@@ -345,15 +342,16 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
 
-  // S0 chunks -> [hi | lo] bf16: warpgroup wg converts chunks 2wg, 2wg+1 of row `lane`.
+  // S0 chunks -> [hi | lo] bf16: warpgroup wg converts chunks 2wg, 2wg+1 of row
+  // `lane`.  Waits on an mbarrier are done by one thread per warpgroup; the
+  // others sleep at a hardware barrier instead of spinning.
   int fail = 0;
   if (issued) {
-    for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-      if (!mbar_wait(&bars[c], 0)) {
-        fail = 1;
-        break;
-      }
-      if (!bad_tree) convert_row_hilo(s0 + c * kS0ChunkBytes + lane * 128, lane & 7);
+    if (lane == 0) fail = !(mbar_wait(&bars[2 * wg], 0) && mbar_wait(&bars[2 * wg + 1], 0));
+    fail = wg ? named_bar_or<2, 128>(fail) : named_bar_or<1, 128>(fail);
+    if (!fail && !bad_tree) {
+      convert_row_hilo(s0 + (2 * wg) * kS0ChunkBytes + lane * 128, lane & 7);
+      convert_row_hilo(s0 + (2 * wg + 1) * kS0ChunkBytes + lane * 128, lane & 7);
     }
     fence_proxy_async_smem();
   }
@@ -398,27 +396,19 @@ __global__ void __launch_bounds__(kThreads)
 
   if (work && !fail) {
     // warpgroup 1 (W^T) waits for S0 [K;Q]^T, warpgroup 0 for the Gram (both products)
-    if (!mbar_wait(&bars[wg ? 5 : 7], 0)) fail = 1;
+    if (lane == 0 && !mbar_wait(&bars[wg ? 5 : 7], 0)) fail = 1;
     fail = wg ? named_bar_or<2, 128>(fail) : named_bar_or<1, 128>(fail);
     tc_fence_after_sync();
     if (fail) {
       // skip this warpgroup's work; the join below reports the failure
     } else if (wg == 0) {
-      // ---- ancestor coefficients from this lane's Gram row
-      const bool isA = lane < N;
-      const int myn = isA ? lane : ((lane >= Np && lane < Np + N) ? lane - Np : -1);
-      if ((lane >= N && lane < Np) || (lane >= Np + N && lane < 2 * Np))
-        zero_operand_row(thi, tlo, lane);  // padding rows of [T;B]
-      unsigned long long mask = 0ull;
-      int Dn = 0, offn = 0;
-      float scale = 0.f;
-      if (myn >= 0) {
-        mask = ts.amask[myn] | (isA ? 0ull : (1ull << myn));
-        Dn = ts.D[myn];
-        offn = ts.off[myn];
-        scale = isA ? ts.bbg[myn].x : 1.0f;
-      }
-      float* dst = isA ? aco : mco;
+      // ---- ancestor coefficients from this lane's Gram row.  The row is
+      //      dumped to shared memory (thread-private, XOR-swizzled, in the
+      //      [T;B] area that is written only later), then each lane walks its
+      //      own node's path: A entries for lanes < N, M entries for lanes
+      //      Np..Np+N-1.
+      float* gdump = reinterpret_cast<float*>(s0 + kThiOff);  // 128 rows x 64 floats
+      const int gsw = lane & 31;
       uint32_t ga[16], gb[16];
       tmem_ld16_async(tmem + lane_base + 2 * NPM, ga);
 #pragma unroll
@@ -428,15 +418,30 @@ __global__ void __launch_bounds__(kThreads)
           uint32_t(&nxt)[16] = (c & 1) ? ga : gb;
           tmem_wait16(cur);
           if (c + 1 < nch) tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * (c + 1), nxt);
-          const unsigned int bits = static_cast<unsigned int>(mask >> (16 * c)) & 0xFFFFu;
-          if (bits) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if ((bits >> j) & 1u) {
-                const int k = Dn - ts.D[16 * c + j];
-                dst[offn + k] = scale * pc[offn + k] * __uint_as_float(cur[j]);
-              }
+          for (int j = 0; j < 16; ++j)
+            gdump[lane * 64 + ((16 * c + j) ^ gsw)] = __uint_as_float(cur[j]);
+        }
+      }
+      const bool isA = lane < N;
+      const int myn = isA ? lane : ((lane >= Np && lane < Np + N) ? lane - Np : -1);
+      if (myn >= 0) {
+        const int Dn = ts.D[myn], offn = ts.off[myn];
+        const float scale = isA ? ts.bbg[myn].x : 1.0f;
+        float* dst = isA ? aco : mco;
+        const int k0 = isA ? 1 : 0;  // A has strict ancestors only
+        if (Dn <= kRegPath) {
+#pragma unroll
+          for (int k = 0; k < kRegPath; ++k) {
+            if (k >= k0 && k < Dn) {
+              const int i = pidx[offn + k];
+              dst[offn + k] = scale * pc[offn + k] * gdump[lane * 64 + (i ^ gsw)];
             }
+          }
+        } else {
+          for (int k = k0; k < Dn; ++k) {
+            const int i = pidx[offn + k];
+            dst[offn + k] = scale * pc[offn + k] * gdump[lane * 64 + (i ^ gsw)];
           }
         }
       }
@@ -479,7 +484,9 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (wg == 0 && !fail) {
       named_bar_sync<1, 128>();
-      // ---- T rows (threads 0..N-1) and B rows (threads 64..64+N-1) together
+      // ---- T rows (threads 0..N-1) and B rows (threads 64..64+N-1) together;
+      //      the padding rows of [T;B] are zeroed by the lanes that own them
+      if ((t >= N && t < Np) || (t >= Np + N && t < 2 * Np)) zero_operand_row(thi, tlo, t);
       if (t < N) build_path_row(ts, t, t, pidx, aco, nullptr, xT, thi, tlo);
       if (t >= 64 && t - 64 < N) build_path_row(ts, t - 64, Np + t - 64, pidx, aco, mco, xB, thi, tlo);
     }
@@ -488,53 +495,56 @@ __global__ void __launch_bounds__(kThreads)
     fail = __syncthreads_or(fail);
     if (!fail && t == 0) {
       tc_fence_after_sync();
+      // [U | O] = W^T [T;B]^T as one N = 2Np product into the columns after the
+      // (consumed) Gram; S0 q_n stays in columns Np..2Np-1.
       const uint64_t da = smem_desc_sw128(smem_addr(s0), 1024);
-      const uint32_t id = idesc_bf16_f32(128, Np);
+      const uint32_t id = idesc_bf16_f32(128, 2 * Np);
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const uint32_t d = tmem + (part ? 2 * NPM : 0);
-        const uint32_t brow = part ? Np * 128 : 0;
-#pragma unroll
-        for (int s = 0; s < NPM / 16; ++s) {
-          if (s < nch) {
-            const uint32_t ko = s * 32;
-            const uint64_t whi = da + ((kWhiOff + ko) >> 4);
-            const uint64_t wlo = da + ((kWloOff + ko) >> 4);
-            const uint64_t thd = da + ((kThiOff + brow + ko) >> 4);
-            const uint64_t tld = da + ((kTloOff + brow + ko) >> 4);
-            mma_bf16(d, whi, thd, id, s ? 1u : 0u);
-            mma_bf16(d, wlo, thd, id, 1u);
-            mma_bf16(d, whi, tld, id, 1u);
-          }
+      for (int s = 0; s < NPM / 16; ++s) {
+        if (s < nch) {
+          const uint32_t ko = s * 32;
+          const uint64_t whi = da + ((kWhiOff + ko) >> 4);
+          const uint64_t wlo = da + ((kWloOff + ko) >> 4);
+          const uint64_t thd = da + ((kThiOff + ko) >> 4);
+          const uint64_t tld = da + ((kTloOff + ko) >> 4);
+          mma_bf16(tmem + 2 * NPM, whi, thd, id, s ? 1u : 0u);
+          mma_bf16(tmem + 2 * NPM, wlo, thd, id, 1u);
+          mma_bf16(tmem + 2 * NPM, whi, tld, id, 1u);
         }
       }
       mma_commit(&bars[6]);
       mma2_issued = true;
     }
-    if (!fail && !mbar_wait(&bars[6], 0)) fail = 1;
+    if (!fail && t == 0 && !mbar_wait(&bars[6], 0)) fail = 1;
     fail = __syncthreads_or(fail);
     if (!fail) {
       tc_fence_after_sync();
-      // ---- U[n] and o_n = gamma_n S0 q_n + O[n], column d = lane; warpgroups
-      //      take alternate 16-node chunks
+      // ---- U[n] and o_n = gamma_n S0 q_n + O[n], column d = lane; warpgroup
+      //      wg stores nodes 8wg..8wg+7 of every 16-node chunk
       float* og = b.o + (tok0 * H + h) * kDim + lane;
       float* ug = b.U + (tok0 * H + h) * kDim + lane;
       const int64_t stride = static_cast<int64_t>(H) * kDim;
-      for (int c = wg; c < nch; c += 2) {
+      for (int c = 0; c < nch; ++c) {
         uint32_t u[16], oo[16], pq[16];
-        tmem_ld16_async(tmem + lane_base + 16 * c, u);
-        tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * c, oo);
+        tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * c, u);
+        tmem_ld16_async(tmem + lane_base + 2 * NPM + Np + 16 * c, oo);
         tmem_ld16_async(tmem + lane_base + Np + 16 * c, pq);
         tmem_wait16(u);
         tmem_regs_ready(oo);
         tmem_regs_ready(pq);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        auto emit = [&](int j) {
           const int n = 16 * c + j;
           if (n < N) {
             ug[n * stride] = __uint_as_float(u[j]);
             og[n * stride] = fmaf(ts.gamma[n], __uint_as_float(pq[j]), __uint_as_float(oo[j]));
           }
+        };
+        if (wg == 0) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) emit(j);
+        } else {
+#pragma unroll
+          for (int j = 8; j < 16; ++j) emit(j);
         }
       }
       if (b.gamma != nullptr && t < N) b.gamma[(tok0 + t) * H + h] = ts.gamma[t];
