@@ -24,9 +24,9 @@ constexpr int kMaxVec = 16;          // float4 per thread for a 128 x 128 state
 __device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(float4* p, float4 v) { __stcs(p, v); }
 
-// Three resident blocks per SM (at most 85 registers a thread) keep three 64 KB
-// state blocks in flight per SM while the blocks' path walks overlap.
-__global__ void __launch_bounds__(kThreads, 3)
+// Two resident blocks per SM: the 16 float4 state registers per thread stay
+// in registers (a three-block cap spills them and was measured slower).
+__global__ void __launch_bounds__(kThreads, 2)
     commit_kernel(const treewy_batch b, const int32_t* __restrict__ accepted) {
   __shared__ int s_parent[kMaxNodes];
   __shared__ float s_alpha[kMaxNodes];
@@ -127,14 +127,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   const float ga = s_gamma_a;
 
   if (vec) {
-#pragma unroll
-    for (int m = 0; m < kMaxVec; ++m) {
-      acc[m].x *= ga;
-      acc[m].y *= ga;
-      acc[m].z *= ga;
-      acc[m].w *= ga;
-    }
-    // 3. rank-|path| update, kSeg path nodes per pass
+    // 3. rank-|path| update, kSeg path nodes per pass.  The path rows are
+    //    requested before the state registers are touched, so their round
+    //    trip overlaps the state loads still in flight.
     for (int seg = 0; seg < len; seg += kSeg) {
       const int ns = min(kSeg, len - seg);
       for (int e = t; e < ns * 128; e += kThreads) {
@@ -144,6 +139,15 @@ __global__ void __launch_bounds__(kThreads, 3)
         kf[j][x] = (x < dk) ? load_qkv(b.k, row * dk + x, bf16) : 0.f;
       }
       __syncthreads();
+      if (seg == 0) {
+#pragma unroll
+        for (int m = 0; m < kMaxVec; ++m) {
+          acc[m].x *= ga;
+          acc[m].y *= ga;
+          acc[m].z *= ga;
+          acc[m].w *= ga;
+        }
+      }
       if (dk == 128) {
         // float4 f = t + 256 m covers row d = t/32 + 8m, columns x..x+3 with
         // x = 4 (t % 32): the k chunk of a path node is loaded once per node
