@@ -72,7 +72,7 @@ class TreewyBatch(ctypes.Structure):
 
 _lib: Optional[ctypes.CDLL] = None
 
-ENTRY_POINTS = ("treewy_verify", "treewy_commit", "treewy_storeall_verify",
+ENTRY_POINTS = ("treewy_verify", "treewy_commit", "treewy_commit_verify", "treewy_storeall_verify",
                 "treewy_storeall_commit", "treewy_last_error", "treewy_version")
 
 
@@ -91,9 +91,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     vp = ctypes.c_void_p
     lib.treewy_verify.argtypes = [bp, vp]
     lib.treewy_commit.argtypes = [bp, vp, vp]
+    lib.treewy_commit_verify.argtypes = [bp, vp, bp, vp]
     lib.treewy_storeall_verify.argtypes = [bp, vp, vp]
     lib.treewy_storeall_commit.argtypes = [bp, vp, vp, vp]
-    for name in ("treewy_verify", "treewy_commit", "treewy_storeall_verify", "treewy_storeall_commit"):
+    for name in ("treewy_verify", "treewy_commit", "treewy_commit_verify", "treewy_storeall_verify",
+                 "treewy_storeall_commit"):
         getattr(lib, name).restype = ctypes.c_int
     lib.treewy_last_error.argtypes = []
     lib.treewy_last_error.restype = ctypes.c_char_p
@@ -142,6 +144,13 @@ def treewy_verify(batch: TreewyBatch, stream=None) -> None:
 def treewy_commit(batch: TreewyBatch, accepted, stream=None) -> None:
     """Rebuild the accepted state in place; ``accepted`` int32 [R] on the device."""
     _check(load().treewy_commit(ctypes.byref(batch), _ptr(accepted), _stream_handle(stream)))
+
+
+def treewy_commit_verify(prev: TreewyBatch, prev_accepted, next_batch: TreewyBatch,
+                         stream=None) -> None:
+    """Apply the previous round's commit inside this round's verification."""
+    _check(load().treewy_commit_verify(ctypes.byref(prev), _ptr(prev_accepted), ctypes.byref(next_batch),
+                                       _stream_handle(stream)))
 
 
 def treewy_storeall_verify(batch: TreewyBatch, snapshots, stream=None) -> None:

@@ -156,6 +156,45 @@ treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted, 
   return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_commit launch");
 }
 
+treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev_accepted,
+                                   const treewy_batch* next, cudaStream_t stream) {
+  g_last_error.clear();
+  treewy_status st = validate(next, true, true, true);
+  if (st != TREEWY_OK) return st;
+  st = validate(prev, false, false, true);
+  if (st != TREEWY_OK) return st;
+  if (prev->R != next->R || prev->H != next->H || prev->dk != next->dk || prev->dv != next->dv)
+    return fail(TREEWY_ERR_INVALID_ARG, "prev and next must have the same R, H, dk and dv");
+  if (prev->state != next->state || prev->state_slot != next->state_slot ||
+      prev->num_slots != next->num_slots)
+    return fail(TREEWY_ERR_INVALID_ARG, "prev and next must share the state pool and state_slot");
+  if (next->R == 0) return TREEWY_OK;
+  if (!prev->U) return fail(TREEWY_ERR_INVALID_ARG, "prev->U is NULL");
+  if (!prev_accepted) return fail(TREEWY_ERR_INVALID_ARG, "prev_accepted is NULL");
+  cudaError_t err;
+  if (use_tensor_cores(next) && next->T > 0 && prev->qkv_dtype == TREEWY_DTYPE_BF16) {
+    treewy::VerifyMaps maps;
+    st = make_maps(next, &maps);
+    if (st != TREEWY_OK) return st;
+    treewy::PrevRound pr;
+    pr.node_offset = prev->node_offset;
+    pr.parent = prev->parent;
+    pr.alpha = prev->alpha;
+    pr.k = prev->k;
+    pr.U = prev->U;
+    pr.accepted = prev_accepted;
+    pr.T = prev->T;
+    pr.max_nodes = prev->max_nodes;
+    pr.active = 1;
+    err = treewy::launch_commit_verify_tc(*next, pr, maps, next->max_nodes, stream);
+    return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_commit_verify launch");
+  }
+  // other shapes: the two kernels back to back on the same stream
+  err = treewy::launch_commit(*prev, prev_accepted, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "treewy_commit_verify (commit) launch");
+  return treewy_verify(next, stream);
+}
+
 treewy_status treewy_storeall_verify(const treewy_batch* batch, float* snapshots, cudaStream_t stream) {
   g_last_error.clear();
   treewy_status st = validate(batch, true, false, true);

@@ -21,10 +21,26 @@ struct VerifyMaps {
 size_t verify_generic_smem(int dk, int dv, int npm);
 cudaError_t launch_verify_generic(const treewy_batch& b, cudaStream_t stream);
 
+// The previous round whose commit is applied inside the next verification:
+// its trees, gates, keys and pseudo-values U, and the accepted nodes.
+struct PrevRound {
+  const int32_t* node_offset;
+  const int32_t* parent;
+  const float* alpha;
+  const void* k;  // bf16 [T][H][128]
+  const float* U;
+  const int32_t* accepted;
+  int64_t T;
+  int32_t max_nodes;
+  int32_t active;  // 0: plain verification
+};
+
 // npm: padded tree capacity (16, 32 or 64).
 size_t verify_tc_smem(int npm);
 cudaError_t launch_verify_tc(const treewy_batch& b, const VerifyMaps& maps, int npm,
                              cudaStream_t stream);
+cudaError_t launch_commit_verify_tc(const treewy_batch& next, const PrevRound& prev,
+                                    const VerifyMaps& maps, int npm, cudaStream_t stream);
 
 cudaError_t launch_commit(const treewy_batch& b, const int32_t* accepted, cudaStream_t stream);
 

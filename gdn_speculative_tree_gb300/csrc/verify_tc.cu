@@ -220,14 +220,34 @@ __device__ __forceinline__ void build_path_row(const TreeTC& ts, int n, int row,
   }
 }
 
-template <int NPM>
+// Previous-round data for the fused commit (shared memory; empty when the
+// kernel is not fused).
+constexpr int kPrevSeg = 8;  // path nodes of the previous round staged per pass
+template <bool FUSED>
+struct PrevSmem {
+  int a;
+};
+template <>
+struct PrevSmem<true> {
+  int parent[kMaxNodes];
+  float alpha[kMaxNodes];
+  float c[kMaxNodes];                // gamma_a / gamma_{path j} (alpha products)
+  uint8_t path[kMaxNodes];           // accepted node, its parent, ... (root last)
+  __nv_bfloat16 k[kPrevSeg][kDim];   // staged k rows of up to kPrevSeg path nodes
+  int tok0, N, a, len;
+  float gamma_a;
+};
+
+template <int NPM, bool FUSED>
 __global__ void __launch_bounds__(kThreads)
     verify_tc_kernel(const __grid_constant__ CUtensorMap map_s0,
                      const __grid_constant__ CUtensorMap map_k,
-                     const __grid_constant__ CUtensorMap map_q, const treewy_batch b) {
+                     const __grid_constant__ CUtensorMap map_q, const treewy_batch b,
+                     const PrevRound prev) {
   using C = TcCfg<NPM>;
   extern __shared__ unsigned char smem_raw[];
   __shared__ TreeTC ts;
+  __shared__ PrevSmem<FUSED> pv;
   // 0-3: S0 chunks, 4: K/Q, 5: S0 [K;Q]^T done, 6: second MMA done, 7: Gram done
   __shared__ __align__(8) uint64_t bars[8];
   __shared__ uint32_t tmem_holder;
@@ -269,17 +289,34 @@ __global__ void __launch_bounds__(kThreads)
     if (N < 0 || N > b.max_nodes) flags |= TREEWY_STATUS_TOO_MANY_NODES;
     else if (lo < 0 || static_cast<int64_t>(hi) > b.T) flags |= TREEWY_STATUS_BAD_TREE;
     if (slot < 0 || static_cast<int64_t>(slot) >= b.num_slots) flags |= TREEWY_STATUS_BAD_SLOT;
+    int pa = -1;
+    if constexpr (FUSED) {
+      // the previous round's accepted node and tree range for this request
+      pa = prev.accepted[r];
+      if (pa != -1) {
+        const int plo = prev.node_offset[r], phi = prev.node_offset[r + 1];
+        const int pn = phi - plo;
+        if (pn < 0 || pn > prev.max_nodes) flags |= TREEWY_STATUS_TOO_MANY_NODES;
+        else if (plo < 0 || static_cast<int64_t>(phi) > prev.T) flags |= TREEWY_STATUS_BAD_TREE;
+        if (pa < -1 || pa >= pn) flags |= TREEWY_STATUS_BAD_ACCEPTED;
+        pv.tok0 = plo;
+        pv.N = pn;
+      }
+      pv.a = flags ? -1 : pa;
+    }
     ts.tok0 = lo;
     ts.N = flags ? 0 : N;
     ts.slot = slot;
     ts.flags = flags;
-    if (flags == 0 && N > 0) {
+    if (flags == 0 && (N > 0 || pa >= 0)) {
       const int y = (slot * H + h) * kDim;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         mbar_arrive_expect_tx(&bars[c], kS0ChunkBytes);
         tma_load_2d(s0 + c * kS0ChunkBytes, &map_s0, &bars[c], 32 * c, y);
       }
+    }
+    if (flags == 0 && N > 0) {
       const int N8 = (N + 7) & ~7;
       const int Np = (N + 15) & ~15;
       // 2 tensors x 2 column chunks x N8 rows x 128 bytes
@@ -305,6 +342,9 @@ __global__ void __launch_bounds__(kThreads)
   const int Np = (N + 15) & ~15;
   const int nch = Np / 16;
   const bool issued = (ts.flags == 0 && N > 0);
+  int commit_a = -1;  // accepted node of the previous round still to be applied
+  if constexpr (FUSED) commit_a = pv.a;
+  const bool have_s0 = issued || commit_a >= 0;
   const int64_t tok0 = ts.tok0;
 
   // Column `lane` of V for the warpgroup that builds W.  Each thread loads the
@@ -326,6 +366,61 @@ __global__ void __launch_bounds__(kThreads)
 
   bool bad_tree = false;
   if (issued) bad_tree = !prepare_tree(ts, pidx, pc, b, h);
+
+  // Fused commit: validate the previous tree, walk the accepted node's path and
+  // stage its first segment (k rows in shared memory, c_j u_j[lane] in registers).
+  bool bad_prev = false;
+  float cu[kPrevSeg];
+#pragma unroll
+  for (int j = 0; j < kPrevSeg; ++j) cu[j] = 0.f;
+  auto stage_prev = [&](int seg) {
+    if constexpr (FUSED) {
+      const int ns = min(kPrevSeg, pv.len - seg);
+      const uint32_t* kg = reinterpret_cast<const uint32_t*>(prev.k);
+      for (int e = t; e < ns * (kDim / 2); e += kThreads) {
+        const int j = e / (kDim / 2), w = e - j * (kDim / 2);
+        const int64_t row = (static_cast<int64_t>(pv.tok0) + pv.path[seg + j]) * H + h;
+        reinterpret_cast<uint32_t*>(&pv.k[j][0])[w] = __ldg(kg + row * (kDim / 2) + w);
+      }
+#pragma unroll
+      for (int j = 0; j < kPrevSeg; ++j) {
+        cu[j] = 0.f;
+        if (j < ns) {
+          const int64_t row = (static_cast<int64_t>(pv.tok0) + pv.path[seg + j]) * H + h;
+          cu[j] = pv.c[seg + j] * __ldg(prev.U + row * kDim + lane);
+        }
+      }
+    }
+  };
+  if constexpr (FUSED) {
+    if (commit_a >= 0) {
+      bool bad = false;
+      if (t < pv.N) {
+        const int64_t row = static_cast<int64_t>(pv.tok0) + t;
+        const int p = __ldg(prev.parent + row);
+        bad = !(p >= -1 && p < t);
+        pv.parent[t] = p;
+        pv.alpha[t] = __ldg(prev.alpha + row * H + h);
+      }
+      bad_prev = __syncthreads_or(bad);
+      if (!bad_prev && t == 0) {
+        int len = 0;
+        float c = 1.0f;
+        for (int cur = commit_a; cur >= 0; cur = pv.parent[cur]) {
+          pv.path[len] = static_cast<uint8_t>(cur);
+          pv.c[len] = c;
+          c *= pv.alpha[cur];
+          ++len;
+        }
+        pv.len = len;
+        pv.gamma_a = c;
+      }
+      __syncthreads();
+      if (!bad_prev) stage_prev(0);
+      __syncthreads();
+    }
+  }
+  const bool commit_now = commit_a >= 0 && !bad_prev;
   if (wg == 1) {
     const int par = lane & 1;
 #pragma unroll
@@ -346,18 +441,67 @@ __global__ void __launch_bounds__(kThreads)
   // `lane`.  Waits on an mbarrier are done by one thread per warpgroup; the
   // others sleep at a hardware barrier instead of spinning.
   int fail = 0;
-  if (issued) {
+  if (have_s0 && !bad_prev) {
     if (lane == 0) fail = !(mbar_wait(&bars[2 * wg], 0) && mbar_wait(&bars[2 * wg + 1], 0));
     fail = wg ? named_bar_or<2, 128>(fail) : named_bar_or<1, 128>(fail);
-    if (!fail && !bad_tree) {
-      convert_row_hilo(s0 + (2 * wg) * kS0ChunkBytes + lane * 128, lane & 7);
-      convert_row_hilo(s0 + (2 * wg + 1) * kS0ChunkBytes + lane * 128, lane & 7);
-    }
-    fence_proxy_async_smem();
   }
+  if constexpr (FUSED) {
+    // S_a = gamma_a S0 + sum_j c_j u_j k_j^T on this thread's own fp32 row
+    // segments (chunks 2wg, 2wg+1 of row `lane`), written back to the pool once.
+    if (commit_now && !__syncthreads_or(fail)) {
+      const float ga = pv.gamma_a;
+      for (int seg = 0; seg < pv.len; seg += kPrevSeg) {
+        if (seg > 0) {
+          __syncthreads();
+          stage_prev(seg);
+          __syncthreads();
+        }
+        const int ns = min(kPrevSeg, pv.len - seg);
+        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+          unsigned char* row = s0 + c * kS0ChunkBytes + lane * 128;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            float4 x = *reinterpret_cast<const float4*>(row + ((g ^ (lane & 7)) << 4));
+            if (seg == 0) {
+              x.x *= ga;
+              x.y *= ga;
+              x.z *= ga;
+              x.w *= ga;
+            }
+            const int col = 32 * c + 4 * g;
+#pragma unroll
+            for (int j = 0; j < kPrevSeg; ++j) {
+              if (j < ns) {
+                const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.k[j][col]));
+                const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.k[j][col + 2]));
+                x.x = fmaf(cu[j], k01.x, x.x);
+                x.y = fmaf(cu[j], k01.y, x.y);
+                x.z = fmaf(cu[j], k23.x, x.z);
+                x.w = fmaf(cu[j], k23.y, x.w);
+              }
+            }
+            *reinterpret_cast<float4*>(row + ((g ^ (lane & 7)) << 4)) = x;
+          }
+        }
+      }
+      float* srow = b.state + ((static_cast<int64_t>(ts.slot) * H + h) * kDim + lane) * kDim;
+      for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
+        const unsigned char* row = s0 + c * kS0ChunkBytes + lane * 128;
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<float4*>(srow + 32 * c + 4 * g) =
+              *reinterpret_cast<const float4*>(row + ((g ^ (lane & 7)) << 4));
+      }
+    }
+  }
+  if (issued && !fail && !bad_tree && !bad_prev) {
+    convert_row_hilo(s0 + (2 * wg) * kS0ChunkBytes + lane * 128, lane & 7);
+    convert_row_hilo(s0 + (2 * wg + 1) * kS0ChunkBytes + lane * 128, lane & 7);
+  }
+  fence_proxy_async_smem();
   fail = __syncthreads_or(fail);
 
-  const bool work = issued && !bad_tree;
+  const bool work = issued && !bad_tree && !bad_prev;
   if (work && !fail && t == 0) {
     if (!mbar_wait(&bars[4], 0)) {
       s_fail = 1;
@@ -553,11 +697,13 @@ __global__ void __launch_bounds__(kThreads)
 
   if (t == 0) {
     int bits = (fail ? kStatusTimeout : 0);
-    if (h == 0) bits |= ts.flags | (bad_tree ? TREEWY_STATUS_BAD_TREE : 0);
+    if (h == 0) bits |= ts.flags | ((bad_tree || bad_prev) ? TREEWY_STATUS_BAD_TREE : 0);
     if (bits) atomicOr(b.status + r, bits);
+    // No async copy or MMA may still target this CTA's memory at exit.
+    if (have_s0)
+      for (int i = 0; i < 4; ++i) mbar_wait(&bars[i], 0);
     if (issued) {
-      // No async copy or MMA may still target this CTA's memory at exit.
-      for (int i = 0; i < 5; ++i) mbar_wait(&bars[i], 0);
+      mbar_wait(&bars[4], 0);
       if (mma_issued) {
         mbar_wait(&bars[5], 0);
         mbar_wait(&bars[7], 0);
@@ -573,14 +719,16 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <int NPM>
-cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, cudaStream_t stream) {
+template <int NPM, bool FUSED>
+cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, const PrevRound& prev,
+                       cudaStream_t stream) {
   static cudaError_t attr = cudaFuncSetAttribute(
-      verify_tc_kernel<NPM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      verify_tc_kernel<NPM, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       static_cast<int>(TcCfg<NPM>::kDynSmem));
   if (attr != cudaSuccess) return attr;
   const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
-  verify_tc_kernel<NPM><<<grid, kThreads, TcCfg<NPM>::kDynSmem, stream>>>(m.s0, m.k, m.q, b);
+  verify_tc_kernel<NPM, FUSED><<<grid, kThreads, TcCfg<NPM>::kDynSmem, stream>>>(m.s0, m.k, m.q, b,
+                                                                                 prev);
   return cudaGetLastError();
 }
 
@@ -594,9 +742,17 @@ size_t verify_tc_smem(int npm) {
 
 cudaError_t launch_verify_tc(const treewy_batch& b, const VerifyMaps& maps, int npm,
                              cudaStream_t stream) {
-  if (npm <= 16) return launch_npm<16>(b, maps, stream);
-  if (npm <= 32) return launch_npm<32>(b, maps, stream);
-  return launch_npm<64>(b, maps, stream);
+  const PrevRound none{};
+  if (npm <= 16) return launch_npm<16, false>(b, maps, none, stream);
+  if (npm <= 32) return launch_npm<32, false>(b, maps, none, stream);
+  return launch_npm<64, false>(b, maps, none, stream);
+}
+
+cudaError_t launch_commit_verify_tc(const treewy_batch& next, const PrevRound& prev,
+                                    const VerifyMaps& maps, int npm, cudaStream_t stream) {
+  if (npm <= 16) return launch_npm<16, true>(next, maps, prev, stream);
+  if (npm <= 32) return launch_npm<32, true>(next, maps, prev, stream);
+  return launch_npm<64, true>(next, maps, prev, stream);
 }
 
 }  // namespace treewy

@@ -160,6 +160,29 @@ treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted,
                             cudaStream_t stream);
 
 /*
+ * treewy_commit_verify -- the previous round's commit fused into this round's
+ * verification (the deferred state write that the paper's §6 and the review's
+ * §7(c)(3) point to: write the accepted state once, inside the next pass that
+ * reads it).
+ *
+ * For every request r, state[state_slot[r]] holds S0 of the previous round;
+ * `prev` describes that round (node_offset, parent, alpha, k and U from its
+ * treewy_verify; q, v, o, beta are not read) and prev_accepted its accepted
+ * nodes (device int32 [R], -1 = nothing accepted).  The kernel rebuilds
+ * S_a = gamma_a S0 + sum_{i on path(a)} (gamma_a/gamma_i) u_i k_i^T on chip,
+ * writes it back to the state block once, and verifies `next` from it: the
+ * results equal treewy_commit(prev, prev_accepted) followed by
+ * treewy_verify(next), with one state read per head instead of two.  A request
+ * with no node in `next` still gets its commit.  prev and next must have the
+ * same R, H, dk, dv, state pool pointer, num_slots and state_slot pointer.
+ * Errors in the previous round's tree or accepted index set status bits in
+ * next->status and skip the request entirely (state and outputs untouched).
+ * Shapes outside the tensor-core path run the two kernels back to back.
+ */
+treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev_accepted,
+                                   const treewy_batch* next, cudaStream_t stream);
+
+/*
  * treewy_storeall_verify -- the snapshot-per-node comparator ("storeall", the
  * full-state snapshotting of paper §2, approach (i)).
  *

@@ -106,3 +106,21 @@ def test_empty_batch_is_a_no_op(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         binding.load(str(tmp_path / "nope.so"))
+
+
+def test_commit_verify_rejects_inconsistent_rounds(lib):
+    prev, nxt = _valid_batch(), _valid_batch()
+    prev.R = 3
+    assert lib.treewy_commit_verify(ctypes.byref(prev), 0x10000, ctypes.byref(nxt), None) == \
+        binding.TREEWY_ERR_INVALID_ARG
+    assert b"same R" in lib.treewy_last_error()
+    prev = _valid_batch()
+    prev.state = 0x20000
+    assert lib.treewy_commit_verify(ctypes.byref(prev), 0x10000, ctypes.byref(nxt), None) == \
+        binding.TREEWY_ERR_INVALID_ARG
+    assert b"state pool" in lib.treewy_last_error()
+    prev = _valid_batch()
+    assert lib.treewy_commit_verify(ctypes.byref(prev), None, ctypes.byref(nxt), None) == \
+        binding.TREEWY_ERR_INVALID_ARG
+    assert lib.treewy_commit_verify(None, 0x10000, ctypes.byref(nxt), None) == \
+        binding.TREEWY_ERR_INVALID_ARG

@@ -1,0 +1,152 @@
+"""GPU parity of treewy_commit_verify (the previous round's commit fused into the
+next round's verification) against the oracle run as commit-then-verify on the
+same seeded inputs, and against the two separate library calls.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gdn_speculative_tree_gb300 import binding
+from gdn_speculative_tree_gb300 import workloads as wl
+from oracle import gdn_tree_oracle as orc
+from tests.gpu_helpers import np32
+
+pytestmark = pytest.mark.gpu
+
+
+def rounds(prev_trees, next_trees, accepted, H=4, dk=128, dv=128, qkv="bf16", seed=41):
+    """Two rounds over the same requests sharing one state pool."""
+    R = len(prev_trees)
+    assert len(next_trees) == R
+    prev = wl.assemble([np.asarray(t, np.int32) for t in prev_trees], np.asarray(accepted, np.int32),
+                       H, dk, dv, qkv, 0.05, (0.9, 0.999), ("sigmoid",), seed=seed, max_nodes=64,
+                       extra_slots=3).to("cuda")
+    nxt = wl.assemble([np.asarray(t, np.int32) for t in next_trees], np.full(R, -1, np.int32),
+                      H, dk, dv, qkv, 0.05, (0.9, 0.999), ("sigmoid",), seed=seed + 1, max_nodes=64,
+                      extra_slots=3).to("cuda")
+    nxt.state = prev.state
+    nxt.state_slot = prev.state_slot
+    return prev, nxt
+
+
+def random_tree(rng, n):
+    return np.array([-1] + [int(rng.integers(-1, i)) for i in range(1, n)], np.int32) if n else \
+        np.zeros(0, np.int32)
+
+
+def oracle_two_rounds(prev, nxt, S0_pool, r):
+    """Oracle: S_a from the previous round's tree, then the next round from S_a."""
+    slot = int(prev.state_slot[r])
+    S0 = np32(S0_pool[slot])
+    pn = prev.node_offset.cpu().numpy()
+    lo, hi = int(pn[r]), int(pn[r + 1])
+    ref_prev = orc.verify_request(S0, prev.parent[lo:hi].cpu().numpy(), np32(prev.q[lo:hi]),
+                                  np32(prev.k[lo:hi]), np32(prev.v[lo:hi]), np32(prev.alpha[lo:hi]),
+                                  np32(prev.beta[lo:hi]))
+    Sa = orc.commit_request(S0, ref_prev, int(prev.accepted[r]))
+    nn = nxt.node_offset.cpu().numpy()
+    lo2, hi2 = int(nn[r]), int(nn[r + 1])
+    ref_next = orc.verify_request(Sa, nxt.parent[lo2:hi2].cpu().numpy(), np32(nxt.q[lo2:hi2]),
+                                  np32(nxt.k[lo2:hi2]), np32(nxt.v[lo2:hi2]), np32(nxt.alpha[lo2:hi2]),
+                                  np32(nxt.beta[lo2:hi2]))
+    return Sa, ref_next, (lo2, hi2)
+
+
+def run_fused(prev, nxt):
+    tp = binding.TreeVerifier(prev)
+    tp.verify()
+    torch.cuda.synchronize()
+    assert not tp.status.any()
+    S0_pool = prev.state.cpu()
+    tn = binding.TreeVerifier(nxt)
+    binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
+    torch.cuda.synchronize()
+    return tp, tn, S0_pool
+
+
+def check(prev, nxt, tn, S0_pool, requests):
+    o = np32(tn.o)
+    U = np32(tn.U)
+    o_err = o_max = s_err = s_max = u_err = u_max = 0.0
+    for r in requests:
+        Sa, ref, (lo, hi) = oracle_two_rounds(prev, nxt, S0_pool, r)
+        S_gpu = np32(prev.state[int(prev.state_slot[r])])
+        s_err = max(s_err, float(np.abs(S_gpu - Sa).max()))
+        s_max = max(s_max, float(np.abs(Sa).max()))
+        if hi > lo:
+            o_err = max(o_err, float(np.abs(o[lo:hi] - ref.o).max()))
+            o_max = max(o_max, float(np.abs(ref.o).max()))
+            u_err = max(u_err, float(np.abs(U[lo:hi] - ref.U).max()))
+            u_max = max(u_max, float(np.abs(ref.U).max()))
+    assert s_err <= 1e-3 * s_max, (s_err, s_max)
+    assert o_err <= 2e-3 * o_max, (o_err, o_max)
+    assert u_err <= 2e-3 * u_max, (u_err, u_max)
+
+
+def test_fused_matches_oracle_mixed(cuda_lib):
+    rng = np.random.default_rng(61)
+    prev_trees = [random_tree(rng, n) for n in (12, 40, 64, 5, 30, 17, 9, 64)]
+    prev_trees[7] = wl.chain_parents(64)  # a 64-long accepted path (several staged segments)
+    next_trees = [random_tree(rng, n) for n in (20, 0, 33, 64, 1, 17, 48, 10)]
+    accepted = [5, 39, -1, 4, 29, 0, 8, 63]
+    prev, nxt = rounds(prev_trees, next_trees, accepted)
+    tp, tn, S0_pool = run_fused(prev, nxt)
+    assert not tn.status.any(), tn.status.tolist()
+    check(prev, nxt, tn, S0_pool, range(len(prev_trees)))
+
+
+def test_fused_matches_separate_calls(cuda_lib):
+    cfg = wl.CONFIGS["wide"]
+    trees, acc = wl.make_trees(cfg, R=10)
+    rng = np.random.default_rng(3)
+    nxt_trees = [random_tree(rng, int(rng.integers(16, 65))) for _ in range(10)]
+    prev_a, nxt_a = rounds(trees, nxt_trees, acc, H=8, seed=7)
+    prev_b, nxt_b = rounds(trees, nxt_trees, acc, H=8, seed=7)
+    # fused
+    tp, tn, _ = run_fused(prev_a, nxt_a)
+    # separate: verify(prev), commit(prev), verify(next)
+    tpb = binding.TreeVerifier(prev_b)
+    tpb.verify()
+    tpb.commit()
+    tnb = binding.TreeVerifier(nxt_b)
+    tnb.verify()
+    torch.cuda.synchronize()
+    assert not tn.status.any() and not tnb.status.any()
+    ds = (prev_a.state - prev_b.state).abs().max().item()
+    assert ds <= 1e-4 * prev_b.state.abs().max().item(), ds
+    do = (tn.o - tnb.o).abs().max().item()
+    assert do <= 1e-3 * tnb.o.abs().max().item(), do
+
+
+def test_fused_bad_previous_round_skips_request(cuda_lib):
+    rng = np.random.default_rng(5)
+    prev_trees = [random_tree(rng, 10), random_tree(rng, 12), random_tree(rng, 8)]
+    next_trees = [random_tree(rng, 9), random_tree(rng, 11), random_tree(rng, 7)]
+    prev, nxt = rounds(prev_trees, next_trees, [3, 12, 2])   # request 1: accepted outside its tree
+    tp = binding.TreeVerifier(prev)
+    tp.verify()
+    torch.cuda.synchronize()
+    S_before = prev.state.clone()
+    tn = binding.TreeVerifier(nxt)
+    tn.o.fill_(float("nan"))
+    binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
+    torch.cuda.synchronize()
+    st = tn.status.cpu().tolist()
+    assert st[0] == 0 and st[2] == 0
+    assert st[1] & binding.STATUS_BAD_ACCEPTED
+    s1 = int(prev.state_slot[1])
+    assert torch.equal(prev.state[s1], S_before[s1])
+    node = nxt.node_offset.cpu().tolist()
+    assert torch.isnan(tn.o[node[1]:node[2]]).all()
+    check(prev, nxt, tn, S_before.cpu(), [0, 2])
+
+
+@pytest.mark.parametrize("dk,dv,qkv", [(128, 128, "f32"), (64, 48, "bf16")])
+def test_fused_fallback_shapes(cuda_lib, dk, dv, qkv):
+    rng = np.random.default_rng(dk)
+    prev_trees = [random_tree(rng, n) for n in (7, 20, 3)]
+    next_trees = [random_tree(rng, n) for n in (5, 0, 9)]
+    prev, nxt = rounds(prev_trees, next_trees, [6, 19, -1], H=2, dk=dk, dv=dv, qkv=qkv)
+    tp, tn, S0_pool = run_fused(prev, nxt)
+    assert not tn.status.any()
+    check(prev, nxt, tn, S0_pool, range(3))
