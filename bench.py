@@ -343,6 +343,7 @@ def run_ours(args, world, rank, local):
     # end to end through the public API: per step, pinned host inputs of all
     # layers copied in, verify + commit, outputs o of all layers copied out
     e2e = run_e2e(args, work, stream, world)
+    fused = run_fused(args, work, stream, world, vb, cb, plen, H, peak)
 
     storeall = run_storeall(work[0], stream) if rank == 0 and not args.no_storeall else None
     cpu = cpu_baseline(args.cpu_requests) if rank == 0 and args.cpu_requests > 0 else None
@@ -369,11 +370,56 @@ def run_ours(args, world, rank, local):
         "head_node_verifies_per_s": nodes * H / (v_avg * 1e-3),
         "gpu_launches": 2 * layers * args.steps,
         "e2e": e2e,
+        "fused": fused,
         "storeall": storeall,
         "cpu_baseline": cpu,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
+
+
+def run_fused(args, work, stream, world, vb, cb, plen, H, peak):
+    """Steady-state step with the previous round's commit fused into the verify:
+    30 treewy_commit_verify launches per step (the same work per step as
+    30 verify + 30 commit launches once the loop runs)."""
+    from gdn_speculative_tree_gb300 import binding
+
+    def step(ev=None):
+        for l, tv in enumerate(work):
+            if ev is not None:
+                ev[l][0].record(stream)
+            binding.treewy_commit_verify(tv.batch, tv.wl.accepted, tv.batch, stream)
+            if ev is not None:
+                ev[l][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in work] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for ev in events:
+        step(ev)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end) / args.steps, world)
+    lay = [a.elapsed_time(b) for ev in events for a, b in ev]
+    layer_ms = sum(lay) / len(lay)
+    for tv in work:
+        if tv.status.any().item():
+            raise SystemExit(f"device status bits set in the fused step: {tv.status.unique().tolist()}")
+    nodes = sum_over_ranks(int(work[0].wl.node_offset[-1]), world)
+    # one state read per committing head is shared by the commit and the verify
+    fb = vb + cb - int(H * 65536 * int((plen > 0).sum()))
+    return {"value": nodes / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "layer_ms": layer_ms,
+            "algorithmic_bytes_per_launch": fb, "achieved_gbs": fb / (layer_ms * 1e-3) / 1e9,
+            "frac": fb / (layer_ms * 1e-3) / 1e9 / peak,
+            "note": "treewy_commit_verify per layer: commit of the previous round inside this "
+                    "round's verify (one state read per head instead of two)"}
 
 
 def run_e2e(args, work, stream, world):
@@ -458,6 +504,114 @@ def run_storeall(tv, stream):
             "state_blocks_per_request": "N+1 (treewy: 1)"}
 
 
+# ---------------------------------------------------------------- studies
+
+def _median_ms(fn, stream, reps, before=None):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        if before is not None:
+            before()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def study_widths(args, local):
+    """Verify and commit cost against tree width: full width trees of the
+    shapes (w1, w2, w3), w in 1..3 (N = w1 + w1 w2 + w1 w2 w3), 256 requests x
+    32 heads, dk = dv = 128, beside the storeall comparator on the same inputs.
+    Every launch's inputs exceed L2; the state is restored before each commit."""
+    from gdn_speculative_tree_gb300 import binding
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = read_peaks()
+    base = wl.CONFIGS[CONFIG_NAME].with_(tree="widths", accepted="uniform")
+    rows = []
+    shapes = sorted(((a, b, c) for a in (1, 2, 3) for b in (1, 2, 3) for c in (1, 2, 3)),
+                    key=lambda s: (s[0] + s[0] * s[1] + s[0] * s[1] * s[2], s))
+    for shape in shapes:
+        cfg = base.with_(widths=shape)
+        w = wl.generate(cfg, device=torch.device("cuda", local))
+        tv = binding.TreeVerifier(w)
+        S0 = w.state.clone()
+        Ns, plen = tree_stats(w.trees, w.accepted.cpu().numpy())
+        vb, cb = verify_bytes(Ns, w.H), commit_bytes(plen, w.H)
+        for _ in range(args.warmup):
+            tv.verify(stream)
+        v_ms = _median_ms(lambda: tv.verify(stream), stream, 20)
+        c_ms = _median_ms(lambda: tv.commit(None, stream), stream, 20,
+                          before=lambda: w.state.copy_(S0))
+        w.state.copy_(S0)
+        if tv.status.any().item():
+            raise SystemExit(f"device status bits set for widths {shape}")
+        row = {"widths": list(shape), "N": int(Ns[0]), "depth": 3,
+               "verify_us": v_ms * 1e3, "verify_gbs": vb / (v_ms * 1e-3) / 1e9,
+               "verify_frac": vb / (v_ms * 1e-3) / 1e9 / peak,
+               "verify_us_per_node": v_ms * 1e3 / int(Ns[0]),
+               "commit_us": c_ms * 1e3, "commit_frac": cb / (c_ms * 1e-3) / 1e9 / peak}
+        sa = run_storeall(tv, stream)
+        if "verify_ms_per_layer" in sa:
+            row["storeall_verify_us"] = sa["verify_ms_per_layer"] * 1e3
+            row["storeall_commit_us"] = sa["commit_ms_per_layer"] * 1e3
+            row["treewy_speedup_verify"] = sa["verify_ms_per_layer"] / v_ms
+        rows.append(row)
+        del tv, w, S0
+        torch.cuda.empty_cache()
+    print(json.dumps({"study": "verify cost vs tree width", "peak_gbs": peak,
+                      "peak_kind": f"{peak_kind} hbm_gbs", "R": base.R, "H": base.H,
+                      "rows": rows}), flush=True)
+
+
+def study_graph(args, local):
+    """Launch overhead on the chain workload (64 requests x 32 heads, chains of
+    4): 30 layers of verify + commit issued eagerly vs replayed as one CUDA
+    graph captured from the same calls."""
+    from gdn_speculative_tree_gb300 import binding
+    dev = torch.device("cuda", local)
+    cfg = wl.CONFIGS["chain"]
+    layers = args.layers
+    work = [binding.TreeVerifier(wl.generate(cfg, layer=l, device=dev)) for l in range(layers)]
+    stream = torch.cuda.Stream(device=dev)
+    nodes = int(work[0].wl.node_offset[-1])
+
+    def step():
+        for tv in work:
+            tv.verify(stream)
+        for tv in work:
+            tv.commit(None, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    reps = max(args.steps, 20)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        eager_ms = _median_ms(step, stream, reps)
+    host_eager = (time.perf_counter() - t0) / reps * 1e3
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        graph_ms = _median_ms(g.replay, stream, reps)
+    for tv in work:
+        if tv.status.any().item():
+            raise SystemExit("device status bits set in the graph study")
+    print(json.dumps({"study": "CUDA-graph capture of batched tree verify+commit",
+                      "workload": f"chain of 4, {cfg.R} requests x {cfg.H} heads, {layers} layers",
+                      "launches_per_step": 2 * layers, "eager_ms_per_step": eager_ms,
+                      "graph_ms_per_step": graph_ms, "eager_host_ms_per_step": host_eager,
+                      "eager_nodes_per_s": nodes * 1e3 / eager_ms,
+                      "graph_nodes_per_s": nodes * 1e3 / graph_ms,
+                      "graph_speedup": eager_ms / graph_ms}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -467,12 +621,22 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--cpu-requests", type=int, default=64)
     ap.add_argument("--no-storeall", action="store_true")
+    ap.add_argument("--study", choices=["widths", "graph"],
+                    help="print one study line instead of the benchmark line (1 GPU)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup(args.gpus)
     try:
-        if args.impl == "reference":
+        if args.study is not None:
+            if rank == 0:
+                from gdn_speculative_tree_gb300 import binding
+                from gdn_speculative_tree_gb300 import build as _build
+                torch.cuda.set_device(local)
+                _build.build()
+                binding.load()
+                {"widths": study_widths, "graph": study_graph}[args.study](args, local)
+        elif args.impl == "reference":
             run_reference(args, world, rank)
         else:
             run_ours(args, world, rank, local)

@@ -282,19 +282,23 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
     fence_mbarrier_init();
     s_fail = 0;
+    // every metadata load of this CTA is independent: one memory round trip
     const int lo = b.node_offset[r], hi = b.node_offset[r + 1];
     const int slot = b.state_slot[r];
+    int pa = -1, plo = 0, phi = 0;
+    if constexpr (FUSED) {
+      pa = prev.accepted[r];
+      plo = prev.node_offset[r];
+      phi = prev.node_offset[r + 1];
+    }
     int flags = 0;
     const int N = hi - lo;
     if (N < 0 || N > b.max_nodes) flags |= TREEWY_STATUS_TOO_MANY_NODES;
     else if (lo < 0 || static_cast<int64_t>(hi) > b.T) flags |= TREEWY_STATUS_BAD_TREE;
     if (slot < 0 || static_cast<int64_t>(slot) >= b.num_slots) flags |= TREEWY_STATUS_BAD_SLOT;
-    int pa = -1;
     if constexpr (FUSED) {
       // the previous round's accepted node and tree range for this request
-      pa = prev.accepted[r];
       if (pa != -1) {
-        const int plo = prev.node_offset[r], phi = prev.node_offset[r + 1];
         const int pn = phi - plo;
         if (pn < 0 || pn > prev.max_nodes) flags |= TREEWY_STATUS_TOO_MANY_NODES;
         else if (plo < 0 || static_cast<int64_t>(phi) > prev.T) flags |= TREEWY_STATUS_BAD_TREE;
@@ -364,6 +368,18 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
 
+  // the previous tree's parents and gates, requested before this tree's so
+  // that both round trips overlap
+  int prev_p = -1;
+  float prev_al = 0.f;
+  if constexpr (FUSED) {
+    if (commit_a >= 0 && t < pv.N) {
+      const int64_t row = static_cast<int64_t>(pv.tok0) + t;
+      prev_p = __ldg(prev.parent + row);
+      prev_al = __ldg(prev.alpha + row * H + h);
+    }
+  }
+
   bool bad_tree = false;
   if (issued) bad_tree = !prepare_tree(ts, pidx, pc, b, h);
 
@@ -396,11 +412,9 @@ __global__ void __launch_bounds__(kThreads)
     if (commit_a >= 0) {
       bool bad = false;
       if (t < pv.N) {
-        const int64_t row = static_cast<int64_t>(pv.tok0) + t;
-        const int p = __ldg(prev.parent + row);
-        bad = !(p >= -1 && p < t);
-        pv.parent[t] = p;
-        pv.alpha[t] = __ldg(prev.alpha + row * H + h);
+        bad = !(prev_p >= -1 && prev_p < t);
+        pv.parent[t] = prev_p;
+        pv.alpha[t] = prev_al;
       }
       bad_prev = __syncthreads_or(bad);
       if (!bad_prev && t == 0) {
@@ -484,14 +498,19 @@ __global__ void __launch_bounds__(kThreads)
           }
         }
       }
-      float* srow = b.state + ((static_cast<int64_t>(ts.slot) * H + h) * kDim + lane) * kDim;
-      for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-        const unsigned char* row = s0 + c * kS0ChunkBytes + lane * 128;
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<float4*>(srow + 32 * c + 4 * g) =
-              *reinterpret_cast<const float4*>(row + ((g ^ (lane & 7)) << 4));
+      // S_a goes back to the pool by two bulk tensor stores per warpgroup
+      // (the tile layout in shared memory is the one the loads produced);
+      // the chunks are converted in place only after the stores have read them
+      fence_proxy_async_smem();
+      if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+      if (lane == 0) {
+        const int y = (ts.slot * H + h) * kDim;
+        tma_store_2d(&map_s0, s0 + (2 * wg) * kS0ChunkBytes, 32 * (2 * wg), y);
+        tma_store_2d(&map_s0, s0 + (2 * wg + 1) * kS0ChunkBytes, 32 * (2 * wg + 1), y);
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
+      if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
     }
   }
   if (issued && !fail && !bad_tree && !bad_prev) {
