@@ -46,7 +46,8 @@ UNIT = "nodes/s"
 CONFIG_NAME = "wide"
 LAYERS = 30
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_tc_wide_traffic.json")
-KERNEL_SOURCES = ["gdn_speculative_tree_gb300/csrc/verify_tc.cu",
+KERNEL_SOURCES = ["gdn_speculative_tree_gb300/csrc/verify_tc.cuh",
+                  "gdn_speculative_tree_gb300/csrc/verify_tc.cu",
                   "gdn_speculative_tree_gb300/csrc/treewy_device.cuh"]
 
 
@@ -83,17 +84,18 @@ def tree_stats(trees, accepted):
     return np.array(Ns), np.array(plen)
 
 
-def verify_bytes(Ns, H):
-    # per (request, head): S0 read 64 KiB + per node q,k,v (768 B bf16), alpha,
-    # beta (8 B), o and U written (1024 B fp32), gamma (4 B); parents once per request
-    return int(H * (65536 * len(Ns) + 1804 * Ns.sum()) + 4 * Ns.sum())
+def verify_bytes(Ns, H, state_bytes=65536):
+    # per (request, head): S0 read (64 KiB fp32 / 32 KiB bf16) + per node q,k,v
+    # (768 B bf16), alpha, beta (8 B), o and U written (1024 B fp32), gamma
+    # (4 B); parents once per request
+    return int(H * (state_bytes * len(Ns) + 1804 * Ns.sum()) + 4 * Ns.sum())
 
 
-def commit_bytes(plen, H):
-    # per (request, head) with an accepted node: state read + written (128 KiB)
+def commit_bytes(plen, H, state_bytes=65536):
+    # per (request, head) with an accepted node: state read + written
     # + per path node u (512 B), k (256 B), alpha (4 B); nothing when a = -1
     live = plen > 0
-    return int(H * (131072 * live.sum() + 772 * plen.sum()))
+    return int(H * (2 * state_bytes * live.sum() + 772 * plen.sum()))
 
 
 # ---------------------------------------------------------------- clocks
@@ -612,6 +614,66 @@ def study_graph(args, local):
                       "graph_speedup": eager_ms / graph_ms}), flush=True)
 
 
+def study_bf16state(args, local):
+    """The benchmark step with a bf16 state pool (32 KiB per head instead of
+    64 KiB): 30 layers of verify + commit, and the fused commit-into-verify
+    step, on the same wide ragged workload."""
+    from gdn_speculative_tree_gb300 import binding
+    dev = torch.device("cuda", local)
+    cfg = wl.CONFIGS[CONFIG_NAME]
+    layers = args.layers
+    work = [binding.TreeVerifier(wl.generate(cfg, layer=l, device=dev, state_dtype="bf16"))
+            for l in range(layers)]
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = read_peaks()
+    Ns, plen = tree_stats(work[0].wl.trees, work[0].wl.accepted.cpu().numpy())
+    H = cfg.H
+    vb, cb = verify_bytes(Ns, H, 32768), commit_bytes(plen, H, 32768)
+    fb = vb + cb - int(H * 32768 * int((plen > 0).sum()))
+    nodes = int(Ns.sum())
+
+    def timed(fn_layer):
+        for _ in range(args.warmup):
+            for tv in work:
+                fn_layer(tv)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps * layers)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        i = 0
+        for _ in range(args.steps):
+            for tv in work:
+                ev[i][0].record(stream)
+                fn_layer(tv)
+                ev[i][1].record(stream)
+                i += 1
+        end.record(stream)
+        torch.cuda.synchronize()
+        per = [a.elapsed_time(b) for a, b in ev]
+        return start.elapsed_time(end) / args.steps, sum(per) / len(per)
+
+    v_step, v_ms = timed(lambda tv: tv.verify(stream))
+    c_step, c_ms = timed(lambda tv: tv.commit(None, stream))
+    f_step, f_ms = timed(lambda tv: binding.treewy_commit_verify(tv.batch, tv.wl.accepted, tv.batch,
+                                                                 stream))
+    for tv in work:
+        if tv.status.any().item():
+            raise SystemExit("device status bits set in the bf16 state study")
+    g = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
+    print(json.dumps({
+        "study": "bf16 state pool", "workload": "wide ragged trees, 256 req x 32 heads, "
+        f"{layers} layers, bf16 state", "peak_gbs": peak, "peak_kind": f"{peak_kind} hbm_gbs",
+        "ms_per_step": v_step + c_step, "value": nodes / ((v_step + c_step) * 1e-3), "unit": UNIT,
+        "verify": {"avg_launch_ms": v_ms, "algorithmic_bytes": vb, "gbs": g(vb, v_ms),
+                   "frac": g(vb, v_ms) / peak},
+        "commit": {"avg_launch_ms": c_ms, "algorithmic_bytes": cb, "gbs": g(cb, c_ms),
+                   "frac": g(cb, c_ms) / peak},
+        "fused": {"ms_per_step": f_step, "value": nodes / (f_step * 1e-3), "avg_launch_ms": f_ms,
+                  "algorithmic_bytes": fb, "gbs": g(fb, f_ms), "frac": g(fb, f_ms) / peak}}),
+        flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -621,7 +683,7 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--cpu-requests", type=int, default=64)
     ap.add_argument("--no-storeall", action="store_true")
-    ap.add_argument("--study", choices=["widths", "graph"],
+    ap.add_argument("--study", choices=["widths", "graph", "bf16state"],
                     help="print one study line instead of the benchmark line (1 GPU)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -635,7 +697,8 @@ def main():
                 torch.cuda.set_device(local)
                 _build.build()
                 binding.load()
-                {"widths": study_widths, "graph": study_graph}[args.study](args, local)
+                {"widths": study_widths, "graph": study_graph,
+                 "bf16state": study_bf16state}[args.study](args, local)
         elif args.impl == "reference":
             run_reference(args, world, rank)
         else:

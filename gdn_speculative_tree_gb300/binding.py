@@ -33,6 +33,7 @@ STATUS_TIMEOUT = 16
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
 FLAG_FORCE_GENERIC = 1
+FLAG_STATE_BF16 = 2
 MAX_NODES = 64
 
 
@@ -189,6 +190,10 @@ def make_batch(*, node_offset, parent, q, k, v, alpha, beta, state, state_slot, 
                     ("parent", parent), ("state_slot", state_slot)):
         if x is not None and not x.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
+    if state.dtype == torch.bfloat16:
+        flags |= FLAG_STATE_BF16
+    elif state.dtype != torch.float32:
+        raise TypeError(f"state dtype {state.dtype} is not fp32 or bf16")
     b = TreewyBatch()
     b.R, b.H, b.dk, b.dv = R, H, dk, dv
     b.max_nodes = int(max_nodes)

@@ -3,9 +3,10 @@
 //
 //   S_a = gamma_a S0 + sum_{i on the root-to-a path} (gamma_a / gamma_i) u_i k_i^T,
 //
-// written in place over S0 in the state pool.  The update has rank
-// |path(a)| <= depth, so the kernel is a streaming pass over the 64 KB state
-// (read once, written once) with the path's u and k rows staged in shared
+// written in place over S0 in the state pool (f32, or bf16 rounded to nearest
+// even from the f32 result).  The update has rank |path(a)| <= depth, so the
+// kernel is a streaming pass over the state (64 KB f32 / 32 KB bf16, read once,
+// written once) with the path's u and k rows staged in shared
 // memory; ratios gamma_a / gamma_i are products of alpha over the path segment.
 //
 // One CTA of 256 threads per (request, head).  The state loads are issued
@@ -18,16 +19,55 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kSeg = 16;             // path nodes staged per pass
-constexpr int kMaxVec = 16;          // float4 per thread for a 128 x 128 state
 
-// Streaming (evict-first) access: every state byte is touched exactly once.
-__device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
-__device__ __forceinline__ void st_stream(float4* p, float4 v) { __stcs(p, v); }
+// State elements per 16-byte vector and the f32 <-> storage conversions: f32
+// state (4 per vector) or bf16 state (8 per vector, rounded to nearest even).
+template <bool SB>
+struct StateVec {
+  static constexpr int E = SB ? 8 : 4;
+  // Streaming (evict-first) access: every state byte is touched exactly once.
+  __device__ static __forceinline__ void load(const void* base, int f, float (&x)[E]) {
+    const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(base) + f);
+    if constexpr (SB) {
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    } else {
+      x[0] = __uint_as_float(raw.x);
+      x[1] = __uint_as_float(raw.y);
+      x[2] = __uint_as_float(raw.z);
+      x[3] = __uint_as_float(raw.w);
+    }
+  }
+  __device__ static __forceinline__ void store(void* base, int f, const float (&x)[E]) {
+    uint4 raw;
+    if constexpr (SB) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+      raw = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      raw = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                       __float_as_uint(x[3]));
+    }
+    __stcs(reinterpret_cast<uint4*>(base) + f, raw);
+  }
+};
 
-// Two resident blocks per SM: the 16 float4 state registers per thread stay
-// in registers (a three-block cap spills them and was measured slower).
+// Two resident blocks per SM: the 64 state values per thread stay in
+// registers (a three-block cap spills them and was measured slower).
+template <bool SB>
 __global__ void __launch_bounds__(kThreads, 2)
     commit_kernel(const treewy_batch b, const int32_t* __restrict__ accepted) {
+  using SV = StateVec<SB>;
+  constexpr int E = SV::E;
+  constexpr int kNV = 128 * 128 / (E * kThreads);  // vectors per thread for a 128 x 128 state
   __shared__ int s_parent[kMaxNodes];
   __shared__ float s_alpha[kMaxNodes];
   __shared__ int s_path[kMaxNodes];
@@ -70,19 +110,25 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   const int64_t tok0 = s_info[0];
   const int N = s_info[1];
-  float* S = b.state + (static_cast<int64_t>(s_info[2]) * H + h) * dv * dk;
+  const int64_t head0 = (static_cast<int64_t>(s_info[2]) * H + h) * dv * dk;
+  void* S = SB ? static_cast<void*>(static_cast<__nv_bfloat16*>(b.state) + head0)
+               : static_cast<void*>(static_cast<float*>(b.state) + head0);
   const int nelem = dv * dk;
-  const bool vec = (dk & 3) == 0;
-  const int nvec = nelem >> 2;
+  const bool vec = (dk % E) == 0;
+  const int nvec = nelem / E;
 
   // 1. state loads in flight
-  float4 acc[kMaxVec];
+  float acc[kNV][E];
   if (vec) {
 #pragma unroll
-    for (int m = 0; m < kMaxVec; ++m) {
+    for (int m = 0; m < kNV; ++m) {
       const int f = t + m * kThreads;
-      acc[m] = (f < nvec) ? ld_stream(reinterpret_cast<const float4*>(S) + f)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (f < nvec) {
+        SV::load(S, f, acc[m]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[m][e] = 0.f;
+      }
     }
   }
 
@@ -141,46 +187,48 @@ __global__ void __launch_bounds__(kThreads, 2)
       __syncthreads();
       if (seg == 0) {
 #pragma unroll
-        for (int m = 0; m < kMaxVec; ++m) {
-          acc[m].x *= ga;
-          acc[m].y *= ga;
-          acc[m].z *= ga;
-          acc[m].w *= ga;
-        }
+        for (int m = 0; m < kNV; ++m)
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[m][e] *= ga;
       }
       if (dk == 128) {
-        // float4 f = t + 256 m covers row d = t/32 + 8m, columns x..x+3 with
-        // x = 4 (t % 32): the k chunk of a path node is loaded once per node
-        const int x = (t & 31) << 2;
-        const int d0 = t >> 5;
+        // vector f = t + 256 m covers row d = t / V + (256 / V) m, columns
+        // x..x+E-1 with x = E (t % V), V = 128 / E vectors per row: the k
+        // chunk of a path node is loaded once per node
+        constexpr int V = 128 / E;
+        const int x = (t % V) * E;
+        const int d0 = t / V;
         for (int j = 0; j < ns; ++j) {
-          const float4 kk = *reinterpret_cast<const float4*>(&kf[j][x]);
+          float kk[E];
 #pragma unroll
-          for (int m = 0; m < kMaxVec; ++m) {
-            const int d = d0 + 8 * m;
+          for (int e = 0; e < E; e += 4) {
+            const float4 k4 = *reinterpret_cast<const float4*>(&kf[j][x + e]);
+            kk[e] = k4.x;
+            kk[e + 1] = k4.y;
+            kk[e + 2] = k4.z;
+            kk[e + 3] = k4.w;
+          }
+#pragma unroll
+          for (int m = 0; m < kNV; ++m) {
+            const int d = d0 + (kThreads / V) * m;
             if (d < dv) {
               const float u = cu[j][d];
-              acc[m].x = fmaf(u, kk.x, acc[m].x);
-              acc[m].y = fmaf(u, kk.y, acc[m].y);
-              acc[m].z = fmaf(u, kk.z, acc[m].z);
-              acc[m].w = fmaf(u, kk.w, acc[m].w);
+#pragma unroll
+              for (int e = 0; e < E; ++e) acc[m][e] = fmaf(u, kk[e], acc[m][e]);
             }
           }
         }
       } else {
 #pragma unroll
-        for (int m = 0; m < kMaxVec; ++m) {
+        for (int m = 0; m < kNV; ++m) {
           const int f = t + m * kThreads;
           if (f < nvec) {
-            const int e = f << 2;
-            const int d = e / dk, x = e - d * dk;
+            const int e0 = f * E;
+            const int d = e0 / dk, x = e0 - d * dk;
             for (int j = 0; j < ns; ++j) {
               const float u = cu[j][d];
-              const float4 kk = *reinterpret_cast<const float4*>(&kf[j][x]);
-              acc[m].x = fmaf(u, kk.x, acc[m].x);
-              acc[m].y = fmaf(u, kk.y, acc[m].y);
-              acc[m].z = fmaf(u, kk.z, acc[m].z);
-              acc[m].w = fmaf(u, kk.w, acc[m].w);
+#pragma unroll
+              for (int e = 0; e < E; ++e) acc[m][e] = fmaf(u, kf[j][x + e], acc[m][e]);
             }
           }
         }
@@ -188,28 +236,49 @@ __global__ void __launch_bounds__(kThreads, 2)
       __syncthreads();
     }
 #pragma unroll
-    for (int m = 0; m < kMaxVec; ++m) {
+    for (int m = 0; m < kNV; ++m) {
       const int f = t + m * kThreads;
-      if (f < nvec) st_stream(reinterpret_cast<float4*>(S) + f, acc[m]);
+      if (f < nvec) SV::store(S, f, acc[m]);
     }
   } else {
-    // scalar path for head sizes that are not a multiple of 4
-    for (int seg = 0; seg < len; seg += kSeg) {
-      const int ns = min(kSeg, len - seg);
-      for (int e = t; e < ns * 128; e += kThreads) {
-        const int j = e >> 7, x = e & 127;
-        const int64_t row = (tok0 + s_path[seg + j]) * H + h;
-        cu[j][x] = (x < dv) ? s_c[seg + j] * __ldg(b.U + row * dv + x) : 0.f;
-        kf[j][x] = (x < dk) ? load_qkv(b.k, row * dk + x, bf16) : 0.f;
+    // scalar path for head sizes that are not a multiple of the vector
+    // width: blocks of kThreads x kSc elements stay in f32 registers across
+    // every pass and are stored (rounded once, for a bf16 state) at the end
+    constexpr int kSc = 16;
+    for (int e0 = 0; e0 < nelem; e0 += kThreads * kSc) {
+      float sreg[kSc];
+#pragma unroll
+      for (int i = 0; i < kSc; ++i) {
+        const int e = e0 + t + i * kThreads;
+        sreg[i] = (e < nelem) ? ga * load_qkv(S, e, SB) : 0.f;
       }
-      __syncthreads();
-      for (int e = t; e < nelem; e += kThreads) {
-        const int d = e / dk, x = e - d * dk;
-        float s = (seg == 0) ? ga * S[e] : S[e];
-        for (int j = 0; j < ns; ++j) s = fmaf(cu[j][d], kf[j][x], s);
-        S[e] = s;
+      for (int seg = 0; seg < len; seg += kSeg) {
+        const int ns = min(kSeg, len - seg);
+        __syncthreads();  // the previous pass is done with cu / kf
+        for (int e = t; e < ns * 128; e += kThreads) {
+          const int j = e >> 7, x = e & 127;
+          const int64_t row = (tok0 + s_path[seg + j]) * H + h;
+          cu[j][x] = (x < dv) ? s_c[seg + j] * __ldg(b.U + row * dv + x) : 0.f;
+          kf[j][x] = (x < dk) ? load_qkv(b.k, row * dk + x, bf16) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kSc; ++i) {
+          const int e = e0 + t + i * kThreads;
+          if (e < nelem) {
+            const int d = e / dk, x = e - d * dk;
+            for (int j = 0; j < ns; ++j) sreg[i] = fmaf(cu[j][d], kf[j][x], sreg[i]);
+          }
+        }
       }
-      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < kSc; ++i) {
+        const int e = e0 + t + i * kThreads;
+        if (e < nelem) {
+          if constexpr (SB) static_cast<__nv_bfloat16*>(S)[e] = __float2bfloat16_rn(sreg[i]);
+          else static_cast<float*>(S)[e] = sreg[i];
+        }
+      }
     }
   }
 }
@@ -218,7 +287,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 cudaError_t launch_commit(const treewy_batch& b, const int32_t* accepted, cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
-  commit_kernel<<<grid, kThreads, 0, stream>>>(b, accepted);
+  if (b.flags & TREEWY_FLAG_STATE_BF16)
+    commit_kernel<true><<<grid, kThreads, 0, stream>>>(b, accepted);
+  else
+    commit_kernel<false><<<grid, kThreads, 0, stream>>>(b, accepted);
   return cudaGetLastError();
 }
 

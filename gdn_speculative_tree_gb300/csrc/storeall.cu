@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kThreads)
   const int c0 = (t & 1) * kCols;
   const bool row_ok = d < dv;
   const int64_t head_elems = static_cast<int64_t>(dv) * dk;
-  const float* S0 = b.state + (static_cast<int64_t>(s_info[2]) * H + h) * head_elems;
+  const float* S0 = static_cast<const float*>(b.state) + (static_cast<int64_t>(s_info[2]) * H + h) * head_elems;
   auto snap = [&](int n) { return snapshots + ((rel0 + n) * H + h) * head_elems; };
 
   float s[kCols];
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads)
   const int x = (t & 31) << 2;
   const int d0 = t >> 5;
   constexpr int64_t kHead = kD * kD;
-  const float* S0 = b.state + (static_cast<int64_t>(s_info[2]) * H + h) * kHead;
+  const float* S0 = static_cast<const float*>(b.state) + (static_cast<int64_t>(s_info[2]) * H + h) * kHead;
   auto snap = [&](int n) { return snapshots + ((rel0 + n) * H + h) * kHead; };
   float4 S[kRowsPerThread];
   auto load_state = [&](const float* src) {
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t head_elems = static_cast<int64_t>(b.dv) * b.dk;
   const int64_t rel = static_cast<int64_t>(lo) - b.node_offset[0] + a;
   const float* src = snapshots + (rel * H + h) * head_elems;
-  float* dst = b.state + (static_cast<int64_t>(slot) * H + h) * head_elems;
+  float* dst = static_cast<float*>(b.state) + (static_cast<int64_t>(slot) * H + h) * head_elems;
   if ((head_elems & 3) == 0) {
     const float4* s4 = reinterpret_cast<const float4*>(src);
     float4* d4 = reinterpret_cast<float4*>(dst);

@@ -47,6 +47,8 @@ treewy_status validate(const treewy_batch* b, bool need_qv, bool need_outputs, b
                 TREEWY_MAX_NODES);
   if (b->qkv_dtype != TREEWY_DTYPE_BF16 && b->qkv_dtype != TREEWY_DTYPE_F32)
     return fail(TREEWY_ERR_INVALID_ARG, "qkv_dtype = %d is not TREEWY_DTYPE_BF16/F32", b->qkv_dtype);
+  if (b->flags & ~(TREEWY_FLAG_FORCE_GENERIC | TREEWY_FLAG_STATE_BF16))
+    return fail(TREEWY_ERR_INVALID_ARG, "flags = 0x%x has unknown bits", b->flags);
   if (b->T < 0 || b->T > (int64_t(1) << 31) - 1)
     return fail(TREEWY_ERR_INVALID_ARG, "T = %lld outside [0, 2^31)", (long long)b->T);
   if (b->num_slots < 1) return fail(TREEWY_ERR_INVALID_ARG, "num_slots = %lld must be >= 1",
@@ -97,12 +99,15 @@ treewy_status make_maps(const treewy_batch* b, treewy::VerifyMaps* m) {
   if (enc == nullptr) return fail(TREEWY_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const cuuint32_t ones[3] = {1, 1, 1};
   {
+    // one box = 128 state rows x 128 bytes (32 f32 or 64 bf16 columns)
+    const bool sb = (b->flags & TREEWY_FLAG_STATE_BF16) != 0;
     const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(b->num_slots) * b->H * 128};
-    const cuuint64_t strides[1] = {128 * sizeof(float)};
-    const cuuint32_t box[2] = {32, 128};
-    CUresult rc = enc(&m->s0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, b->state, dims, strides, box,
-                      ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint64_t strides[1] = {128 * (sb ? 2u : 4u)};
+    const cuuint32_t box[2] = {sb ? 64u : 32u, 128};
+    CUresult rc = enc(&m->s0, sb ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                      2, b->state, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (rc != CUDA_SUCCESS) return fail(TREEWY_ERR_CUDA, "tensor map for state failed (%d)", (int)rc);
   }
   const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(b->H), static_cast<cuuint64_t>(b->T)};
@@ -168,6 +173,8 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
   if (prev->state != next->state || prev->state_slot != next->state_slot ||
       prev->num_slots != next->num_slots)
     return fail(TREEWY_ERR_INVALID_ARG, "prev and next must share the state pool and state_slot");
+  if ((prev->flags ^ next->flags) & TREEWY_FLAG_STATE_BF16)
+    return fail(TREEWY_ERR_INVALID_ARG, "prev and next must agree on TREEWY_FLAG_STATE_BF16");
   if (next->R == 0) return TREEWY_OK;
   if (!prev->U) return fail(TREEWY_ERR_INVALID_ARG, "prev->U is NULL");
   if (!prev_accepted) return fail(TREEWY_ERR_INVALID_ARG, "prev_accepted is NULL");
@@ -198,7 +205,10 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
 treewy_status treewy_storeall_verify(const treewy_batch* batch, float* snapshots, cudaStream_t stream) {
   g_last_error.clear();
   treewy_status st = validate(batch, true, false, true);
-  if (st != TREEWY_OK || batch->R == 0) return st;
+  if (st != TREEWY_OK) return st;
+  if (batch->flags & TREEWY_FLAG_STATE_BF16)
+    return fail(TREEWY_ERR_UNSUPPORTED, "the storeall comparator keeps f32 states only");
+  if (batch->R == 0) return st;
   if (!batch->o) return fail(TREEWY_ERR_INVALID_ARG, "o is NULL");
   if (!snapshots || !aligned16(snapshots))
     return fail(TREEWY_ERR_INVALID_ARG, "snapshots must be non-NULL and 16-byte aligned");
@@ -210,6 +220,8 @@ treewy_status treewy_storeall_commit(const treewy_batch* batch, const float* sna
                                      const int32_t* accepted, cudaStream_t stream) {
   g_last_error.clear();
   treewy_status st = validate(batch, false, false, false, false);
+  if (st == TREEWY_OK && (batch->flags & TREEWY_FLAG_STATE_BF16))
+    return fail(TREEWY_ERR_UNSUPPORTED, "the storeall comparator keeps f32 states only");
   if (st == TREEWY_OK && batch->R > 0 && !batch->parent)
     return fail(TREEWY_ERR_INVALID_ARG, "parent is NULL");
   if (st != TREEWY_OK || batch->R == 0) return st;

@@ -48,7 +48,7 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// Load element i of a q/k/v row as float (bf16 or fp32 storage).
+// Load element i of a q/k/v row (or of a state block) as float (bf16 or fp32 storage).
 __device__ __forceinline__ float load_qkv(const void* base, int64_t idx, bool is_bf16) {
   if (is_bf16) {
     return bf16_bits_to_float(__ldg(reinterpret_cast<const unsigned short*>(base) + idx));

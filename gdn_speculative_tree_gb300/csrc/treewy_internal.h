@@ -13,7 +13,8 @@ namespace treewy {
 // Tensor maps the tensor-core verify kernel reads through (built on the host
 // per call; passed by value as kernel parameters).
 struct VerifyMaps {
-  CUtensorMap s0;  // state pool, fp32 [rows = slots*H*128][128], box 32 x 128, 128B swizzle
+  CUtensorMap s0;  // state pool [rows = slots*H*128][128], box 128 rows x 128 bytes
+                   // (32 fp32 or 64 bf16 columns), 128B swizzle
   CUtensorMap k;   // keys, bf16 [T][H][128], box 64 x 1 x 8, 128B swizzle
   CUtensorMap q;   // queries, same layout as keys
 };
@@ -41,6 +42,9 @@ cudaError_t launch_verify_tc(const treewy_batch& b, const VerifyMaps& maps, int 
                              cudaStream_t stream);
 cudaError_t launch_commit_verify_tc(const treewy_batch& next, const PrevRound& prev,
                                     const VerifyMaps& maps, int npm, cudaStream_t stream);
+// The same kernel for a bf16 state pool; prev == nullptr for plain verification.
+cudaError_t launch_verify_tc_bf16state(const treewy_batch& b, const VerifyMaps& maps,
+                                       const PrevRound* prev, int npm, cudaStream_t stream);
 
 cudaError_t launch_commit(const treewy_batch& b, const int32_t* accepted, cudaStream_t stream);
 

@@ -88,10 +88,11 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t tok0 = ts.tok0;
 
   // stage S0 (row pitch dk+1 keeps column reads conflict-free), K, Q, V
-  const float* S0 = b.state + (static_cast<int64_t>(ts.slot) * H + h) * dv * dk;
+  const bool state_bf16 = (b.flags & TREEWY_FLAG_STATE_BF16) != 0;
+  const int64_t s0_base = (static_cast<int64_t>(ts.slot) * H + h) * dv * dk;
   for (int e = t; e < dv * dk; e += kThreads) {
     const int d = e / dk, j = e - d * dk;
-    S0s[d * (dk + 1) + j] = __ldg(S0 + e);
+    S0s[d * (dk + 1) + j] = load_qkv(b.state, s0_base + e, state_bf16);
   }
   for (int e = t; e < N * dk; e += kThreads) {
     const int n = e / dk, j = e - n * dk;

@@ -1,757 +1,9 @@
-// verify_tc.cu -- TreeWY verification on the 5th-generation tensor cores
-// (tcgen05, TMEM accumulators, TMA staging) for dk = dv = 128, bf16 q/k/v,
-// fp32 committed state.
-//
-// One CTA (256 threads, two warpgroups; thread t owns TMEM lane t % 128 =
-// value row d) per (request, head).  With Np = N rounded up to 16:
-//
-//  TMA      S0 (64 KB fp32 as 4 boxes of 128 rows x 32 columns, 128B swizzle)
-//           and the tree's K and Q rows (bf16, 8-row boxes).
-//  split    each thread turns its own 128-byte S0 row segments in place into
-//           [hi | lo] bf16 halves, S0 ~= hi + lo (16 significant bits).
-//  MMA 1    D1 = S0 [K;Q]^T   (M = 128, N = 2Np, K = 128; hi and lo accumulate
-//           into one fp32 accumulator): column n = S0 k_n, column Np+n = S0 q_n
-//           (TreeWY paper §3 Eq. (2), R term; review §3.2 Algorithm steps 3, 5).
-//           D2 = [K;Q] K^T    (M = 128, N = Np): Gram rows k_m.k_i and q_m.k_i
-//           (paper Eq. (2) G; review Algorithm step 2).
-//  coeffs   per node n with root-to-n path p_0 = n, p_1 = parent(n), ...:
-//             A[n, p_k] = beta_n (gamma_n/gamma_{p_k}) k_{p_k}.k_n  (k >= 1)
-//             M[n, p_k] = (gamma_n/gamma_{p_k}) k_{p_k}.q_n         (k >= 0)
-//           then the rows of T = (I + A)^-1 and B = M T restricted to the path,
-//           each by its own O(depth^2) recurrence, since T (I + A) = I and
-//           B (I + A) = M: row n solves x_q = r_q - sum_{a<q} x_a A[p_a, p_q]
-//           with r = e_0 for T and r_q = M[n, p_q] for B.
-//  MMA 2    U = T W and O = B W with W = diag(beta)(V - diag(gamma)(S0 K^T)^T),
-//           as one product [U | O] = W^T [T;B]^T (M = 128, N = 2Np, K = Np;
-//           bf16 hi/lo splits of W, T and B, three accumulating terms), so the
-//           triangular solve of paper Eq. (2) needs no per-column recurrence.
-//  store    U[n] and o_n = gamma_n S0 q_n + O[n] (review Eq. (5) restricted to
-//           ancestors), coalesced, thread d writing column d.
-//
-// Nothing per node is kept beyond U (N x dv), the object that replaces the
-// per-node snapshots (paper §3 "Reconstruct on commit").
-#include "treewy_device.cuh"
-#include "treewy_internal.h"
+// verify_tc.cu -- launchers of the tensor-core verification kernel
+// (verify_tc.cuh) for an fp32 state pool; a bf16 pool is dispatched to
+// verify_tc_bf16state.cu, so the two sets of instances compile in parallel.
+#include "verify_tc.cuh"
 
 namespace treewy {
-namespace {
-
-constexpr int kThreads = 256;
-constexpr int kDim = 128;
-constexpr uint32_t kS0ChunkBytes = 128u * 128u;     // 128 rows x 32 fp32
-constexpr uint32_t kS0Bytes = 4u * kS0ChunkBytes;   // 64 KB: S0, then W^T and [T;B]
-constexpr uint32_t kKQChunkBytes = 128u * 128u;     // 128 rows x 64 bf16
-constexpr uint32_t kKQBytes = 2u * kKQChunkBytes;   // 32 KB: K,Q, then coefficient lists
-// Operands of the second MMA, placed in the S0 region once the first is done:
-// each is 128 rows x 128 bytes (K-major, 128B swizzle, K <= 64 bf16).
-constexpr uint32_t kWhiOff = 0, kWloOff = 16384, kThiOff = 32768, kTloOff = 49152;
-constexpr int kRegPath = 8;  // paths up to this length keep T/B rows in registers
-
-template <int NPM>
-struct TcCfg {
-  // D1 = [S0k | S0q] in columns [0, 2NPM); the Gram, then [U | O], from 2NPM
-  static constexpr uint32_t kCols = 4u * NPM;
-  static_assert(NPM == 16 || NPM == 32 || NPM == 64, "tree capacity bucket");
-  static constexpr int kE = NPM * (NPM + 1) / 2;              // path-list entries, worst case
-  static constexpr uint32_t kListBytes = 4u * kE;
-  static constexpr uint32_t kPidxBytes = (kE + 15u) & ~15u;
-  static constexpr uint32_t kR2Bytes = kPidxBytes + kListBytes;  // pidx + (pc | B scratch)
-  static constexpr uint32_t kDynSmem = kS0Bytes + kKQBytes + kR2Bytes + 1024u;
-  static_assert(3u * kListBytes <= kKQBytes, "A, M and T-scratch lists must fit the K/Q region");
-};
-
-// Per-CTA tree data for one (request, head).
-struct TreeTC {
-  int parent[kMaxNodes];
-  float alpha[kMaxNodes];
-  float gamma[kMaxNodes];
-  float2 bbg[kMaxNodes];                // (beta_n, beta_n * gamma_n)
-  int D[kMaxNodes];                     // path length root..n, n included
-  int off[kMaxNodes + 1];               // CSR offsets of the path lists
-  int tok0, N, slot, flags;
-};
-
-// Load parents and gates, validate the tree, and build every node's path list
-// p_0 = n, p_1, ... with the decay products c_k = gamma_n / gamma_{p_k} formed
-// as products of alpha along the path (no division).  All threads must call
-// it; returns false uniformly when a parent index is out of range.
-__device__ __forceinline__ bool prepare_tree(TreeTC& ts, uint8_t* pidx, float* pc,
-                                             const treewy_batch& b, int h) {
-  const int t = threadIdx.x;
-  const int N = ts.N;
-  const int H = b.H;
-  bool bad = false;
-  float beta = 0.f;
-  if (t < N) {
-    const int64_t row = static_cast<int64_t>(ts.tok0) + t;
-    const int p = __ldg(b.parent + row);
-    bad = !(p >= -1 && p < t);
-    ts.parent[t] = bad ? -1 : p;
-    ts.alpha[t] = __ldg(b.alpha + row * H + h);
-    beta = __ldg(b.beta + row * H + h);
-  }
-  if (__syncthreads_or(bad)) return false;
-  if (t < N) {
-    float g = ts.alpha[t];
-    int D = 1;
-    for (int p = ts.parent[t]; p >= 0; p = ts.parent[p]) {
-      g *= ts.alpha[p];
-      ++D;
-    }
-    ts.gamma[t] = g;
-    ts.bbg[t] = make_float2(beta, beta * g);
-    ts.D[t] = D;
-  }
-  __syncthreads();
-  if (t < 32) {
-    const int i0 = 2 * t, i1 = 2 * t + 1;
-    const int a0 = i0 < N ? ts.D[i0] : 0;
-    const int a1 = i1 < N ? ts.D[i1] : 0;
-    int s = a0 + a1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (t >= o) s += y;
-    }
-    const int excl = s - a0 - a1;
-    ts.off[i0] = excl;
-    ts.off[i1] = excl + a0;
-    if (t == 31) ts.off[kMaxNodes] = s;
-  }
-  __syncthreads();
-  if (t < N) {
-    const int o = ts.off[t];
-    float c = 1.0f;
-    int k = 0;
-    for (int cur = t; cur >= 0; cur = ts.parent[cur], ++k) {
-      pidx[o + k] = static_cast<uint8_t>(cur);
-      pc[o + k] = c;
-      c *= ts.alpha[cur];
-    }
-  }
-  return true;
-}
-
-// Thread-private in-place conversion of one 128-byte swizzled row segment:
-// 32 fp32 values become 64 bf16 values [hi(32) | lo(32)] with
-// hi = rn(x), lo = rn(x - hi), in the same 128B-swizzle layout.
-__device__ __forceinline__ void convert_row_hilo(unsigned char* row, int sw) {
-  float f[32];
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    const float4 x = *reinterpret_cast<const float4*>(row + ((g ^ sw) << 4));
-    f[4 * g + 0] = x.x;
-    f[4 * g + 1] = x.y;
-    f[4 * g + 2] = x.z;
-    f[4 * g + 3] = x.w;
-  }
-  uint32_t hi[16], lo[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) split_pair(f[2 * j], f[2 * j + 1], hi[j], lo[j]);
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    const uint32_t* src = (g < 4) ? (hi + 4 * g) : (lo + 4 * (g - 4));
-    *reinterpret_cast<uint4*>(row + ((g ^ sw) << 4)) = make_uint4(src[0], src[1], src[2], src[3]);
-  }
-}
-
-// Zero row `row` of the hi and lo halves of a K-major 128B-swizzled operand.
-__device__ __forceinline__ void zero_operand_row(unsigned char* hi, unsigned char* lo, int row) {
-  unsigned char* rh = hi + row * 128;
-  unsigned char* rl = lo + row * 128;
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {  // swizzled order: conflict-free across rows
-    *reinterpret_cast<uint4*>(rh + ((g ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(rl + ((g ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
-// Store x (hi/lo bf16) at column `col` of row `row` of a K-major 128B-swizzled operand.
-__device__ __forceinline__ void put_operand(unsigned char* hi, unsigned char* lo, int row, int col,
-                                            float x) {
-  const __nv_bfloat16 xh = __float2bfloat16_rn(x);
-  const __nv_bfloat16 xl = __float2bfloat16_rn(x - __bfloat162float(xh));
-  const int byte = row * 128 + (((col >> 3) ^ (row & 7)) << 4) + ((col & 7) << 1);
-  *reinterpret_cast<__nv_bfloat16*>(hi + byte) = xh;
-  *reinterpret_cast<__nv_bfloat16*>(lo + byte) = xl;
-}
-
-// Row of T = (I + A)^-1 (rhs = nullptr: r = e_0) or of B = M T (rhs = node n's
-// M coefficients along its path) on node n's path p_0 = n, p_1, ...: solves
-// x_q = r_q - sum_{a<q} x_a A[p_a, p_q], where A[p_a, p_q] is the entry of
-// p_a's strict-ancestor list at position q - a, and writes x_q (hi/lo bf16) at
-// column p_q of operand row `row`.  `scratch` holds x for paths longer than
-// kRegPath (registers otherwise).
-__device__ __forceinline__ void build_path_row(const TreeTC& ts, int n, int row,
-                                               const uint8_t* pidx, const float* aco,
-                                               const float* rhs, float* scratch,
-                                               unsigned char* thi, unsigned char* tlo) {
-  const int Dn = ts.D[n], o = ts.off[n];
-  zero_operand_row(thi, tlo, row);
-  if (Dn <= kRegPath) {
-    int col[kRegPath], opa[kRegPath];
-    float x[kRegPath];
-#pragma unroll
-    for (int a = 0; a < kRegPath; ++a) {
-      const int c = (a < Dn) ? pidx[o + a] : 0;
-      col[a] = c;
-      opa[a] = ts.off[c];
-      x[a] = rhs ? ((a < Dn) ? rhs[o + a] : 0.f) : (a == 0 ? 1.0f : 0.f);
-    }
-#pragma unroll
-    for (int q = 1; q < kRegPath; ++q) {
-#pragma unroll
-      for (int a = 0; a < q; ++a) {
-        const float A = (q < Dn) ? aco[opa[a] + (q - a)] : 0.f;
-        x[q] = fmaf(-x[a], A, x[q]);
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < kRegPath; ++q)
-      if (q < Dn) put_operand(thi, tlo, row, col[q], x[q]);
-  } else {
-    for (int q = 0; q < Dn; ++q) scratch[o + q] = rhs ? rhs[o + q] : (q == 0 ? 1.0f : 0.f);
-    for (int a = 0; a + 1 < Dn; ++a) {
-      const float xa = scratch[o + a];
-      const int opa = ts.off[pidx[o + a]];
-      for (int q = a + 1; q < Dn; ++q) scratch[o + q] = fmaf(-xa, aco[opa + (q - a)], scratch[o + q]);
-    }
-    for (int q = 0; q < Dn; ++q) put_operand(thi, tlo, row, pidx[o + q], scratch[o + q]);
-  }
-}
-
-// Previous-round data for the fused commit (shared memory; empty when the
-// kernel is not fused).
-constexpr int kPrevSeg = 8;  // path nodes of the previous round staged per pass
-template <bool FUSED>
-struct PrevSmem {
-  int a;
-};
-template <>
-struct PrevSmem<true> {
-  int parent[kMaxNodes];
-  float alpha[kMaxNodes];
-  float c[kMaxNodes];                // gamma_a / gamma_{path j} (alpha products)
-  uint8_t path[kMaxNodes];           // accepted node, its parent, ... (root last)
-  __nv_bfloat16 k[kPrevSeg][kDim];   // staged k rows of up to kPrevSeg path nodes
-  int tok0, N, a, len;
-  float gamma_a;
-};
-
-template <int NPM, bool FUSED>
-__global__ void __launch_bounds__(kThreads)
-    verify_tc_kernel(const __grid_constant__ CUtensorMap map_s0,
-                     const __grid_constant__ CUtensorMap map_k,
-                     const __grid_constant__ CUtensorMap map_q, const treewy_batch b,
-                     const PrevRound prev) {
-  using C = TcCfg<NPM>;
-  extern __shared__ unsigned char smem_raw[];
-  __shared__ TreeTC ts;
-  __shared__ PrevSmem<FUSED> pv;
-  // 0-3: S0 chunks, 4: K/Q, 5: S0 [K;Q]^T done, 6: second MMA done, 7: Gram done
-  __shared__ __align__(8) uint64_t bars[8];
-  __shared__ uint32_t tmem_holder;
-  __shared__ int s_fail;
-
-  unsigned char* base = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
-  unsigned char* s0 = base;
-  unsigned char* kq = base + kS0Bytes;
-  uint8_t* pidx = base + kS0Bytes + kKQBytes;
-  float* pc = reinterpret_cast<float*>(pidx + C::kPidxBytes);
-  float* xB = pc;  // long-path B rows reuse the decay products once consumed
-  float* aco = reinterpret_cast<float*>(kq);
-  float* mco = aco + C::kE;
-  float* xT = mco + C::kE;
-  unsigned char* thi = s0 + kThiOff;
-  unsigned char* tlo = s0 + kTloOff;
-
-  const int H = b.H;
-  const int r = blockIdx.x / H;
-  const int h = blockIdx.x - r * H;
-  const int t = threadIdx.x;
-  const int lane = t & 127;  // TMEM lane = value row d
-  const int wg = t >> 7;
-  const int warp = t >> 5;
-  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  bool mma_issued = false;
-  bool mma2_issued = false;
-
-  if (t == 0) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
-    fence_mbarrier_init();
-    s_fail = 0;
-    // every metadata load of this CTA is independent: one memory round trip
-    const int lo = b.node_offset[r], hi = b.node_offset[r + 1];
-    const int slot = b.state_slot[r];
-    int pa = -1, plo = 0, phi = 0;
-    if constexpr (FUSED) {
-      pa = prev.accepted[r];
-      plo = prev.node_offset[r];
-      phi = prev.node_offset[r + 1];
-    }
-    int flags = 0;
-    const int N = hi - lo;
-    if (N < 0 || N > b.max_nodes) flags |= TREEWY_STATUS_TOO_MANY_NODES;
-    else if (lo < 0 || static_cast<int64_t>(hi) > b.T) flags |= TREEWY_STATUS_BAD_TREE;
-    if (slot < 0 || static_cast<int64_t>(slot) >= b.num_slots) flags |= TREEWY_STATUS_BAD_SLOT;
-    if constexpr (FUSED) {
-      // the previous round's accepted node and tree range for this request
-      if (pa != -1) {
-        const int pn = phi - plo;
-        if (pn < 0 || pn > prev.max_nodes) flags |= TREEWY_STATUS_TOO_MANY_NODES;
-        else if (plo < 0 || static_cast<int64_t>(phi) > prev.T) flags |= TREEWY_STATUS_BAD_TREE;
-        if (pa < -1 || pa >= pn) flags |= TREEWY_STATUS_BAD_ACCEPTED;
-        pv.tok0 = plo;
-        pv.N = pn;
-      }
-      pv.a = flags ? -1 : pa;
-    }
-    ts.tok0 = lo;
-    ts.N = flags ? 0 : N;
-    ts.slot = slot;
-    ts.flags = flags;
-    if (flags == 0 && (N > 0 || pa >= 0)) {
-      const int y = (slot * H + h) * kDim;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        mbar_arrive_expect_tx(&bars[c], kS0ChunkBytes);
-        tma_load_2d(s0 + c * kS0ChunkBytes, &map_s0, &bars[c], 32 * c, y);
-      }
-    }
-    if (flags == 0 && N > 0) {
-      const int N8 = (N + 7) & ~7;
-      const int Np = (N + 15) & ~15;
-      // 2 tensors x 2 column chunks x N8 rows x 128 bytes
-      mbar_arrive_expect_tx(&bars[4], static_cast<uint32_t>(N8) * 512u);
-      for (int c2 = 0; c2 < 2; ++c2) {
-        unsigned char* chunk = kq + c2 * kKQChunkBytes;
-        for (int rb = 0; rb < N8; rb += 8) {
-          tma_load_3d(chunk + rb * 128, &map_k, &bars[4], 64 * c2, h, lo + rb);
-          tma_load_3d(chunk + (Np + rb) * 128, &map_q, &bars[4], 64 * c2, h, lo + rb);
-        }
-      }
-    }
-  }
-  if (warp == 0) {
-    tmem_alloc(&tmem_holder, C::kCols);
-    tmem_relinquish();
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = tmem_holder;
-  const int N = ts.N;
-  const int Np = (N + 15) & ~15;
-  const int nch = Np / 16;
-  const bool issued = (ts.flags == 0 && N > 0);
-  int commit_a = -1;  // accepted node of the previous round still to be applied
-  if constexpr (FUSED) commit_a = pv.a;
-  const bool have_s0 = issued || commit_a >= 0;
-  const int64_t tok0 = ts.tok0;
-
-  // Column `lane` of V for the warpgroup that builds W.  Each thread loads the
-  // bf16 pair of columns (lane & ~1, lane | 1) of every other node (half the
-  // load requests of one 2-byte load per node), and neighbouring lanes swap
-  // halves after the tree is prepared.
-  uint32_t vpk[NPM / 2];
-#pragma unroll
-  for (int i = 0; i < NPM / 2; ++i) vpk[i] = 0u;
-  if (issued && wg == 1) {
-    const uint32_t* vg = reinterpret_cast<const uint32_t*>(b.v);
-    const int par = lane & 1;
-#pragma unroll
-    for (int i = 0; i < NPM / 2; ++i) {
-      const int n = 2 * i + par;
-      if (n < N) vpk[i] = __ldg(vg + (((tok0 + n) * H + h) * kDim + (lane & ~1)) / 2);
-    }
-  }
-
-  // the previous tree's parents and gates, requested before this tree's so
-  // that both round trips overlap
-  int prev_p = -1;
-  float prev_al = 0.f;
-  if constexpr (FUSED) {
-    if (commit_a >= 0 && t < pv.N) {
-      const int64_t row = static_cast<int64_t>(pv.tok0) + t;
-      prev_p = __ldg(prev.parent + row);
-      prev_al = __ldg(prev.alpha + row * H + h);
-    }
-  }
-
-  bool bad_tree = false;
-  if (issued) bad_tree = !prepare_tree(ts, pidx, pc, b, h);
-
-  // Fused commit: validate the previous tree, walk the accepted node's path and
-  // stage its first segment (k rows in shared memory, c_j u_j[lane] in registers).
-  bool bad_prev = false;
-  float cu[kPrevSeg];
-#pragma unroll
-  for (int j = 0; j < kPrevSeg; ++j) cu[j] = 0.f;
-  auto stage_prev = [&](int seg) {
-    if constexpr (FUSED) {
-      const int ns = min(kPrevSeg, pv.len - seg);
-      const uint32_t* kg = reinterpret_cast<const uint32_t*>(prev.k);
-      for (int e = t; e < ns * (kDim / 2); e += kThreads) {
-        const int j = e / (kDim / 2), w = e - j * (kDim / 2);
-        const int64_t row = (static_cast<int64_t>(pv.tok0) + pv.path[seg + j]) * H + h;
-        reinterpret_cast<uint32_t*>(&pv.k[j][0])[w] = __ldg(kg + row * (kDim / 2) + w);
-      }
-#pragma unroll
-      for (int j = 0; j < kPrevSeg; ++j) {
-        cu[j] = 0.f;
-        if (j < ns) {
-          const int64_t row = (static_cast<int64_t>(pv.tok0) + pv.path[seg + j]) * H + h;
-          cu[j] = pv.c[seg + j] * __ldg(prev.U + row * kDim + lane);
-        }
-      }
-    }
-  };
-  if constexpr (FUSED) {
-    if (commit_a >= 0) {
-      bool bad = false;
-      if (t < pv.N) {
-        bad = !(prev_p >= -1 && prev_p < t);
-        pv.parent[t] = prev_p;
-        pv.alpha[t] = prev_al;
-      }
-      bad_prev = __syncthreads_or(bad);
-      if (!bad_prev && t == 0) {
-        int len = 0;
-        float c = 1.0f;
-        for (int cur = commit_a; cur >= 0; cur = pv.parent[cur]) {
-          pv.path[len] = static_cast<uint8_t>(cur);
-          pv.c[len] = c;
-          c *= pv.alpha[cur];
-          ++len;
-        }
-        pv.len = len;
-        pv.gamma_a = c;
-      }
-      __syncthreads();
-      if (!bad_prev) stage_prev(0);
-      __syncthreads();
-    }
-  }
-  const bool commit_now = commit_a >= 0 && !bad_prev;
-  if (wg == 1) {
-    const int par = lane & 1;
-#pragma unroll
-    for (int i = 0; i < NPM / 2; ++i) {
-      // this lane holds a column pair of node 2i+par, its neighbour of node 2i+1-par
-      const uint32_t mine2 = vpk[i];
-      const uint32_t other = __shfl_xor_sync(0xffffffffu, mine2, 1);
-      // node 2i: from the even lane's load; node 2i+1: from the odd lane's load
-      const uint32_t n0 = par ? other : mine2;   // node 2i columns pair
-      const uint32_t n1 = par ? mine2 : other;   // node 2i+1 columns pair
-      const uint32_t v0 = par ? (n0 >> 16) : (n0 & 0xFFFFu);
-      const uint32_t v1 = par ? (n1 >> 16) : (n1 & 0xFFFFu);
-      vpk[i] = v0 | (v1 << 16);
-    }
-  }
-
-  // S0 chunks -> [hi | lo] bf16: warpgroup wg converts chunks 2wg, 2wg+1 of row
-  // `lane`.  Waits on an mbarrier are done by one thread per warpgroup; the
-  // others sleep at a hardware barrier instead of spinning.
-  int fail = 0;
-  if (have_s0 && !bad_prev) {
-    if (lane == 0) fail = !(mbar_wait(&bars[2 * wg], 0) && mbar_wait(&bars[2 * wg + 1], 0));
-    fail = wg ? named_bar_or<2, 128>(fail) : named_bar_or<1, 128>(fail);
-  }
-  if constexpr (FUSED) {
-    // S_a = gamma_a S0 + sum_j c_j u_j k_j^T on this thread's own fp32 row
-    // segments (chunks 2wg, 2wg+1 of row `lane`), written back to the pool once.
-    if (commit_now && !__syncthreads_or(fail)) {
-      const float ga = pv.gamma_a;
-      for (int seg = 0; seg < pv.len; seg += kPrevSeg) {
-        if (seg > 0) {
-          __syncthreads();
-          stage_prev(seg);
-          __syncthreads();
-        }
-        const int ns = min(kPrevSeg, pv.len - seg);
-        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-          unsigned char* row = s0 + c * kS0ChunkBytes + lane * 128;
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            float4 x = *reinterpret_cast<const float4*>(row + ((g ^ (lane & 7)) << 4));
-            if (seg == 0) {
-              x.x *= ga;
-              x.y *= ga;
-              x.z *= ga;
-              x.w *= ga;
-            }
-            const int col = 32 * c + 4 * g;
-#pragma unroll
-            for (int j = 0; j < kPrevSeg; ++j) {
-              if (j < ns) {
-                const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.k[j][col]));
-                const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.k[j][col + 2]));
-                x.x = fmaf(cu[j], k01.x, x.x);
-                x.y = fmaf(cu[j], k01.y, x.y);
-                x.z = fmaf(cu[j], k23.x, x.z);
-                x.w = fmaf(cu[j], k23.y, x.w);
-              }
-            }
-            *reinterpret_cast<float4*>(row + ((g ^ (lane & 7)) << 4)) = x;
-          }
-        }
-      }
-      // S_a goes back to the pool by two bulk tensor stores per warpgroup
-      // (the tile layout in shared memory is the one the loads produced);
-      // the chunks are converted in place only after the stores have read them
-      fence_proxy_async_smem();
-      if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
-      if (lane == 0) {
-        const int y = (ts.slot * H + h) * kDim;
-        tma_store_2d(&map_s0, s0 + (2 * wg) * kS0ChunkBytes, 32 * (2 * wg), y);
-        tma_store_2d(&map_s0, s0 + (2 * wg + 1) * kS0ChunkBytes, 32 * (2 * wg + 1), y);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-      }
-      if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
-    }
-  }
-  if (issued && !fail && !bad_tree && !bad_prev) {
-    convert_row_hilo(s0 + (2 * wg) * kS0ChunkBytes + lane * 128, lane & 7);
-    convert_row_hilo(s0 + (2 * wg + 1) * kS0ChunkBytes + lane * 128, lane & 7);
-  }
-  fence_proxy_async_smem();
-  fail = __syncthreads_or(fail);
-
-  const bool work = issued && !bad_tree && !bad_prev;
-  if (work && !fail && t == 0) {
-    if (!mbar_wait(&bars[4], 0)) {
-      s_fail = 1;
-    } else {
-      tc_fence_after_sync();
-      const uint64_t da = smem_desc_sw128(smem_addr(s0), 1024);
-      const uint64_t db = smem_desc_sw128(smem_addr(kq), 1024);
-      // S0 [K;Q]^T first: its completion frees the S0 region for W^T while the
-      // Gram still runs; the Gram's commit covers both products, after which
-      // the K/Q region and the rest of the S0 region are free.
-      const uint32_t id1 = idesc_bf16_f32(128, 2 * Np);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const uint64_t bd = db + (((c >> 1) * kKQChunkBytes + (c & 1) * 64 + s * 32) >> 4);
-          const uint64_t ahi = da + ((c * kS0ChunkBytes + s * 32) >> 4);
-          const uint64_t alo = da + ((c * kS0ChunkBytes + 64 + s * 32) >> 4);
-          mma_bf16(tmem, ahi, bd, id1, (c | s) ? 1u : 0u);
-          mma_bf16(tmem, alo, bd, id1, 1u);
-        }
-      }
-      mma_commit(&bars[5]);
-      const uint32_t id2 = idesc_bf16_f32(128, Np);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint64_t dsc = db + (((s >> 2) * kKQChunkBytes + (s & 3) * 32) >> 4);
-        mma_bf16(tmem + 2 * NPM, dsc, dsc, id2, s ? 1u : 0u);
-      }
-      mma_commit(&bars[7]);
-      mma_issued = true;
-    }
-  }
-  __syncthreads();
-  fail |= s_fail;
-
-  if (work && !fail) {
-    // warpgroup 1 (W^T) waits for S0 [K;Q]^T, warpgroup 0 for the Gram (both products)
-    if (lane == 0 && !mbar_wait(&bars[wg ? 5 : 7], 0)) fail = 1;
-    fail = wg ? named_bar_or<2, 128>(fail) : named_bar_or<1, 128>(fail);
-    tc_fence_after_sync();
-    if (fail) {
-      // skip this warpgroup's work; the join below reports the failure
-    } else if (wg == 0) {
-      // ---- ancestor coefficients from this lane's Gram row.  The row is
-      //      dumped to shared memory (thread-private, XOR-swizzled, in the
-      //      [T;B] area that is written only later), then each lane walks its
-      //      own node's path: A entries for lanes < N, M entries for lanes
-      //      Np..Np+N-1.
-      float* gdump = reinterpret_cast<float*>(s0 + kThiOff);  // 128 rows x 64 floats
-      const int gsw = lane & 31;
-      uint32_t ga[16], gb[16];
-      tmem_ld16_async(tmem + lane_base + 2 * NPM, ga);
-#pragma unroll
-      for (int c = 0; c < NPM / 16; ++c) {
-        if (c < nch) {
-          uint32_t(&cur)[16] = (c & 1) ? gb : ga;
-          uint32_t(&nxt)[16] = (c & 1) ? ga : gb;
-          tmem_wait16(cur);
-          if (c + 1 < nch) tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * (c + 1), nxt);
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            gdump[lane * 64 + ((16 * c + j) ^ gsw)] = __uint_as_float(cur[j]);
-        }
-      }
-      const bool isA = lane < N;
-      const int myn = isA ? lane : ((lane >= Np && lane < Np + N) ? lane - Np : -1);
-      if (myn >= 0) {
-        const int Dn = ts.D[myn], offn = ts.off[myn];
-        const float scale = isA ? ts.bbg[myn].x : 1.0f;
-        float* dst = isA ? aco : mco;
-        const int k0 = isA ? 1 : 0;  // A has strict ancestors only
-        if (Dn <= kRegPath) {
-#pragma unroll
-          for (int k = 0; k < kRegPath; ++k) {
-            if (k >= k0 && k < Dn) {
-              const int i = pidx[offn + k];
-              dst[offn + k] = scale * pc[offn + k] * gdump[lane * 64 + (i ^ gsw)];
-            }
-          }
-        } else {
-          for (int k = k0; k < Dn; ++k) {
-            const int i = pidx[offn + k];
-            dst[offn + k] = scale * pc[offn + k] * gdump[lane * 64 + (i ^ gsw)];
-          }
-        }
-      }
-    } else {
-      // ---- row `lane` of W^T: W[n][d] = beta_n v_n[d] - beta_n gamma_n (S0 k_n)[d]
-      unsigned char* whi = s0 + kWhiOff + lane * 128;
-      unsigned char* wlo = s0 + kWloOff + lane * 128;
-      const int sw = lane & 7;
-      uint32_t pa[16], pb[16];
-      tmem_ld16_async(tmem + lane_base, pa);
-#pragma unroll
-      for (int c = 0; c < NPM / 16; ++c) {
-        if (c < nch) {
-          uint32_t(&cur)[16] = (c & 1) ? pb : pa;
-          uint32_t(&nxt)[16] = (c & 1) ? pa : pb;
-          tmem_wait16(cur);
-          if (c + 1 < nch) tmem_ld16_async(tmem + lane_base + 16 * (c + 1), nxt);
-          float w[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = 16 * c + j;
-            const uint32_t pair = vpk[n >> 1];
-            const float vv = bf16_bits_to_float(static_cast<uint16_t>((n & 1) ? (pair >> 16) : pair));
-            const float2 bb = ts.bbg[n];
-            w[j] = (n < N) ? fmaf(-bb.y, __uint_as_float(cur[j]), bb.x * vv) : 0.f;
-          }
-          uint32_t hi[8], lo[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) split_pair(w[2 * j], w[2 * j + 1], hi[j], lo[j]);
-#pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            const int gg = 2 * c + g;
-            *reinterpret_cast<uint4*>(whi + ((gg ^ sw) << 4)) =
-                make_uint4(hi[4 * g], hi[4 * g + 1], hi[4 * g + 2], hi[4 * g + 3]);
-            *reinterpret_cast<uint4*>(wlo + ((gg ^ sw) << 4)) =
-                make_uint4(lo[4 * g], lo[4 * g + 1], lo[4 * g + 2], lo[4 * g + 3]);
-          }
-        }
-      }
-    }
-    if (wg == 0 && !fail) {
-      named_bar_sync<1, 128>();
-      // ---- T rows (threads 0..N-1) and B rows (threads 64..64+N-1) together;
-      //      the padding rows of [T;B] are zeroed by the lanes that own them
-      if ((t >= N && t < Np) || (t >= Np + N && t < 2 * Np)) zero_operand_row(thi, tlo, t);
-      if (t < N) build_path_row(ts, t, t, pidx, aco, nullptr, xT, thi, tlo);
-      if (t >= 64 && t - 64 < N) build_path_row(ts, t - 64, Np + t - 64, pidx, aco, mco, xB, thi, tlo);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    fail = __syncthreads_or(fail);
-    if (!fail && t == 0) {
-      tc_fence_after_sync();
-      // [U | O] = W^T [T;B]^T as one N = 2Np product into the columns after the
-      // (consumed) Gram; S0 q_n stays in columns Np..2Np-1.
-      const uint64_t da = smem_desc_sw128(smem_addr(s0), 1024);
-      const uint32_t id = idesc_bf16_f32(128, 2 * Np);
-#pragma unroll
-      for (int s = 0; s < NPM / 16; ++s) {
-        if (s < nch) {
-          const uint32_t ko = s * 32;
-          const uint64_t whi = da + ((kWhiOff + ko) >> 4);
-          const uint64_t wlo = da + ((kWloOff + ko) >> 4);
-          const uint64_t thd = da + ((kThiOff + ko) >> 4);
-          const uint64_t tld = da + ((kTloOff + ko) >> 4);
-          mma_bf16(tmem + 2 * NPM, whi, thd, id, s ? 1u : 0u);
-          mma_bf16(tmem + 2 * NPM, wlo, thd, id, 1u);
-          mma_bf16(tmem + 2 * NPM, whi, tld, id, 1u);
-        }
-      }
-      mma_commit(&bars[6]);
-      mma2_issued = true;
-    }
-    if (!fail && t == 0 && !mbar_wait(&bars[6], 0)) fail = 1;
-    fail = __syncthreads_or(fail);
-    if (!fail) {
-      tc_fence_after_sync();
-      // ---- U[n] and o_n = gamma_n S0 q_n + O[n], column d = lane; warpgroup
-      //      wg stores nodes 8wg..8wg+7 of every 16-node chunk
-      float* og = b.o + (tok0 * H + h) * kDim + lane;
-      float* ug = b.U + (tok0 * H + h) * kDim + lane;
-      const int64_t stride = static_cast<int64_t>(H) * kDim;
-      for (int c = 0; c < nch; ++c) {
-        uint32_t u[16], oo[16], pq[16];
-        tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * c, u);
-        tmem_ld16_async(tmem + lane_base + 2 * NPM + Np + 16 * c, oo);
-        tmem_ld16_async(tmem + lane_base + Np + 16 * c, pq);
-        tmem_wait16(u);
-        tmem_regs_ready(oo);
-        tmem_regs_ready(pq);
-        auto emit = [&](int j) {
-          const int n = 16 * c + j;
-          if (n < N) {
-            ug[n * stride] = __uint_as_float(u[j]);
-            og[n * stride] = fmaf(ts.gamma[n], __uint_as_float(pq[j]), __uint_as_float(oo[j]));
-          }
-        };
-        if (wg == 0) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) emit(j);
-        } else {
-#pragma unroll
-          for (int j = 8; j < 16; ++j) emit(j);
-        }
-      }
-      if (b.gamma != nullptr && t < N) b.gamma[(tok0 + t) * H + h] = ts.gamma[t];
-    }
-  }
-
-  if (t == 0) {
-    int bits = (fail ? kStatusTimeout : 0);
-    if (h == 0) bits |= ts.flags | ((bad_tree || bad_prev) ? TREEWY_STATUS_BAD_TREE : 0);
-    if (bits) atomicOr(b.status + r, bits);
-    // No async copy or MMA may still target this CTA's memory at exit.
-    if (have_s0)
-      for (int i = 0; i < 4; ++i) mbar_wait(&bars[i], 0);
-    if (issued) {
-      mbar_wait(&bars[4], 0);
-      if (mma_issued) {
-        mbar_wait(&bars[5], 0);
-        mbar_wait(&bars[7], 0);
-      }
-      if (mma2_issued) mbar_wait(&bars[6], 0);
-    }
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after_sync();
-    tmem_dealloc(tmem, C::kCols);
-  }
-}
-
-template <int NPM, bool FUSED>
-cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, const PrevRound& prev,
-                       cudaStream_t stream) {
-  static cudaError_t attr = cudaFuncSetAttribute(
-      verify_tc_kernel<NPM, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      static_cast<int>(TcCfg<NPM>::kDynSmem));
-  if (attr != cudaSuccess) return attr;
-  const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
-  verify_tc_kernel<NPM, FUSED><<<grid, kThreads, TcCfg<NPM>::kDynSmem, stream>>>(m.s0, m.k, m.q, b,
-                                                                                 prev);
-  return cudaGetLastError();
-}
-
-}  // namespace
 
 size_t verify_tc_smem(int npm) {
   if (npm <= 16) return TcCfg<16>::kDynSmem;
@@ -761,17 +13,15 @@ size_t verify_tc_smem(int npm) {
 
 cudaError_t launch_verify_tc(const treewy_batch& b, const VerifyMaps& maps, int npm,
                              cudaStream_t stream) {
-  const PrevRound none{};
-  if (npm <= 16) return launch_npm<16, false>(b, maps, none, stream);
-  if (npm <= 32) return launch_npm<32, false>(b, maps, none, stream);
-  return launch_npm<64, false>(b, maps, none, stream);
+  if (b.flags & TREEWY_FLAG_STATE_BF16) return launch_verify_tc_bf16state(b, maps, nullptr, npm, stream);
+  return launch_tc<false>(b, maps, nullptr, npm, stream);
 }
 
 cudaError_t launch_commit_verify_tc(const treewy_batch& next, const PrevRound& prev,
                                     const VerifyMaps& maps, int npm, cudaStream_t stream) {
-  if (npm <= 16) return launch_npm<16, true>(next, maps, prev, stream);
-  if (npm <= 32) return launch_npm<32, true>(next, maps, prev, stream);
-  return launch_npm<64, true>(next, maps, prev, stream);
+  if (next.flags & TREEWY_FLAG_STATE_BF16)
+    return launch_verify_tc_bf16state(next, maps, &prev, npm, stream);
+  return launch_tc<false>(next, maps, &prev, npm, stream);
 }
 
 }  // namespace treewy

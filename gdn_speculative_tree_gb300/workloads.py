@@ -240,14 +240,15 @@ class Workload:
 def assemble(trees: Sequence[np.ndarray], accepted: np.ndarray, H: int, dk: int, dv: int,
              qkv_dtype: str, s0_std: float, alpha_range: Tuple[float, float], beta: Tuple,
              seed: int, device="cpu", max_nodes: Optional[int] = None,
-             extra_slots: int = 0) -> Workload:
+             extra_slots: int = 0, state_dtype: str = "f32") -> Workload:
     """Draw the per-node and per-head tensors for the given trees.
 
     Draw order (one torch generator seeded with ``seed``): slot permutation,
     S0, q, k, v, alpha, beta.  q and k are drawn N(0,1) in fp32 and divided by
     their L2 norm (no epsilon) before rounding to the qkv dtype (round to
     nearest even); beta of kind "sigmoid" is sigmoid(N(0,1)) evaluated in fp64
-    and rounded to fp32.
+    and rounded to fp32.  A bf16 state pool (``state_dtype="bf16"``) is the
+    same fp32 draw rounded to nearest even bf16.
     """
     R = len(trees)
     sizes = np.array([len(t) for t in trees], dtype=np.int64)
@@ -266,6 +267,10 @@ def assemble(trees: Sequence[np.ndarray], accepted: np.ndarray, H: int, dk: int,
     perm = torch.randperm(num_slots, generator=g, device=dev)[:R].to(torch.int32)
 
     state = torch.randn(num_slots, H, dv, dk, generator=g, device=dev, dtype=torch.float32) * s0_std
+    if state_dtype == "bf16":
+        state = state.to(torch.bfloat16)
+    elif state_dtype != "f32":
+        raise ValueError(f"state_dtype {state_dtype!r} is not 'f32' or 'bf16'")
 
     def unit(shape):
         x = torch.randn(*shape, generator=g, device=dev, dtype=torch.float32)
@@ -300,7 +305,7 @@ def assemble(trees: Sequence[np.ndarray], accepted: np.ndarray, H: int, dk: int,
 
 
 def generate(cfg: WorkloadConfig, R: Optional[int] = None, layer: int = 0, device="cpu",
-             extra_slots: int = 0) -> Workload:
+             extra_slots: int = 0, state_dtype: str = "f32") -> Workload:
     """Seeded inputs for one GDN layer of a configuration (optionally fewer requests).
 
     Trees and accepted nodes depend only on (cfg.seed, R); tensors use the
@@ -309,7 +314,7 @@ def generate(cfg: WorkloadConfig, R: Optional[int] = None, layer: int = 0, devic
     trees, accepted = make_trees(cfg, R)
     return assemble(trees, accepted, cfg.H, cfg.dk, cfg.dv, cfg.qkv_dtype, cfg.s0_std,
                     cfg.alpha_range, cfg.beta, seed=cfg.seed * 1000 + layer, device=device,
-                    extra_slots=extra_slots)
+                    extra_slots=extra_slots, state_dtype=state_dtype)
 
 
 def as_float64(x: torch.Tensor) -> np.ndarray:

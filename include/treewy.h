@@ -76,7 +76,15 @@ enum {
 enum {
   /* Use the portable CUDA-core kernel even where the tensor-core kernel
      applies (dk = dv = 128, bf16 q/k/v).  Same results within rounding. */
-  TREEWY_FLAG_FORCE_GENERIC = 1u
+  TREEWY_FLAG_FORCE_GENERIC = 1u,
+  /* The state pool holds bf16 instead of f32: the dtype in which the GDN
+     state is kept when serving (paper §2 "The memory problem": dv x dk x 2 B
+     per head), half the bytes of every state read and write.  Verification
+     takes the bf16 S0 as exact values; commit forms S_a in f32 and stores it
+     rounded to nearest (ties to even) bf16, so each committed element is
+     within 2^-8 of its relative value.  The storeall comparator entry points
+     reject this flag with TREEWY_ERR_UNSUPPORTED. */
+  TREEWY_FLAG_STATE_BF16 = 2u
 };
 
 /* Largest draft tree per request. */
@@ -98,7 +106,8 @@ enum {
  *   v            bf16|f32 [T][H][dv]   (16-byte aligned base)
  *   alpha, beta  f32 [T][H]       decay gate and write strength, in (0,1)
  *   state        f32 [num_slots][H][dv][dk]  committed states S0 (row d of a
- *                                 head's state holds S0[d][0..dk-1]); 16-byte aligned
+ *                                 head's state holds S0[d][0..dk-1]); 16-byte aligned;
+ *                                 bf16, same shape, with TREEWY_FLAG_STATE_BF16
  *   state_slot   int32 [R]        pool slot of each request, in [0, num_slots)
  *   o            f32 [T][H][dv]   verify output o_n
  *   U            f32 [T][H][dv]   verify output u_n, commit input (keep it
@@ -123,7 +132,7 @@ typedef struct treewy_batch {
   const void* v;
   const float* alpha;
   const float* beta;
-  float* state;
+  void* state;                    /* f32, or bf16 with TREEWY_FLAG_STATE_BF16 */
   const int32_t* state_slot;
   float* o;
   float* U;

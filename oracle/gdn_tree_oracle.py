@@ -111,14 +111,48 @@ def verify_request(S0: np.ndarray, parent: Sequence[int], q: np.ndarray, k: np.n
     return RequestResult(o=o, U=U, gamma=gamma, states=states)
 
 
-def commit_request(S0: np.ndarray, result: RequestResult, accepted: int) -> np.ndarray:
-    """The state that becomes the next round's S0: S_a, or S0 when a = -1."""
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round fp64 values to the nearest bfloat16 value, ties to even.
+
+    bfloat16 has the binary32 exponent range and 8 significant bits.  Writing
+    x = m 2^e with 1/2 <= |m| < 1, its neighbours in bfloat16 are the
+    multiples of 2^(e-8), so the nearest one is rint(m 2^8) 2^(e-8), with
+    numpy's rint rounding halves to even.  The rounding is taken once, from
+    fp64 (no intermediate fp32).  Only normal-range values occur here;
+    anything below the smallest normal bfloat16 or above the largest finite
+    one raises.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    nz = x != 0
+    if np.any(nz & ((e < -125) | (e > 128))) or not np.all(np.isfinite(x)):
+        raise ValueError("value outside the normal bfloat16 range")
+    out = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+    if np.any(np.isinf(out)):
+        raise ValueError("value rounds past the largest finite bfloat16")
+    return out
+
+
+def commit_request(S0: np.ndarray, result: RequestResult, accepted: int,
+                   state_dtype: str = "f32") -> np.ndarray:
+    """The state that becomes the next round's S0: S_a, or S0 when a = -1.
+
+    With a bf16 state pool (the serving dtype of the GDN state, TreeWY paper
+    §2 "The memory problem": 2 bytes per element) the committed value is S_a
+    rounded to the nearest bf16 (ties to even); S0 of a bf16 pool is already
+    a bf16 value and is returned unchanged for a = -1.
+    """
     a = int(accepted)
     if a < 0:
         return np.array(S0, dtype=np.float64, copy=True)
     if a >= result.states.shape[0]:
         raise ValueError(f"accepted node {a} outside the tree")
-    return result.states[a].copy()
+    S_a = result.states[a].copy()
+    if state_dtype == "bf16":
+        return round_to_bf16(S_a)
+    if state_dtype != "f32":
+        raise ValueError(f"state_dtype {state_dtype!r}")
+    return S_a
 
 
 def verify_batch(node_offset: np.ndarray, parent: np.ndarray, q: np.ndarray, k: np.ndarray,

@@ -124,3 +124,41 @@ def test_commit_verify_rejects_inconsistent_rounds(lib):
         binding.TREEWY_ERR_INVALID_ARG
     assert lib.treewy_commit_verify(None, 0x10000, ctypes.byref(nxt), None) == \
         binding.TREEWY_ERR_INVALID_ARG
+
+
+def test_state_flags(lib):
+    b = _valid_batch()
+    b.flags = 4  # no such flag
+    assert lib.treewy_verify(ctypes.byref(b), None) == binding.TREEWY_ERR_INVALID_ARG
+    assert b"unknown bits" in lib.treewy_last_error()
+    b = _valid_batch()
+    b.flags = binding.FLAG_STATE_BF16
+    assert lib.treewy_storeall_verify(ctypes.byref(b), 0x10000, None) == binding.TREEWY_ERR_UNSUPPORTED
+    assert lib.treewy_storeall_commit(ctypes.byref(b), 0x10000, 0x10000, None) == \
+        binding.TREEWY_ERR_UNSUPPORTED
+    prev, nxt = _valid_batch(), _valid_batch()
+    nxt.flags = binding.FLAG_STATE_BF16
+    assert lib.treewy_commit_verify(ctypes.byref(prev), 0x10000, ctypes.byref(nxt), None) == \
+        binding.TREEWY_ERR_INVALID_ARG
+    assert b"STATE_BF16" in lib.treewy_last_error()
+
+
+def test_make_batch_sets_the_state_flag():
+    torch = pytest.importorskip("torch")
+    from gdn_speculative_tree_gb300 import workloads as wl
+    w = wl.assemble([wl.chain_parents(3)], [1], 2, 16, 16, "bf16", 0.05, (0.9, 0.999), ("sigmoid",),
+                    seed=1, state_dtype="bf16")
+    assert w.state.dtype == torch.bfloat16
+    o = torch.empty(w.T, w.H, w.dv)
+    st = torch.zeros(w.R, dtype=torch.int32)
+    b = binding.make_batch(node_offset=w.node_offset, parent=w.parent, q=w.q, k=w.k, v=w.v,
+                           alpha=w.alpha, beta=w.beta, state=w.state, state_slot=w.state_slot,
+                           o=o, U=o, status=st)
+    assert b.flags == binding.FLAG_STATE_BF16
+    w32 = wl.assemble([wl.chain_parents(3)], [1], 2, 16, 16, "bf16", 0.05, (0.9, 0.999),
+                      ("sigmoid",), seed=1)
+    assert torch.equal(w32.state.to(torch.bfloat16), w.state)  # same draw, rounded
+    with pytest.raises(TypeError):
+        binding.make_batch(node_offset=w.node_offset, parent=w.parent, q=w.q, k=w.k, v=w.v,
+                           alpha=w.alpha, beta=w.beta, state=w.state.half(),
+                           state_slot=w.state_slot, o=o, U=o, status=st)

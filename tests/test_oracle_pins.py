@@ -327,3 +327,48 @@ def test_pins_accept_the_oracle():
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_pins_catch_planted_mistake(name):
     assert not pins_pass(mutant(name))
+
+
+# ------------------------------------------------------------ bf16 state rounding
+
+def test_round_to_bf16_hand_cases():
+    """Nearest bfloat16 (8 significant bits), ties to even, from fp64 in one step."""
+    cases = [
+        (1.0 + 2.0 ** -8, 1.0),                    # tie: stays on the even neighbour 1
+        (1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -6),    # tie: goes up to the even neighbour
+        (-(1.0 + 2.0 ** -8), -1.0),                # sign symmetric
+        (1.0 + 2.0 ** -8 + 2.0 ** -30, 1.0 + 2.0 ** -7),  # just above a tie: up (no fp32 step)
+        (255.5, 256.0),                            # tie at the top of a binade carries
+        (1.0 - 2.0 ** -9, 1.0),                    # tie below 1 (spacing 2^-8 there)
+        (0.0, 0.0),
+        (3.0, 3.0),
+        (0.1, 0.10009765625),                      # 0x3DCD
+    ]
+    x = np.array([c[0] for c in cases])
+    want = np.array([c[1] for c in cases])
+    assert np.array_equal(orc.round_to_bf16(x), want)
+
+
+def test_round_to_bf16_matches_torch_on_fp32_inputs():
+    """On fp32 inputs the one-step rounding equals torch's float32 -> bfloat16
+    conversion (round to nearest even), a library routine."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(17)
+    x = np.concatenate([rng.standard_normal(200000) * 0.05, rng.standard_normal(2000) * 1e3,
+                        rng.uniform(-1, 1, 2000) * 1e-20]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(orc.round_to_bf16(x.astype(np.float64)), ref)
+
+
+def test_commit_bf16_state_rounds_the_accepted_state():
+    rng = np.random.default_rng(23)
+    parent = np.array([-1, 0, 1, 0])
+    q, k, v, alpha, beta, S0 = random_head(rng, 4, 3, 5)
+    S0 = orc.round_to_bf16(S0)
+    res = orc.verify_request(S0[None], parent, q[:, None], k[:, None], v[:, None], alpha[:, None],
+                             beta[:, None])
+    S_f = orc.commit_request(S0[None], res, 2)
+    S_b = orc.commit_request(S0[None], res, 2, state_dtype="bf16")
+    assert np.array_equal(S_b, orc.round_to_bf16(S_f))
+    assert np.all(np.abs(S_b - S_f) <= 2.0 ** -8 * np.abs(S_f))
+    assert np.array_equal(orc.commit_request(S0[None], res, -1, state_dtype="bf16"), S0[None])
