@@ -1,0 +1,278 @@
+// commit_tma.cu -- reconstruct-on-commit for dk = dv = 128 with the state
+// tile moved by TMA (TreeWY paper §3 "Reconstruct on commit", Eq. (3);
+// technical review §3.3, Eq. (6)):
+//
+//   S_a = gamma_a S0 + sum_{i on the root-to-a path} (gamma_a / gamma_i) u_i k_i^T.
+//
+// One CTA of 128 threads per (request, head); thread d owns state row d.
+// The state block (64 KB f32 or 32 KB bf16) is requested by one bulk tensor
+// load as soon as the request's slot is known, lands in shared memory in the
+// 128-byte-swizzled tile layout, is updated there row by row while the path's
+// u and k rows are staged, and leaves by bulk tensor stores.  Nothing of the
+// state passes through registers while in flight, so several CTAs per SM
+// (3 for f32, 5 for bf16) keep enough bytes in flight to stream HBM.
+#include "treewy_device.cuh"
+#include "treewy_internal.h"
+
+namespace treewy {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kSeg = 16;                            // path nodes staged per pass
+constexpr uint32_t kChunkBytes = 128u * 128u;       // 128 rows x 128 bytes
+
+template <bool SB>
+struct CommitCfg {
+  static constexpr int kChunks = SB ? 2 : 4;        // 32 KB bf16 / 64 KB f32
+  static constexpr int kChunkCols = SB ? 64 : 32;
+  static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
+  static constexpr uint32_t kDynSmem = kTileBytes + 1024u;  // + alignment slack
+};
+
+struct CommitSmem {
+  int parent[kMaxNodes];
+  float alpha[kMaxNodes];
+  float c[kMaxNodes];                 // gamma_a / gamma_{path j} (alpha products)
+  uint8_t path[kMaxNodes];            // a, parent(a), ..., root
+  float k[kSeg][128];                 // staged k rows of one pass
+  int tok0, N, slot, a, flags, len;
+  float gamma_a;
+};
+
+// Columns 32 blk .. 32 blk + 31 of row d of the swizzled tile, as f32.
+template <bool SB>
+__device__ __forceinline__ void load_block(const unsigned char* tile, int d, int blk, float (&x)[32]) {
+  if constexpr (SB) {
+    const unsigned char* row = tile + (blk >> 1) * kChunkBytes + d * 128;
+#pragma unroll
+    for (int g4 = 0; g4 < 4; ++g4) {
+      const int g = 4 * (blk & 1) + g4;
+      const uint4 raw = *reinterpret_cast<const uint4*>(row + ((g ^ (d & 7)) << 4));
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[8 * g4 + 2 * i] = __uint_as_float(w[i] << 16);
+        x[8 * g4 + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+  } else {
+    const unsigned char* row = tile + blk * kChunkBytes + d * 128;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const float4 v = *reinterpret_cast<const float4*>(row + ((g ^ (d & 7)) << 4));
+      x[4 * g] = v.x;
+      x[4 * g + 1] = v.y;
+      x[4 * g + 2] = v.z;
+      x[4 * g + 3] = v.w;
+    }
+  }
+}
+
+template <bool SB>
+__device__ __forceinline__ void store_block(unsigned char* tile, int d, int blk, const float (&x)[32]) {
+  if constexpr (SB) {
+    unsigned char* row = tile + (blk >> 1) * kChunkBytes + d * 128;
+#pragma unroll
+    for (int g4 = 0; g4 < 4; ++g4) {
+      const int g = 4 * (blk & 1) + g4;
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(x[8 * g4 + 2 * i], x[8 * g4 + 2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+      *reinterpret_cast<uint4*>(row + ((g ^ (d & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    unsigned char* row = tile + blk * kChunkBytes + d * 128;
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      *reinterpret_cast<float4*>(row + ((g ^ (d & 7)) << 4)) =
+          make_float4(x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
+  }
+}
+
+template <bool SB>
+__global__ void __launch_bounds__(kThreads)
+    commit_tma_kernel(const __grid_constant__ CUtensorMap map_s, const treewy_batch b,
+                      const int32_t* __restrict__ accepted) {
+  using C = CommitCfg<SB>;
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ CommitSmem cs;
+  __shared__ __align__(8) uint64_t bar;
+  unsigned char* tile = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
+
+  const int H = b.H;
+  const int r = blockIdx.x / H;
+  const int h = blockIdx.x - r * H;
+  const int t = threadIdx.x;  // = state row d
+  const bool kbf16 = b.qkv_dtype == TREEWY_DTYPE_BF16;
+
+  if (t == 0) {
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+    // independent loads: one round trip
+    const int a = accepted[r];
+    const int lo = b.node_offset[r], hi = b.node_offset[r + 1];
+    const int slot = b.state_slot[r];
+    const int N = hi - lo;
+    int flags = 0;
+    if (a != -1) {
+      if (N < 0 || N > b.max_nodes) flags |= TREEWY_STATUS_TOO_MANY_NODES;
+      else if (lo < 0 || static_cast<int64_t>(hi) > b.T) flags |= TREEWY_STATUS_BAD_TREE;
+      if (a < -1 || a >= N) flags |= TREEWY_STATUS_BAD_ACCEPTED;
+      if (slot < 0 || static_cast<int64_t>(slot) >= b.num_slots) flags |= TREEWY_STATUS_BAD_SLOT;
+    }
+    cs.tok0 = lo;
+    cs.N = N;
+    cs.slot = slot;
+    cs.flags = flags;
+    cs.a = flags ? -1 : a;
+    if (a != -1 && flags == 0) {
+      const int y = (slot * H + h) * 128;
+      mbar_arrive_expect_tx(&bar, C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_2d(tile + c * kChunkBytes, &map_s, &bar, C::kChunkCols * c, y);
+    }
+  }
+  __syncthreads();
+  const int a = cs.a;
+  if (a < 0) {
+    // nothing accepted (state neither read nor written) or a bad request
+    if (t == 0 && h == 0 && cs.flags) atomicOr(b.status + r, cs.flags);
+    return;
+  }
+  const int64_t tok0 = cs.tok0;
+  const int N = cs.N;
+
+  // the whole tree is validated (U of an invalid tree was never written)
+  bool bad = false;
+  if (t < N) {
+    const int p = __ldg(b.parent + tok0 + t);
+    bad = !(p >= -1 && p < t);
+    cs.parent[t] = p;
+    cs.alpha[t] = __ldg(b.alpha + (tok0 + t) * H + h);
+  }
+  bad = __syncthreads_or(bad);
+  if (!bad && t == 0) {
+    int len = 0;
+    float c = 1.0f;
+    for (int cur = a; cur >= 0; cur = cs.parent[cur]) {
+      cs.path[len] = static_cast<uint8_t>(cur);
+      cs.c[len] = c;
+      c *= cs.alpha[cur];
+      ++len;
+    }
+    cs.len = len;
+    cs.gamma_a = c;
+  }
+  __syncthreads();
+
+  // stage pass `s`: k rows in shared memory, c_j u_j[d] in registers
+  float cu[kSeg];
+  auto stage = [&](int s) {
+    const int ns = min(kSeg, cs.len - s * kSeg);
+    for (int e = t; e < ns * 128; e += kThreads) {
+      const int j = e >> 7, x = e & 127;
+      const int64_t row = (tok0 + cs.path[s * kSeg + j]) * H + h;
+      cs.k[j][x] = load_qkv(b.k, row * 128 + x, kbf16);
+    }
+#pragma unroll
+    for (int j = 0; j < kSeg; ++j) {
+      cu[j] = 0.f;
+      if (j < ns) {
+        const int64_t row = (tok0 + cs.path[s * kSeg + j]) * H + h;
+        cu[j] = cs.c[s * kSeg + j] * __ldg(b.U + row * 128 + t);
+      }
+    }
+  };
+  if (!bad) stage(0);
+
+  int fail = 0;
+  if (t == 0) fail = !mbar_wait(&bar, 0);
+  fail = __syncthreads_or(fail);
+  if (bad || fail) {
+    if (t == 0) {
+      if (fail) mbar_wait(&bar, 0);  // nothing may still target this CTA's memory
+      atomicOr(b.status + r, (fail ? kStatusTimeout : 0) | ((bad && h == 0) ? TREEWY_STATUS_BAD_TREE : 0));
+    }
+    return;
+  }
+
+  // row t, 32 columns at a time, f32 across every pass, stored once
+  const int len = cs.len;
+  const int nseg = (len + kSeg - 1) / kSeg;
+  const float ga = cs.gamma_a;
+  int staged = 0;
+  for (int blk = 0; blk < 4; ++blk) {
+    float x[32];
+    load_block<SB>(tile, t, blk, x);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) x[e] *= ga;
+    for (int s = 0; s < nseg; ++s) {
+      if (s != staged) {
+        __syncthreads();
+        stage(s);
+        __syncthreads();
+        staged = s;
+      }
+      const int ns = min(kSeg, len - s * kSeg);
+#pragma unroll
+      for (int j = 0; j < kSeg; ++j) {
+        if (j < ns) {
+          const float u = cu[j];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 kk = *reinterpret_cast<const float4*>(&cs.k[j][32 * blk + e]);
+            x[e] = fmaf(u, kk.x, x[e]);
+            x[e + 1] = fmaf(u, kk.y, x[e + 1]);
+            x[e + 2] = fmaf(u, kk.z, x[e + 2]);
+            x[e + 3] = fmaf(u, kk.w, x[e + 3]);
+          }
+        }
+      }
+    }
+    store_block<SB>(tile, t, blk, x);
+  }
+
+  // S_a back to the pool; the tile must stay until the stores have read it
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (t == 0) {
+    const int y = (cs.slot * H + h) * 128;
+#pragma unroll
+    for (int c = 0; c < C::kChunks; ++c) tma_store_2d(&map_s, tile + c * kChunkBytes, C::kChunkCols * c, y);
+    bulk_commit_group();
+    bulk_wait_group_read0();
+  }
+}
+
+template <bool SB>
+cudaError_t launch(const treewy_batch& b, const CUtensorMap& map, const int32_t* accepted,
+                   cudaStream_t stream) {
+  static cudaError_t attr = [] {
+    cudaError_t e = cudaFuncSetAttribute(commit_tma_kernel<SB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(CommitCfg<SB>::kDynSmem));
+    if (e != cudaSuccess) return e;
+    // the whole unified L1/shared array as shared memory: 3 (f32) or 5 (bf16) CTAs per SM
+    return cudaFuncSetAttribute(commit_tma_kernel<SB>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  }();
+  if (attr != cudaSuccess) return attr;
+  const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
+  commit_tma_kernel<SB><<<grid, kThreads, CommitCfg<SB>::kDynSmem, stream>>>(map, b, accepted);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_commit_tma(const treewy_batch& b, const CUtensorMap& state_map,
+                              const int32_t* accepted, cudaStream_t stream) {
+  if (b.flags & TREEWY_FLAG_STATE_BF16) return launch<true>(b, state_map, accepted, stream);
+  return launch<false>(b, state_map, accepted, stream);
+}
+
+}  // namespace treewy

@@ -94,22 +94,30 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// State pool of a dk = dv = 128 batch as rows [slots*H*128][128]; one box =
+// 128 state rows x 128 bytes (32 f32 or 64 bf16 columns), 128-byte swizzle.
+treewy_status make_state_map(const treewy_batch* b, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return fail(TREEWY_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint32_t ones[2] = {1, 1};
+  const bool sb = (b->flags & TREEWY_FLAG_STATE_BF16) != 0;
+  const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(b->num_slots) * b->H * 128};
+  const cuuint64_t strides[1] = {128 * (sb ? 2u : 4u)};
+  const cuuint32_t box[2] = {sb ? 64u : 32u, 128};
+  CUresult rc = enc(map, sb ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                    b->state, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (rc != CUDA_SUCCESS) return fail(TREEWY_ERR_CUDA, "tensor map for state failed (%d)", (int)rc);
+  return TREEWY_OK;
+}
+
 treewy_status make_maps(const treewy_batch* b, treewy::VerifyMaps* m) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return fail(TREEWY_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const cuuint32_t ones[3] = {1, 1, 1};
-  {
-    // one box = 128 state rows x 128 bytes (32 f32 or 64 bf16 columns)
-    const bool sb = (b->flags & TREEWY_FLAG_STATE_BF16) != 0;
-    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(b->num_slots) * b->H * 128};
-    const cuuint64_t strides[1] = {128 * (sb ? 2u : 4u)};
-    const cuuint32_t box[2] = {sb ? 64u : 32u, 128};
-    CUresult rc = enc(&m->s0, sb ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                      2, b->state, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (rc != CUDA_SUCCESS) return fail(TREEWY_ERR_CUDA, "tensor map for state failed (%d)", (int)rc);
-  }
+  treewy_status st = make_state_map(b, &m->s0);
+  if (st != TREEWY_OK) return st;
   const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(b->H), static_cast<cuuint64_t>(b->T)};
   const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(b->H) * 128 * 2};
   const cuuint32_t box[3] = {64, 1, 8};
@@ -124,6 +132,22 @@ treewy_status make_maps(const treewy_batch* b, treewy::VerifyMaps* m) {
       return fail(TREEWY_ERR_CUDA, "tensor map for %s failed (%d)", i ? "q" : "k", (int)rc);
   }
   return TREEWY_OK;
+}
+
+// Commit with the bulk-copy kernel for dk = dv = 128 (unless the portable
+// kernels are forced), with the register-streaming kernel otherwise.
+treewy_status launch_commit_any(const treewy_batch* b, const int32_t* accepted, cudaStream_t stream,
+                                const char* what) {
+  cudaError_t err;
+  if (b->dk == 128 && b->dv == 128 && (b->flags & TREEWY_FLAG_FORCE_GENERIC) == 0) {
+    CUtensorMap map;
+    treewy_status st = make_state_map(b, &map);
+    if (st != TREEWY_OK) return st;
+    err = treewy::launch_commit_tma(*b, map, accepted, stream);
+  } else {
+    err = treewy::launch_commit(*b, accepted, stream);
+  }
+  return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, what);
 }
 
 }  // namespace
@@ -157,8 +181,7 @@ treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted, 
   if (st != TREEWY_OK || batch->R == 0) return st;
   if (!batch->U) return fail(TREEWY_ERR_INVALID_ARG, "U is NULL");
   if (!accepted) return fail(TREEWY_ERR_INVALID_ARG, "accepted is NULL");
-  cudaError_t err = treewy::launch_commit(*batch, accepted, stream);
-  return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_commit launch");
+  return launch_commit_any(batch, accepted, stream, "treewy_commit launch");
 }
 
 treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev_accepted,
@@ -197,8 +220,8 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
     return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_commit_verify launch");
   }
   // other shapes: the two kernels back to back on the same stream
-  err = treewy::launch_commit(*prev, prev_accepted, stream);
-  if (err != cudaSuccess) return cuda_fail(err, "treewy_commit_verify (commit) launch");
+  st = launch_commit_any(prev, prev_accepted, stream, "treewy_commit_verify (commit) launch");
+  if (st != TREEWY_OK) return st;
   return treewy_verify(next, stream);
 }
 

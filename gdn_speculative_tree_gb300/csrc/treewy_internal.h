@@ -47,6 +47,9 @@ cudaError_t launch_verify_tc_bf16state(const treewy_batch& b, const VerifyMaps& 
                                        const PrevRound* prev, int npm, cudaStream_t stream);
 
 cudaError_t launch_commit(const treewy_batch& b, const int32_t* accepted, cudaStream_t stream);
+// dk = dv = 128: the state tile moved by bulk tensor copies (state_map as VerifyMaps::s0).
+cudaError_t launch_commit_tma(const treewy_batch& b, const CUtensorMap& state_map,
+                              const int32_t* accepted, cudaStream_t stream);
 
 cudaError_t launch_storeall_verify(const treewy_batch& b, float* snapshots, cudaStream_t stream);
 cudaError_t launch_storeall_commit(const treewy_batch& b, const float* snapshots,

@@ -74,8 +74,9 @@ enum {
 
 /* Flags. */
 enum {
-  /* Use the portable CUDA-core kernel even where the tensor-core kernel
-     applies (dk = dv = 128, bf16 q/k/v).  Same results within rounding. */
+  /* Use the portable kernels (CUDA cores, no bulk tensor copies) even where
+     the tensor-core verification (dk = dv = 128, bf16 q/k/v) or the
+     bulk-copy commit (dk = dv = 128) applies.  Same results within rounding. */
   TREEWY_FLAG_FORCE_GENERIC = 1u,
   /* The state pool holds bf16 instead of f32: the dtype in which the GDN
      state is kept when serving (paper §2 "The memory problem": dv x dk x 2 B
