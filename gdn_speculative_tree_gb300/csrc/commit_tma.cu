@@ -4,13 +4,14 @@
 //
 //   S_a = gamma_a S0 + sum_{i on the root-to-a path} (gamma_a / gamma_i) u_i k_i^T.
 //
-// One CTA of 128 threads per (request, head); thread d owns state row d.
-// The state block (64 KB f32 or 32 KB bf16) is requested by one bulk tensor
-// load as soon as the request's slot is known, lands in shared memory in the
-// 128-byte-swizzled tile layout, is updated there row by row while the path's
-// u and k rows are staged, and leaves by bulk tensor stores.  Nothing of the
-// state passes through registers while in flight, so several CTAs per SM
-// (3 for f32, 5 for bf16) keep enough bytes in flight to stream HBM.
+// One CTA of 128 threads owns a 32 KB tile of one (request, head): half of
+// an f32 state (64 rows, two CTAs per head) or all of a bf16 state (128
+// rows).  The tile is requested by bulk tensor loads as soon as the request's
+// slot is known, lands in shared memory in the 128-byte-swizzled layout, is
+// updated there row by row while the path's u and k rows are staged, and
+// leaves by bulk tensor stores.  Nothing of the state passes through
+// registers while in flight, and six CTAs per SM (192 KB of tiles) keep
+// enough independent load chains in flight to stream HBM.
 #include "treewy_device.cuh"
 #include "treewy_internal.h"
 
@@ -18,19 +19,23 @@ namespace treewy {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kSeg = 16;                            // path nodes staged per pass
-constexpr uint32_t kChunkBytes = 128u * 128u;       // 128 rows x 128 bytes
+constexpr int kSeg = 8;                             // path nodes staged per pass
+constexpr uint32_t kTileBytes = 32768u;
 
+// Tile geometry: f32 state -> 64 rows x 4 chunks of 32 columns (8 KB each),
+// two CTAs per head; bf16 state -> 128 rows x 2 chunks of 64 columns (16 KB).
 template <bool SB>
 struct CommitCfg {
-  static constexpr int kChunks = SB ? 2 : 4;        // 32 KB bf16 / 64 KB f32
+  static constexpr int kRows = SB ? 128 : 64;
+  static constexpr int kChunks = SB ? 2 : 4;
   static constexpr int kChunkCols = SB ? 64 : 32;
-  static constexpr uint32_t kTileBytes = kChunks * kChunkBytes;
-  static constexpr uint32_t kDynSmem = kTileBytes + 1024u;  // + alignment slack
+  static constexpr uint32_t kChunkBytes = kRows * 128u;
+  static constexpr int kSplit = 128 / kRows;        // CTAs per head
+  static constexpr int kBlocksPerThread = 4 * kRows / kThreads;  // 32-column blocks
 };
 
 struct CommitSmem {
-  int parent[kMaxNodes];
+  int8_t parent[kMaxNodes];
   float alpha[kMaxNodes];
   float c[kMaxNodes];                 // gamma_a / gamma_{path j} (alpha products)
   uint8_t path[kMaxNodes];            // a, parent(a), ..., root
@@ -39,9 +44,10 @@ struct CommitSmem {
   float gamma_a;
 };
 
-// Columns 32 blk .. 32 blk + 31 of row d of the swizzled tile, as f32.
+// Columns 32 blk .. 32 blk + 31 of tile row d, as f32.
 template <bool SB>
 __device__ __forceinline__ void load_block(const unsigned char* tile, int d, int blk, float (&x)[32]) {
+  constexpr uint32_t kChunkBytes = CommitCfg<SB>::kChunkBytes;
   if constexpr (SB) {
     const unsigned char* row = tile + (blk >> 1) * kChunkBytes + d * 128;
 #pragma unroll
@@ -70,6 +76,7 @@ __device__ __forceinline__ void load_block(const unsigned char* tile, int d, int
 
 template <bool SB>
 __device__ __forceinline__ void store_block(unsigned char* tile, int d, int blk, const float (&x)[32]) {
+  constexpr uint32_t kChunkBytes = CommitCfg<SB>::kChunkBytes;
   if constexpr (SB) {
     unsigned char* row = tile + (blk >> 1) * kChunkBytes + d * 128;
 #pragma unroll
@@ -97,17 +104,21 @@ __global__ void __launch_bounds__(kThreads)
     commit_tma_kernel(const __grid_constant__ CUtensorMap map_s, const treewy_batch b,
                       const int32_t* __restrict__ accepted) {
   using C = CommitCfg<SB>;
-  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(1024) unsigned char tile[kTileBytes];
   __shared__ CommitSmem cs;
   __shared__ __align__(8) uint64_t bar;
-  unsigned char* tile = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
 
   const int H = b.H;
-  const int r = blockIdx.x / H;
-  const int h = blockIdx.x - r * H;
-  const int t = threadIdx.x;  // = state row d
+  const int head = blockIdx.x / C::kSplit;
+  const int part = blockIdx.x - head * C::kSplit;   // which rows of the head
+  const int r = head / H;
+  const int h = head - r * H;
+  const int t = threadIdx.x;
+  const int dl = t % C::kRows;                       // tile row of this thread
+  const int d = part * C::kRows + dl;                // state row (value index)
+  const int blk0 = (t / C::kRows) * C::kBlocksPerThread;
   const bool kbf16 = b.qkv_dtype == TREEWY_DTYPE_BF16;
+  const bool lead = (h == 0 && part == 0);           // reports request-level flags
 
   if (t == 0) {
     mbar_init(&bar, 1);
@@ -130,18 +141,18 @@ __global__ void __launch_bounds__(kThreads)
     cs.flags = flags;
     cs.a = flags ? -1 : a;
     if (a != -1 && flags == 0) {
-      const int y = (slot * H + h) * 128;
-      mbar_arrive_expect_tx(&bar, C::kTileBytes);
+      const int y = (slot * H + h) * 128 + part * C::kRows;
+      mbar_arrive_expect_tx(&bar, kTileBytes);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_2d(tile + c * kChunkBytes, &map_s, &bar, C::kChunkCols * c, y);
+        tma_load_2d(tile + c * C::kChunkBytes, &map_s, &bar, C::kChunkCols * c, y);
     }
   }
   __syncthreads();
   const int a = cs.a;
   if (a < 0) {
     // nothing accepted (state neither read nor written) or a bad request
-    if (t == 0 && h == 0 && cs.flags) atomicOr(b.status + r, cs.flags);
+    if (t == 0 && lead && cs.flags) atomicOr(b.status + r, cs.flags);
     return;
   }
   const int64_t tok0 = cs.tok0;
@@ -152,7 +163,7 @@ __global__ void __launch_bounds__(kThreads)
   if (t < N) {
     const int p = __ldg(b.parent + tok0 + t);
     bad = !(p >= -1 && p < t);
-    cs.parent[t] = p;
+    cs.parent[t] = static_cast<int8_t>(bad ? -1 : p);
     cs.alpha[t] = __ldg(b.alpha + (tok0 + t) * H + h);
   }
   bad = __syncthreads_or(bad);
@@ -184,7 +195,7 @@ __global__ void __launch_bounds__(kThreads)
       cu[j] = 0.f;
       if (j < ns) {
         const int64_t row = (tok0 + cs.path[s * kSeg + j]) * H + h;
-        cu[j] = cs.c[s * kSeg + j] * __ldg(b.U + row * 128 + t);
+        cu[j] = cs.c[s * kSeg + j] * __ldg(b.U + row * 128 + d);
       }
     }
   };
@@ -196,19 +207,20 @@ __global__ void __launch_bounds__(kThreads)
   if (bad || fail) {
     if (t == 0) {
       if (fail) mbar_wait(&bar, 0);  // nothing may still target this CTA's memory
-      atomicOr(b.status + r, (fail ? kStatusTimeout : 0) | ((bad && h == 0) ? TREEWY_STATUS_BAD_TREE : 0));
+      const int bits = (fail ? kStatusTimeout : 0) | ((bad && lead) ? TREEWY_STATUS_BAD_TREE : 0);
+      if (bits) atomicOr(b.status + r, bits);
     }
     return;
   }
 
-  // row t, 32 columns at a time, f32 across every pass, stored once
+  // tile row dl, 32 columns at a time, f32 across every pass, stored once
   const int len = cs.len;
   const int nseg = (len + kSeg - 1) / kSeg;
   const float ga = cs.gamma_a;
   int staged = 0;
-  for (int blk = 0; blk < 4; ++blk) {
+  for (int blk = blk0; blk < blk0 + C::kBlocksPerThread; ++blk) {
     float x[32];
-    load_block<SB>(tile, t, blk, x);
+    load_block<SB>(tile, dl, blk, x);
 #pragma unroll
     for (int e = 0; e < 32; ++e) x[e] *= ga;
     for (int s = 0; s < nseg; ++s) {
@@ -234,16 +246,17 @@ __global__ void __launch_bounds__(kThreads)
         }
       }
     }
-    store_block<SB>(tile, t, blk, x);
+    store_block<SB>(tile, dl, blk, x);
   }
 
   // S_a back to the pool; the tile must stay until the stores have read it
   fence_proxy_async_smem();
   __syncthreads();
   if (t == 0) {
-    const int y = (cs.slot * H + h) * 128;
+    const int y = (cs.slot * H + h) * 128 + part * C::kRows;
 #pragma unroll
-    for (int c = 0; c < C::kChunks; ++c) tma_store_2d(&map_s, tile + c * kChunkBytes, C::kChunkCols * c, y);
+    for (int c = 0; c < C::kChunks; ++c)
+      tma_store_2d(&map_s, tile + c * C::kChunkBytes, C::kChunkCols * c, y);
     bulk_commit_group();
     bulk_wait_group_read0();
   }
@@ -252,18 +265,14 @@ __global__ void __launch_bounds__(kThreads)
 template <bool SB>
 cudaError_t launch(const treewy_batch& b, const CUtensorMap& map, const int32_t* accepted,
                    cudaStream_t stream) {
-  static cudaError_t attr = [] {
-    cudaError_t e = cudaFuncSetAttribute(commit_tma_kernel<SB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(CommitCfg<SB>::kDynSmem));
-    if (e != cudaSuccess) return e;
-    // the whole unified L1/shared array as shared memory: 3 (f32) or 5 (bf16) CTAs per SM
-    return cudaFuncSetAttribute(commit_tma_kernel<SB>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
-  }();
+  // the whole unified L1/shared array as shared memory: six 38 KB CTAs per SM
+  static cudaError_t attr = cudaFuncSetAttribute(
+      commit_tma_kernel<SB>, cudaFuncAttributePreferredSharedMemoryCarveout,
+      static_cast<int>(cudaSharedmemCarveoutMaxShared));
   if (attr != cudaSuccess) return attr;
-  const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
-  commit_tma_kernel<SB><<<grid, kThreads, CommitCfg<SB>::kDynSmem, stream>>>(map, b, accepted);
+  const unsigned grid =
+      static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H) * CommitCfg<SB>::kSplit;
+  commit_tma_kernel<SB><<<grid, kThreads, 0, stream>>>(map, b, accepted);
   return cudaGetLastError();
 }
 

@@ -95,15 +95,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // State pool of a dk = dv = 128 batch as rows [slots*H*128][128]; one box =
-// 128 state rows x 128 bytes (32 f32 or 64 bf16 columns), 128-byte swizzle.
-treewy_status make_state_map(const treewy_batch* b, CUtensorMap* map) {
+// box_rows state rows x 128 bytes (32 f32 or 64 bf16 columns), 128-byte swizzle.
+treewy_status make_state_map(const treewy_batch* b, CUtensorMap* map, uint32_t box_rows = 128) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return fail(TREEWY_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const cuuint32_t ones[2] = {1, 1};
   const bool sb = (b->flags & TREEWY_FLAG_STATE_BF16) != 0;
   const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(b->num_slots) * b->H * 128};
   const cuuint64_t strides[1] = {128 * (sb ? 2u : 4u)};
-  const cuuint32_t box[2] = {sb ? 64u : 32u, 128};
+  const cuuint32_t box[2] = {sb ? 64u : 32u, box_rows};
   CUresult rc = enc(map, sb ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                     b->state, dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -140,8 +140,9 @@ treewy_status launch_commit_any(const treewy_batch* b, const int32_t* accepted, 
                                 const char* what) {
   cudaError_t err;
   if (b->dk == 128 && b->dv == 128 && (b->flags & TREEWY_FLAG_FORCE_GENERIC) == 0) {
+    // tiles of 64 rows for an f32 pool (two CTAs per head), 128 rows for bf16
     CUtensorMap map;
-    treewy_status st = make_state_map(b, &map);
+    treewy_status st = make_state_map(b, &map, (b->flags & TREEWY_FLAG_STATE_BF16) ? 128u : 64u);
     if (st != TREEWY_OK) return st;
     err = treewy::launch_commit_tma(*b, map, accepted, stream);
   } else {
