@@ -181,21 +181,28 @@ __global__ void __launch_bounds__(kThreads)
   }
   __syncthreads();
 
-  // stage pass `s`: k rows in shared memory, c_j u_j[d] in registers
+  // stage pass `s`: k rows in shared memory, c_j u_j[d] in registers.  Every
+  // load is issued before any result is used (a shared-memory store of a
+  // loaded value would hold back the loads behind it by a round trip).
   float cu[kSeg];
   auto stage = [&](int s) {
     const int ns = min(kSeg, cs.len - s * kSeg);
-    for (int e = t; e < ns * 128; e += kThreads) {
-      const int j = e >> 7, x = e & 127;
-      const int64_t row = (tok0 + cs.path[s * kSeg + j]) * H + h;
-      cs.k[j][x] = load_qkv(b.k, row * 128 + x, kbf16);
-    }
+    float kv[kSeg];                     // element x = t of path node j
 #pragma unroll
     for (int j = 0; j < kSeg; ++j) {
+      kv[j] = 0.f;
       cu[j] = 0.f;
       if (j < ns) {
         const int64_t row = (tok0 + cs.path[s * kSeg + j]) * H + h;
-        cu[j] = cs.c[s * kSeg + j] * __ldg(b.U + row * 128 + d);
+        kv[j] = load_qkv(b.k, row * 128 + t, kbf16);
+        cu[j] = __ldg(b.U + row * 128 + d);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kSeg; ++j) {
+      if (j < ns) {
+        cs.k[j][t] = kv[j];
+        cu[j] *= cs.c[s * kSeg + j];
       }
     }
   };

@@ -244,11 +244,11 @@ struct PrevSmem<true> {
 
 // SB: the state pool holds bf16 (2 chunks of 64 columns) instead of fp32
 // (4 chunks of 32 columns).  Two CTAs share an SM either way (shared memory
-// and TMEM); the bf16 instances state it so the register allocation avoids
-// spills, the fp32 ones (0: no minimum) were measured faster with the
-// default allocation.
+// and TMEM); the bf16 and fused instances state it so the register
+// allocation avoids spills, the plain fp32 ones (0: no minimum) were
+// measured faster with the default allocation.
 template <int NPM, bool FUSED, bool SB>
-__global__ void __launch_bounds__(kThreads, SB ? 2 : 0)
+__global__ void __launch_bounds__(kThreads, (SB || FUSED) ? 2 : 0)
     verify_tc_kernel(const __grid_constant__ CUtensorMap map_s0,
                      const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_q, const treewy_batch b,
@@ -402,21 +402,40 @@ __global__ void __launch_bounds__(kThreads, SB ? 2 : 0)
   for (int j = 0; j < kPrevSeg; ++j) cu[j] = 0.f;
   auto stage_prev = [&](int seg) {
     if constexpr (FUSED) {
+      // every load of the pass is issued before any of its results is used
+      // (a shared-memory store of a loaded value would hold back the loads
+      // behind it by a full memory round trip)
+      constexpr int kPer = kPrevSeg * (kDim / 2) / kThreads;  // k words per thread
       const int ns = min(kPrevSeg, pv.len - seg);
       const uint32_t* kg = reinterpret_cast<const uint32_t*>(prev.k);
-      for (int e = t; e < ns * (kDim / 2); e += kThreads) {
-        const int j = e / (kDim / 2), w = e - j * (kDim / 2);
-        const int64_t row = (static_cast<int64_t>(pv.tok0) + pv.path[seg + j]) * H + h;
-        reinterpret_cast<uint32_t*>(&pv.k[j][0])[w] = __ldg(kg + row * (kDim / 2) + w);
-      }
+      uint32_t kw[kPer];
 #pragma unroll
-      for (int j = 0; j < kPrevSeg; ++j) {
-        cu[j] = 0.f;
+      for (int i = 0; i < kPer; ++i) {
+        const int e = t + i * kThreads;
+        const int j = e / (kDim / 2), w = e - j * (kDim / 2);
+        kw[i] = 0u;
         if (j < ns) {
           const int64_t row = (static_cast<int64_t>(pv.tok0) + pv.path[seg + j]) * H + h;
-          cu[j] = pv.c[seg + j] * __ldg(prev.U + row * kDim + lane);
+          kw[i] = __ldg(kg + row * (kDim / 2) + w);
         }
       }
+      float uv[kPrevSeg];
+#pragma unroll
+      for (int j = 0; j < kPrevSeg; ++j) {
+        uv[j] = 0.f;
+        if (j < ns) {
+          const int64_t row = (static_cast<int64_t>(pv.tok0) + pv.path[seg + j]) * H + h;
+          uv[j] = __ldg(prev.U + row * kDim + lane);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = t + i * kThreads;
+        const int j = e / (kDim / 2), w = e - j * (kDim / 2);
+        if (j < ns) reinterpret_cast<uint32_t*>(&pv.k[j][0])[w] = kw[i];
+      }
+#pragma unroll
+      for (int j = 0; j < kPrevSeg; ++j) cu[j] = (j < ns) ? pv.c[seg + j] * uv[j] : 0.f;
     }
   };
   if constexpr (FUSED) {
