@@ -237,7 +237,7 @@ struct PrevSmem<true> {
   float alpha[kMaxNodes];
   float c[kMaxNodes];                // gamma_a / gamma_{path j} (alpha products)
   uint8_t path[kMaxNodes];           // accepted node, its parent, ... (root last)
-  __nv_bfloat16 k[kPrevSeg][kDim];   // staged k rows of up to kPrevSeg path nodes
+  __align__(16) __nv_bfloat16 k[kPrevSeg][kDim];  // staged k rows of up to kPrevSeg path nodes
   int tok0, N, a, len;
   float gamma_a;
 };
@@ -494,22 +494,24 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED) ? 2 : 0)
     fail = wg ? named_bar_or<2, 128>(fail) : named_bar_or<1, 128>(fail);
   }
   if constexpr (FUSED) {
-    // S_a = gamma_a S0 + sum_j c_j u_j k_j^T on this thread's own fp32 row
-    // segments (chunks 2wg, 2wg+1 of row `lane`), written back to the pool once.
+    // S_a = gamma_a S0 + sum_j c_j u_j k_j^T on this thread's own part of row
+    // `lane` (columns 64wg .. 64wg+63: chunks 2wg, 2wg+1 of an fp32 tile,
+    // chunk wg of a bf16 one), 32 columns at a time held in f32 registers
+    // across every staged path segment and stored back once (rounded once
+    // for a bf16 state); the k rows are read as 16-byte broadcasts.
     if (commit_now && !__syncthreads_or(fail)) {
       const float ga = pv.gamma_a;
-      if constexpr (SB) {
-        // bf16 state: chunk wg of row `lane` (64 columns) in two halves of 32
-        // held in f32 registers across every staged path segment, then
-        // rounded once to bf16 in place (the operand of the first MMA and the
-        // committed value are the same bf16 numbers)
-        const int nseg = (pv.len + kPrevSeg - 1) / kPrevSeg;
-        unsigned char* row = s0 + wg * kS0ChunkBytes + lane * 128;
-        for (int hf = 0; hf < 2; ++hf) {
-          float x[32];
+      const int len = pv.len;
+      const int nseg = (len + kPrevSeg - 1) / kPrevSeg;
+      int staged = 0;
+      for (int hb = 0; hb < 2; ++hb) {
+        const int col0 = 64 * wg + 32 * hb;
+        float x[32];
+        if constexpr (SB) {
+          const unsigned char* row = s0 + wg * kS0ChunkBytes + lane * 128;
 #pragma unroll
           for (int g4 = 0; g4 < 4; ++g4) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(row + (((4 * hf + g4) ^ (lane & 7)) << 4));
+            const uint4 raw = *reinterpret_cast<const uint4*>(row + (((4 * hb + g4) ^ (lane & 7)) << 4));
             const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -517,27 +519,45 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED) ? 2 : 0)
               x[8 * g4 + 2 * i + 1] = ga * __uint_as_float(w[i] & 0xFFFF0000u);
             }
           }
-          for (int sg = 0; sg < nseg; ++sg) {
-            if (nseg > 1 && (hf | sg)) {
-              __syncthreads();
-              stage_prev(sg * kPrevSeg);
-              __syncthreads();
-            }
-            const int ns = min(kPrevSeg, pv.len - sg * kPrevSeg);
-            const int col0 = 64 * wg + 32 * hf;
+        } else {
+          const unsigned char* row = s0 + (2 * wg + hb) * kS0ChunkBytes + lane * 128;
 #pragma unroll
-            for (int j = 0; j < kPrevSeg; ++j) {
-              if (j < ns) {
+          for (int g = 0; g < 8; ++g) {
+            const float4 v = *reinterpret_cast<const float4*>(row + ((g ^ (lane & 7)) << 4));
+            x[4 * g] = ga * v.x;
+            x[4 * g + 1] = ga * v.y;
+            x[4 * g + 2] = ga * v.z;
+            x[4 * g + 3] = ga * v.w;
+          }
+        }
+        for (int sg = 0; sg < nseg; ++sg) {
+          if (sg != staged) {
+            __syncthreads();
+            stage_prev(sg * kPrevSeg);
+            __syncthreads();
+            staged = sg;
+          }
+          const int ns = min(kPrevSeg, len - sg * kPrevSeg);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                  const float2 kk =
-                      __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.k[j][col0 + e]));
-                  x[e] = fmaf(cu[j], kk.x, x[e]);
-                  x[e + 1] = fmaf(cu[j], kk.y, x[e + 1]);
+          for (int j = 0; j < kPrevSeg; ++j) {
+            if (j < ns) {
+              const float u = cu[j];
+              const uint4* kr = reinterpret_cast<const uint4*>(&pv.k[j][col0]);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint4 raw = kr[q];
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  x[8 * q + 2 * i] = fmaf(u, __uint_as_float(w[i] << 16), x[8 * q + 2 * i]);
+                  x[8 * q + 2 * i + 1] = fmaf(u, __uint_as_float(w[i] & 0xFFFF0000u), x[8 * q + 2 * i + 1]);
                 }
               }
             }
           }
+        }
+        if constexpr (SB) {
+          unsigned char* row = s0 + wg * kS0ChunkBytes + lane * 128;
 #pragma unroll
           for (int g4 = 0; g4 < 4; ++g4) {
             uint32_t w[4];
@@ -546,49 +566,22 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED) ? 2 : 0)
               const __nv_bfloat162 p = __floats2bfloat162_rn(x[8 * g4 + 2 * i], x[8 * g4 + 2 * i + 1]);
               w[i] = *reinterpret_cast<const uint32_t*>(&p);
             }
-            *reinterpret_cast<uint4*>(row + (((4 * hf + g4) ^ (lane & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(row + (((4 * hb + g4) ^ (lane & 7)) << 4)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
           }
-        }
-      } else {
-      for (int seg = 0; seg < pv.len; seg += kPrevSeg) {
-        if (seg > 0) {
-          __syncthreads();
-          stage_prev(seg);
-          __syncthreads();
-        }
-        const int ns = min(kPrevSeg, pv.len - seg);
-        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-          unsigned char* row = s0 + c * kS0ChunkBytes + lane * 128;
+        } else {
+          unsigned char* row = s0 + (2 * wg + hb) * kS0ChunkBytes + lane * 128;
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            float4 x = *reinterpret_cast<const float4*>(row + ((g ^ (lane & 7)) << 4));
-            if (seg == 0) {
-              x.x *= ga;
-              x.y *= ga;
-              x.z *= ga;
-              x.w *= ga;
-            }
-            const int col = 32 * c + 4 * g;
-#pragma unroll
-            for (int j = 0; j < kPrevSeg; ++j) {
-              if (j < ns) {
-                const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.k[j][col]));
-                const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.k[j][col + 2]));
-                x.x = fmaf(cu[j], k01.x, x.x);
-                x.y = fmaf(cu[j], k01.y, x.y);
-                x.z = fmaf(cu[j], k23.x, x.z);
-                x.w = fmaf(cu[j], k23.y, x.w);
-              }
-            }
-            *reinterpret_cast<float4*>(row + ((g ^ (lane & 7)) << 4)) = x;
-          }
+          for (int g = 0; g < 8; ++g)
+            *reinterpret_cast<float4*>(row + ((g ^ (lane & 7)) << 4)) =
+                make_float4(x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
         }
       }
-      }
-      // S_a goes back to the pool by bulk tensor stores of this warpgroup's chunks
-      // (the tile layout in shared memory is the one the loads produced);
-      // the chunks are converted in place only after the stores have read them
+      // S_a goes back to the pool by bulk tensor stores of this warpgroup's
+      // chunks (the tile layout in shared memory is the one the loads
+      // produced; per-thread stores straight from the registers, 32 rows per
+      // warp instruction, were measured slower); the chunks are converted in
+      // place only after the stores have read them
       fence_proxy_async_smem();
       if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
       if (lane == 0) {
