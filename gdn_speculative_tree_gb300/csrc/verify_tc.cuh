@@ -244,11 +244,11 @@ struct PrevSmem<true> {
 
 // SB: the state pool holds bf16 (2 chunks of 64 columns) instead of fp32
 // (4 chunks of 32 columns).  Two CTAs share an SM either way (shared memory
-// and TMEM); the bf16 and fused instances state it so the register
-// allocation avoids spills, the plain fp32 ones (0: no minimum) were
-// measured faster with the default allocation.
+// and TMEM); the instances other than the plain fp32 one for 64-node trees
+// state it so the register allocation avoids spills, that one (0: no
+// minimum) was measured faster with the default allocation.
 template <int NPM, bool FUSED, bool SB>
-__global__ void __launch_bounds__(kThreads, (SB || FUSED) ? 2 : 0)
+__global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
     verify_tc_kernel(const __grid_constant__ CUtensorMap map_s0,
                      const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_q, const treewy_batch b,
@@ -332,20 +332,30 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED) ? 2 : 0)
       }
     }
     if (flags == 0 && N > 0) {
-      const int N8 = (N + 7) & ~7;
-      const int Np = (N + 15) & ~15;
       // 2 tensors x 2 column chunks x N8 rows x 128 bytes
-      mbar_arrive_expect_tx(&bars[4], static_cast<uint32_t>(N8) * 512u);
-      for (int c2 = 0; c2 < 2; ++c2) {
-        unsigned char* chunk = kq + c2 * kKQChunkBytes;
-        for (int rb = 0; rb < N8; rb += 8) {
-          tma_load_3d(chunk + rb * 128, &map_k, &bars[4], 64 * c2, h, lo + rb);
-          tma_load_3d(chunk + (Np + rb) * 128, &map_q, &bars[4], 64 * c2, h, lo + rb);
-        }
-      }
+      mbar_arrive_expect_tx(&bars[4], static_cast<uint32_t>((N + 7) & ~7) * 512u);
     }
   }
   if (warp == 0) {
+    // the K and Q boxes (8 rows each) are issued by the lanes of warp 0 in
+    // parallel, after lane 0 has set up the barrier and the expected bytes
+    __syncwarp();
+    const int N = ts.N;
+    if (ts.flags == 0 && N > 0) {
+      const int N8 = (N + 7) & ~7;
+      const int Np = (N + 15) & ~15;
+      const int nbox = 4 * (N8 / 8);  // (tensor, column chunk, 8-row block)
+      for (int i = t; i < nbox; i += 32) {
+        const int c2 = (i >> 1) & 1, rb = 8 * (i >> 2);
+        unsigned char* chunk = kq + c2 * kKQChunkBytes;
+        if (i & 1)
+          tma_load_3d(chunk + (Np + rb) * 128, &map_q, &bars[4], 64 * c2, h, ts.tok0 + rb);
+        else
+          tma_load_3d(chunk + rb * 128, &map_k, &bars[4], 64 * c2, h, ts.tok0 + rb);
+      }
+    }
+  } else if (warp == 1) {
+    // TMEM is allocated by a warp that does not wait on the metadata loads
     tmem_alloc(&tmem_holder, C::kCols);
     tmem_relinquish();
   }
@@ -672,15 +682,14 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED) ? 2 : 0)
       //      Np..Np+N-1.
       float* gdump = reinterpret_cast<float*>(s0 + kThiOff);  // 128 rows x 64 floats
       const int gsw = lane & 31;
-      uint32_t ga[16], gb[16];
-      tmem_ld16_async(tmem + lane_base + 2 * NPM, ga);
 #pragma unroll
       for (int c = 0; c < NPM / 16; ++c) {
         if (c < nch) {
-          uint32_t(&cur)[16] = (c & 1) ? gb : ga;
-          uint32_t(&nxt)[16] = (c & 1) ? ga : gb;
+          // load and wait back to back: the load targets are written
+          // asynchronously, so no other code may run in between
+          uint32_t cur[16];
+          tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * c, cur);
           tmem_wait16(cur);
-          if (c + 1 < nch) tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * (c + 1), nxt);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             gdump[lane * 64 + ((16 * c + j) ^ gsw)] = __uint_as_float(cur[j]);
@@ -713,15 +722,12 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED) ? 2 : 0)
       unsigned char* whi = s0 + kWhiOff + lane * 128;
       unsigned char* wlo = s0 + kWloOff + lane * 128;
       const int sw = lane & 7;
-      uint32_t pa[16], pb[16];
-      tmem_ld16_async(tmem + lane_base, pa);
 #pragma unroll
       for (int c = 0; c < NPM / 16; ++c) {
         if (c < nch) {
-          uint32_t(&cur)[16] = (c & 1) ? pb : pa;
-          uint32_t(&nxt)[16] = (c & 1) ? pa : pb;
+          uint32_t cur[16];
+          tmem_ld16_async(tmem + lane_base + 16 * c, cur);
           tmem_wait16(cur);
-          if (c + 1 < nch) tmem_ld16_async(tmem + lane_base + 16 * (c + 1), nxt);
           float w[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -783,31 +789,47 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED) ? 2 : 0)
     if (!fail) {
       tc_fence_after_sync();
       // ---- U[n] and o_n = gamma_n S0 q_n + O[n], column d = lane; warpgroup
-      //      wg stores nodes 8wg..8wg+7 of every 16-node chunk
+      //      wg stores nodes 16c + 8wg .. 16c + 8wg + 7 of every 16-node chunk,
+      //      reading only those 8 columns of U, O and S0 q, two chunks per
+      //      wait (no code runs between the loads and their wait: the load
+      //      targets are written asynchronously)
       float* og = b.o + (tok0 * H + h) * kDim + lane;
       float* ug = b.U + (tok0 * H + h) * kDim + lane;
       const int64_t stride = static_cast<int64_t>(H) * kDim;
-      for (int c = 0; c < nch; ++c) {
-        uint32_t u[16], oo[16], pq[16];
-        tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * c, u);
-        tmem_ld16_async(tmem + lane_base + 2 * NPM + Np + 16 * c, oo);
-        tmem_ld16_async(tmem + lane_base + Np + 16 * c, pq);
-        tmem_wait16(u);
-        tmem_regs_ready(oo);
-        tmem_regs_ready(pq);
-        auto emit = [&](int j) {
-          const int n = 16 * c + j;
-          if (n < N) {
-            ug[n * stride] = __uint_as_float(u[j]);
-            og[n * stride] = fmaf(ts.gamma[n], __uint_as_float(pq[j]), __uint_as_float(oo[j]));
+      const int half = 8 * wg;
+      constexpr int kPairs = (NPM / 16 + 1) / 2;
+#pragma unroll
+      for (int cp = 0; cp < kPairs; ++cp) {
+        const int c0 = 2 * cp;
+        if (c0 < nch) {
+          uint32_t ua[8], oa[8], qa[8], ub[8], ob[8], qb[8];
+          const bool two = (c0 + 1 < nch) && (c0 + 1 < NPM / 16);
+          tmem_ld8_async(tmem + lane_base + 2 * NPM + 16 * c0 + half, ua);
+          tmem_ld8_async(tmem + lane_base + 2 * NPM + Np + 16 * c0 + half, oa);
+          tmem_ld8_async(tmem + lane_base + Np + 16 * c0 + half, qa);
+          if (two) {
+            tmem_ld8_async(tmem + lane_base + 2 * NPM + 16 * (c0 + 1) + half, ub);
+            tmem_ld8_async(tmem + lane_base + 2 * NPM + Np + 16 * (c0 + 1) + half, ob);
+            tmem_ld8_async(tmem + lane_base + Np + 16 * (c0 + 1) + half, qb);
           }
-        };
-        if (wg == 0) {
+          tmem_wait8(ua, oa, qa);
+          tmem_wait8(ub, ob, qb);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) emit(j);
-        } else {
+          for (int k = 0; k < 2; ++k) {
+            uint32_t(&u)[8] = k ? ub : ua;
+            uint32_t(&oo)[8] = k ? ob : oa;
+            uint32_t(&pq)[8] = k ? qb : qa;
+            if (k == 0 || two) {
 #pragma unroll
-          for (int j = 8; j < 16; ++j) emit(j);
+              for (int j = 0; j < 8; ++j) {
+                const int n = 16 * (c0 + k) + half + j;
+                if (n < N) {
+                  ug[n * stride] = __uint_as_float(u[j]);
+                  og[n * stride] = fmaf(ts.gamma[n], __uint_as_float(pq[j]), __uint_as_float(oo[j]));
+                }
+              }
+            }
+          }
         }
       }
       if (b.gamma != nullptr && t < N) b.gamma[(tok0 + t) * H + h] = ts.gamma[t];
@@ -832,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED) ? 2 : 0)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, C::kCols);
   }
