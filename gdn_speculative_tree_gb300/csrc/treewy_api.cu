@@ -51,6 +51,9 @@ treewy_status validate(const treewy_batch* b, bool need_qv, bool need_outputs, b
     return fail(TREEWY_ERR_INVALID_ARG, "flags = 0x%x has unknown bits", b->flags);
   if (b->T < 0 || b->T > (int64_t(1) << 31) - 1)
     return fail(TREEWY_ERR_INVALID_ARG, "T = %lld outside [0, 2^31)", (long long)b->T);
+  if (int64_t(b->R) * b->H > (int64_t(1) << 31) - 1)
+    return fail(TREEWY_ERR_UNSUPPORTED, "R * H = %lld (request, head) pairs exceed 2^31 - 1",
+                (long long)(int64_t(b->R) * b->H));
   if (b->num_slots < 1) return fail(TREEWY_ERR_INVALID_ARG, "num_slots = %lld must be >= 1",
                                     (long long)b->num_slots);
   if (b->num_slots * b->H * int64_t(b->dv) > (int64_t(1) << 31) - 1)

@@ -162,3 +162,10 @@ def test_make_batch_sets_the_state_flag():
         binding.make_batch(node_offset=w.node_offset, parent=w.parent, q=w.q, k=w.k, v=w.v,
                            alpha=w.alpha, beta=w.beta, state=w.state.half(),
                            state_slot=w.state_slot, o=o, U=o, status=st)
+
+
+def test_too_many_request_head_pairs(lib):
+    b = _valid_batch()
+    b.R, b.H = 1 << 20, 1 << 12
+    assert lib.treewy_verify(ctypes.byref(b), None) == binding.TREEWY_ERR_UNSUPPORTED
+    assert b"R * H" in lib.treewy_last_error()
