@@ -425,6 +425,13 @@ def run_fused(args, work, stream, world, vb, cb, plen, H, peak):
 
 
 def run_e2e(args, work, stream, world):
+    """End to end through the public API: per step, every layer's inputs are
+    copied in from pinned host memory, verified and committed, and its o is
+    copied back.  Separate streams pipeline the layers: host-to-device copies of
+    layer l+1 and device-to-host copies of layer l-1 run while layer l
+    computes (events order each layer's copy-in, compute and copy-out, and a
+    layer's buffers are not overwritten before the previous step is done with
+    them)."""
     from gdn_speculative_tree_gb300 import binding
     hosts = []
     h2d = d2h = 0
@@ -436,16 +443,34 @@ def run_e2e(args, work, stream, world):
         hosts.append((ins, out))
         h2d += sum(x.numel() * x.element_size() for x in ins.values())
         d2h += out.numel() * out.element_size()
+    dev = work[0].o.device
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    L = len(work)
+    ev_in = [torch.cuda.Event() for _ in range(L)]
+    ev_done = [torch.cuda.Event() for _ in range(L)]
+    ev_out = [torch.cuda.Event() for _ in range(L)]
+    first = [True]
 
     def step():
-        for tv, (ins, _) in zip(work, hosts):
+        for l, (tv, (ins, out)) in enumerate(zip(work, hosts)):
             w = tv.wl
-            for name, x in ins.items():
-                getattr(w, name).copy_(x, non_blocking=True)
+            if not first[0]:
+                s_in.wait_event(ev_done[l])      # the previous step's compute of this layer
+            with torch.cuda.stream(s_in):
+                for name, x in ins.items():
+                    getattr(w, name).copy_(x, non_blocking=True)
+                ev_in[l].record(s_in)
+            stream.wait_event(ev_in[l])
+            if not first[0]:
+                stream.wait_event(ev_out[l])     # o of the previous step has left
             binding.treewy_verify(tv.batch, stream)
-        for tv, (_, out) in zip(work, hosts):
             binding.treewy_commit(tv.batch, tv.wl.accepted, stream)
-            out.copy_(tv.o, non_blocking=True)
+            ev_done[l].record(stream)
+            s_out.wait_event(ev_done[l])
+            with torch.cuda.stream(s_out):
+                out.copy_(tv.o, non_blocking=True)
+                ev_out[l].record(s_out)
+        first[0] = False
 
     step()
     torch.cuda.synchronize()
@@ -461,8 +486,8 @@ def run_e2e(args, work, stream, world):
     return {"value": nodes / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": dt * 1e3, "steps": steps,
             "note": "pinned host inputs (q,k,v,alpha,beta,tree,accepted) of all layers copied in and "
-                    "o of all layers copied out each step; the state pool is model state and stays "
-                    "resident on the device"}
+                    "o of all layers copied out each step, pipelined across layers over a compute, "
+                    "a copy-in and a copy-out stream; the state pool is model state and stays resident on the device"}
 
 
 def run_storeall(tv, stream):
