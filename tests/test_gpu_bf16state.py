@@ -190,3 +190,50 @@ def test_bf16_state_fused_equals_separate_calls(cuda_lib):
     assert bool((ds <= ulp + 1e-30).all())   # at most one bf16 step apart
     do = (tna.o - tnb.o).abs().max().item()
     assert do <= 1e-3 * tnb.o.abs().max().item(), do
+
+
+@pytest.mark.parametrize("dk,dv,qkv", [(128, 128, "f32"), (64, 48, "bf16")])
+def test_bf16_state_fused_fallback_shapes(cuda_lib, dk, dv, qkv):
+    """Shapes outside the tensor-core path: treewy_commit_verify runs the
+    commit and the verification back to back; results as the oracle's
+    commit, rounding to bf16, then verification."""
+    rng = np.random.default_rng(dk + dv)
+    prev_trees = random_trees(rng, [7, 20, 3])
+    next_trees = random_trees(rng, [5, 0, 9])
+    accepted = [6, 19, -1]
+    prev = wl.assemble(prev_trees, np.asarray(accepted, np.int32), 2, dk, dv, qkv, 0.05,
+                       (0.9, 0.999), ("sigmoid",), seed=12, max_nodes=64, extra_slots=1,
+                       state_dtype="bf16").to("cuda")
+    nxt = wl.assemble(next_trees, np.full(3, -1, np.int32), 2, dk, dv, qkv, 0.05, (0.9, 0.999),
+                      ("sigmoid",), seed=13, max_nodes=64, extra_slots=1,
+                      state_dtype="bf16").to("cuda")
+    nxt.state = prev.state
+    nxt.state_slot = prev.state_slot
+    tp = binding.TreeVerifier(prev)
+    tp.verify()
+    torch.cuda.synchronize()
+    S0_pool = prev.state.cpu()
+    tn = binding.TreeVerifier(nxt)
+    binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
+    torch.cuda.synchronize()
+    assert not tn.status.any()
+    pn, nn = prev.node_offset.cpu().numpy(), nxt.node_offset.cpu().numpy()
+    o = np32(tn.o)
+    for r in range(3):
+        slot = int(prev.state_slot[r])
+        S0 = np32(S0_pool[slot]).astype(np.float64)
+        lo, hi = int(pn[r]), int(pn[r + 1])
+        ref_prev = orc.verify_request(S0, prev.parent[lo:hi].cpu().numpy(), np32(prev.q[lo:hi]),
+                                      np32(prev.k[lo:hi]), np32(prev.v[lo:hi]),
+                                      np32(prev.alpha[lo:hi]), np32(prev.beta[lo:hi]))
+        S_a = orc.commit_request(S0, ref_prev, accepted[r])
+        S_gpu = np32(prev.state[slot]).astype(np.float64)
+        assert np.all(np.abs(S_gpu - S_a) <= S_REL * np.abs(S_a) + S_ABS * np.abs(S_a).max()), r
+        lo2, hi2 = int(nn[r]), int(nn[r + 1])
+        if hi2 == lo2:
+            continue
+        S_pool = orc.commit_request(S0, ref_prev, accepted[r], state_dtype="bf16")
+        ref = orc.verify_request(S_pool, nxt.parent[lo2:hi2].cpu().numpy(), np32(nxt.q[lo2:hi2]),
+                                 np32(nxt.k[lo2:hi2]), np32(nxt.v[lo2:hi2]),
+                                 np32(nxt.alpha[lo2:hi2]), np32(nxt.beta[lo2:hi2]))
+        assert np.abs(o[lo2:hi2] - ref.o).max() <= O_TOL * np.abs(ref.o).max(), r
