@@ -150,3 +150,20 @@ def test_fused_fallback_shapes(cuda_lib, dk, dv, qkv):
     tp, tn, S0_pool = run_fused(prev, nxt)
     assert not tn.status.any()
     check(prev, nxt, tn, S0_pool, range(3))
+
+
+def test_fused_full_size_sampled(cuda_lib):
+    """The benchmark's layer size and launch configuration (256 requests x 32
+    heads, N 16..64): the previous round is one layer, the next round another
+    layer's draws on the same state pool; sampled requests (all heads) against
+    the oracle's commit-then-verify."""
+    cfg = wl.CONFIGS["wide"]
+    prev = wl.generate(cfg, device="cuda")
+    nxt = wl.generate(cfg, layer=1, device="cuda")
+    nxt.state = prev.state
+    nxt.state_slot = prev.state_slot
+    tp, tn, S0_pool = run_fused(prev, nxt)
+    assert not tn.status.any()
+    rng = np.random.default_rng(2024)
+    reqs = sorted(set(rng.choice(cfg.R, 3, replace=False).tolist()) | {cfg.R - 1})
+    check(prev, nxt, tn, S0_pool, reqs)
