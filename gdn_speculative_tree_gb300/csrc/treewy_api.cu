@@ -223,8 +223,11 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
     err = treewy::launch_commit_verify_tc(*next, pr, maps, next->max_nodes, stream);
     return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_commit_verify launch");
   }
-  // other shapes: the two kernels back to back on the same stream
-  st = launch_commit_any(prev, prev_accepted, stream, "treewy_commit_verify (commit) launch");
+  // other shapes: the two kernels back to back on the same stream, the
+  // commit's status bits going to next->status as on the fused path
+  treewy_batch pc = *prev;
+  pc.status = next->status;
+  st = launch_commit_any(&pc, prev_accepted, stream, "treewy_commit_verify (commit) launch");
   if (st != TREEWY_OK) return st;
   return treewy_verify(next, stream);
 }

@@ -98,7 +98,7 @@ enum {
  * 1 <= dk, dv <= 128 (the tensor-core path needs dk = dv = 128 and bf16
  * q/k/v; every other size runs the CUDA-core path), 1 <= max_nodes <= 64,
  * T >= node_offset[R] rows in every per-node array, num_slots >= 1 blocks in
- * the state pool.
+ * the state pool, R * H < 2^31 (request, head) pairs.
  *
  * Layouts (row-major, innermost index last; all device memory):
  *   node_offset  int32 [R+1], non-decreasing
@@ -184,10 +184,14 @@ treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted,
  * results equal treewy_commit(prev, prev_accepted) followed by
  * treewy_verify(next), with one state read per head instead of two.  A request
  * with no node in `next` still gets its commit.  prev and next must have the
- * same R, H, dk, dv, state pool pointer, num_slots and state_slot pointer.
+ * same R, H, dk, dv, state pool pointer, num_slots, state_slot pointer and
+ * TREEWY_FLAG_STATE_BF16.
  * Errors in the previous round's tree or accepted index set status bits in
- * next->status and skip the request entirely (state and outputs untouched).
- * Shapes outside the tensor-core path run the two kernels back to back.
+ * next->status and leave the request's state untouched; on the tensor-core
+ * path (dk = dv = 128, bf16 q/k/v) the request is then skipped entirely (its
+ * outputs untouched).  Other shapes run the two kernels back to back, and
+ * there a request whose commit was refused is still verified, from its
+ * unchanged state.
  */
 treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev_accepted,
                                    const treewy_batch* next, cudaStream_t stream);

@@ -167,3 +167,25 @@ def test_fused_full_size_sampled(cuda_lib):
     rng = np.random.default_rng(2024)
     reqs = sorted(set(rng.choice(cfg.R, 3, replace=False).tolist()) | {cfg.R - 1})
     check(prev, nxt, tn, S0_pool, reqs)
+
+
+def test_fused_fallback_bad_previous_round(cuda_lib):
+    """Outside the tensor-core path: a refused commit reports in next's status
+    and leaves the state unchanged; that request is still verified from it."""
+    rng = np.random.default_rng(8)
+    prev_trees = [random_tree(rng, 6), random_tree(rng, 9)]
+    next_trees = [random_tree(rng, 5), random_tree(rng, 4)]
+    prev, nxt = rounds(prev_trees, next_trees, [2, 9], H=2, qkv="f32")  # request 1: a >= N
+    tp = binding.TreeVerifier(prev)
+    tp.verify()
+    torch.cuda.synchronize()
+    S_before = prev.state.clone()
+    tn = binding.TreeVerifier(nxt)
+    binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
+    torch.cuda.synchronize()
+    st = tn.status.cpu().tolist()
+    assert st[0] == 0 and st[1] & binding.STATUS_BAD_ACCEPTED
+    assert not tp.status.any()
+    s1 = int(prev.state_slot[1])
+    assert torch.equal(prev.state[s1], S_before[s1])
+    check(prev, nxt, tn, S_before.cpu(), [0])
