@@ -101,12 +101,15 @@ def commit_bytes(plen, H, state_bytes=65536):
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples during the timed region (SM clock and throttle reasons)."""
+    """nvidia-smi samples (SM clock and throttle reasons) every 25 ms; each
+    sample is stamped with the host time it arrived, and the summary keeps
+    only those between mark_start() and mark_end() (the timed region)."""
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -114,17 +117,28 @@ class ClockSampler:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "100",
+                ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "25",
                  "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            # let the sampler start before the timed region begins
+            deadline = time.time() + 2.0
+            while not self.lines and time.time() < deadline:
+                time.sleep(0.02)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+        time.sleep(0.05)  # the sample that covers the last instants
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -135,11 +149,13 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        if not self.lines:
+        if not self.lines or self.t0 is None or self.t1 is None:
             return None
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for stamp, ln in list(self.lines):
+            if not (self.t0 <= stamp <= self.t1 + 0.03):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -154,7 +170,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "sm_mhz_min": min(sm), "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------- distributed
@@ -314,15 +330,17 @@ def run_ours(args, world, rank, local):
     # per-launch events sit on the same stream and are read after the region
     events = [(new_events(), new_events()) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(local) as clk:  # sampling starts before the barrier
+        barrier(world)
+        torch.cuda.synchronize()
+        clk.mark_start()
         start.record(stream)
         for ev_v, ev_c in events:
             step(ev_v, ev_c)
         end.record(stream)
         torch.cuda.synchronize()
-    barrier(world)
+        clk.mark_end()
+        barrier(world)
     total_ms = start.elapsed_time(end)
     v_ms = [a.elapsed_time(b) for ev_v, _ in events for a, b in ev_v]
     c_ms = [a.elapsed_time(b) for _, ev_c in events for a, b in ev_c]
@@ -702,7 +720,7 @@ def study_bf16state(args, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=LAYERS)
