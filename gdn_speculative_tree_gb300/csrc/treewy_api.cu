@@ -64,12 +64,15 @@ treewy_status validate(const treewy_batch* b, bool need_qv, bool need_outputs, b
   if (!b->node_offset || !b->state || !b->state_slot || !b->status)
     return fail(TREEWY_ERR_INVALID_ARG,
                 "node_offset, state, state_slot and status must be non-NULL");
-  if (need_tree && (!b->parent || !b->alpha))
+  // per-node arrays have T rows; with T = 0 (every tree empty) they may be NULL
+  const bool rows = b->T > 0;
+  if (rows && need_tree && (!b->parent || !b->alpha))
     return fail(TREEWY_ERR_INVALID_ARG, "parent and alpha must be non-NULL");
-  if (need_k && !b->k) return fail(TREEWY_ERR_INVALID_ARG, "k is NULL");
-  if (need_qv && (!b->q || !b->v || !b->beta))
+  if (rows && need_k && !b->k) return fail(TREEWY_ERR_INVALID_ARG, "k is NULL");
+  if (rows && need_qv && (!b->q || !b->v || !b->beta))
     return fail(TREEWY_ERR_INVALID_ARG, "q, v and beta must be non-NULL");
-  if (need_outputs && (!b->o || !b->U)) return fail(TREEWY_ERR_INVALID_ARG, "o and U must be non-NULL");
+  if (rows && need_outputs && (!b->o || !b->U))
+    return fail(TREEWY_ERR_INVALID_ARG, "o and U must be non-NULL");
   if (!aligned16(b->state)) return fail(TREEWY_ERR_INVALID_ARG, "state must be 16-byte aligned");
   if (need_k && !aligned16(b->k)) return fail(TREEWY_ERR_INVALID_ARG, "k must be 16-byte aligned");
   if (need_qv && (!aligned16(b->q) || !aligned16(b->v)))
@@ -167,8 +170,9 @@ treewy_status treewy_verify(const treewy_batch* batch, cudaStream_t stream) {
   treewy_status st = validate(batch, true, true, true);
   if (st != TREEWY_OK || batch->R == 0) return st;
   cudaError_t err;
-  if (use_tensor_cores(batch)) {
-    if (batch->T == 0) return TREEWY_OK;
+  // (a batch of empty trees, T = 0, goes to the CUDA-core kernel: there are
+  // no rows to map, and it still checks node_offset and the slots)
+  if (use_tensor_cores(batch) && batch->T > 0) {
     treewy::VerifyMaps maps;
     st = make_maps(batch, &maps);
     if (st != TREEWY_OK) return st;
@@ -183,7 +187,7 @@ treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted, 
   g_last_error.clear();
   treewy_status st = validate(batch, false, false, true);
   if (st != TREEWY_OK || batch->R == 0) return st;
-  if (!batch->U) return fail(TREEWY_ERR_INVALID_ARG, "U is NULL");
+  if (!batch->U && batch->T > 0) return fail(TREEWY_ERR_INVALID_ARG, "U is NULL");
   if (!accepted) return fail(TREEWY_ERR_INVALID_ARG, "accepted is NULL");
   return launch_commit_any(batch, accepted, stream, "treewy_commit launch");
 }
@@ -203,7 +207,7 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
   if ((prev->flags ^ next->flags) & TREEWY_FLAG_STATE_BF16)
     return fail(TREEWY_ERR_INVALID_ARG, "prev and next must agree on TREEWY_FLAG_STATE_BF16");
   if (next->R == 0) return TREEWY_OK;
-  if (!prev->U) return fail(TREEWY_ERR_INVALID_ARG, "prev->U is NULL");
+  if (!prev->U && prev->T > 0) return fail(TREEWY_ERR_INVALID_ARG, "prev->U is NULL");
   if (!prev_accepted) return fail(TREEWY_ERR_INVALID_ARG, "prev_accepted is NULL");
   cudaError_t err;
   if (use_tensor_cores(next) && next->T > 0 && prev->qkv_dtype == TREEWY_DTYPE_BF16) {
@@ -239,8 +243,8 @@ treewy_status treewy_storeall_verify(const treewy_batch* batch, float* snapshots
   if (batch->flags & TREEWY_FLAG_STATE_BF16)
     return fail(TREEWY_ERR_UNSUPPORTED, "the storeall comparator keeps f32 states only");
   if (batch->R == 0) return st;
-  if (!batch->o) return fail(TREEWY_ERR_INVALID_ARG, "o is NULL");
-  if (!snapshots || !aligned16(snapshots))
+  if (batch->T > 0 && !batch->o) return fail(TREEWY_ERR_INVALID_ARG, "o is NULL");
+  if ((batch->T > 0 && !snapshots) || !aligned16(snapshots))
     return fail(TREEWY_ERR_INVALID_ARG, "snapshots must be non-NULL and 16-byte aligned");
   cudaError_t err = treewy::launch_storeall_verify(*batch, snapshots, stream);
   return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_storeall_verify launch");
@@ -252,10 +256,10 @@ treewy_status treewy_storeall_commit(const treewy_batch* batch, const float* sna
   treewy_status st = validate(batch, false, false, false, false);
   if (st == TREEWY_OK && (batch->flags & TREEWY_FLAG_STATE_BF16))
     return fail(TREEWY_ERR_UNSUPPORTED, "the storeall comparator keeps f32 states only");
-  if (st == TREEWY_OK && batch->R > 0 && !batch->parent)
+  if (st == TREEWY_OK && batch->R > 0 && batch->T > 0 && !batch->parent)
     return fail(TREEWY_ERR_INVALID_ARG, "parent is NULL");
   if (st != TREEWY_OK || batch->R == 0) return st;
-  if (!snapshots || !aligned16(snapshots))
+  if ((batch->T > 0 && !snapshots) || !aligned16(snapshots))
     return fail(TREEWY_ERR_INVALID_ARG, "snapshots must be non-NULL and 16-byte aligned");
   if (!accepted) return fail(TREEWY_ERR_INVALID_ARG, "accepted is NULL");
   cudaError_t err = treewy::launch_storeall_commit(*batch, snapshots, accepted, stream);

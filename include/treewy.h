@@ -116,6 +116,8 @@ enum {
  *                                 the per-node snapshots)
  *   gamma        f32 [T][H]       optional verify output gamma_n (may be NULL)
  *   status       int32 [R]        per-request error bits, OR-ed (see above)
+ * The per-node arrays (parent, q, k, v, alpha, beta, o, U, gamma) may be
+ * NULL when T = 0, a batch whose trees are all empty.
  */
 typedef struct treewy_batch {
   int32_t R;

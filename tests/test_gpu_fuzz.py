@@ -1,0 +1,133 @@
+"""Randomised GPU parity: every seed draws a batch shape (requests, heads,
+head sizes, q/k/v and state dtypes, tree capacity, tree shapes including
+chains, stars, deep paths and empty trees, accepted nodes) and runs verify +
+commit and the two-round fused path through the C ABI against the oracle.
+
+Tolerances as in tests/gpu_helpers.py (o, U: 2e-3 of the largest reference
+value; state: 1e-3 of the largest reference value) plus, for a bf16 pool,
+the per-element rounding bound 2^-8 |S| of the stored state.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gdn_speculative_tree_gb300 import binding
+from gdn_speculative_tree_gb300 import workloads as wl
+from oracle import gdn_tree_oracle as orc
+from tests.gpu_helpers import np32
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(128, 128, "bf16"), (128, 128, "f32"), (64, 64, "bf16"), (32, 96, "bf16"), (5, 7, "f32")]
+
+
+def draw_tree(rng, cap):
+    kind = rng.integers(0, 6)
+    n = int(rng.integers(0, cap + 1))
+    if kind == 0 or n == 0:
+        return np.zeros(0, np.int32)                         # an empty tree
+    if kind == 1:
+        return wl.chain_parents(n)
+    if kind == 2:
+        return np.full(n, -1, np.int32)                     # all nodes on S0
+    if kind == 3:
+        return np.array([-1] + [0] * (n - 1), np.int32)     # a star under node 0
+    return np.array([-1] + [int(rng.integers(-1, i)) for i in range(1, n)], np.int32)
+
+
+def draw_batch(seed):
+    rng = np.random.default_rng(1000 + seed)
+    dk, dv, qkv = SHAPES[int(rng.integers(0, len(SHAPES)))]
+    sd = "bf16" if rng.integers(0, 2) else "f32"
+    cap = int(rng.choice([16, 32, 64]))
+    R = int(rng.integers(1, 9))
+    H = int(rng.integers(1, 4))
+    trees = [draw_tree(rng, cap) for _ in range(R)]
+    acc = [int(rng.integers(-1, len(t))) if len(t) else -1 for t in trees]
+    return rng, dict(H=H, dk=dk, dv=dv, qkv=qkv, sd=sd, cap=cap, trees=trees, acc=acc)
+
+
+def assemble(p, trees, acc, seed):
+    return wl.assemble(trees, np.asarray(acc, np.int32), p["H"], p["dk"], p["dv"], p["qkv"], 0.05,
+                       (0.85, 0.999), ("uniform", 0.05, 0.95), seed=seed, max_nodes=p["cap"],
+                       extra_slots=1, state_dtype=p["sd"]).to("cuda")
+
+
+def f64(x):
+    return np32(x).astype(np.float64)
+
+
+def check_state(S_gpu, S_ref, sd):
+    bound = 1e-3 * np.abs(S_ref).max() + (2.0 ** -8 * np.abs(S_ref) if sd == "bf16" else 0.0)
+    assert np.all(np.abs(S_gpu - S_ref) <= bound + 1e-30)
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_fuzz_verify_commit(cuda_lib, seed):
+    _, p = draw_batch(seed)
+    w = assemble(p, p["trees"], p["acc"], seed)
+    S0_pool = w.state.cpu()
+    tv = binding.TreeVerifier(w)
+    tv.verify()
+    tv.commit()
+    torch.cuda.synchronize()
+    assert not tv.status.any(), (p, tv.status.tolist())
+    o, U = np32(tv.o), np32(tv.U)
+    node = w.node_offset.cpu().numpy()
+    o_err = o_max = u_err = u_max = 0.0
+    for r in range(w.R):
+        lo, hi = int(node[r]), int(node[r + 1])
+        slot = int(w.state_slot[r])
+        S0 = f64(S0_pool[slot])
+        ref = orc.verify_request(S0, w.parent[lo:hi].cpu().numpy(), f64(w.q[lo:hi]), f64(w.k[lo:hi]),
+                                 f64(w.v[lo:hi]), f64(w.alpha[lo:hi]), f64(w.beta[lo:hi]))
+        if hi > lo:
+            o_err = max(o_err, float(np.abs(o[lo:hi] - ref.o).max()))
+            o_max = max(o_max, float(np.abs(ref.o).max()))
+            u_err = max(u_err, float(np.abs(U[lo:hi] - ref.U).max()))
+            u_max = max(u_max, float(np.abs(ref.U).max()))
+        S_ref = orc.commit_request(S0, ref, p["acc"][r])
+        check_state(f64(w.state[slot]), S_ref, p["sd"])
+    assert o_err <= 2e-3 * max(o_max, 1e-30), (p["dk"], p["dv"], p["qkv"], p["sd"], o_err, o_max)
+    assert u_err <= 2e-3 * max(u_max, 1e-30), (u_err, u_max)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_fuzz_fused_two_rounds(cuda_lib, seed):
+    rng, p = draw_batch(100 + seed)
+    R = len(p["trees"])
+    nxt_trees = [draw_tree(rng, p["cap"]) for _ in range(R)]
+    prev = assemble(p, p["trees"], p["acc"], 2 * seed)
+    nxt = assemble(p, nxt_trees, [-1] * R, 2 * seed + 1)
+    nxt.state = prev.state
+    nxt.state_slot = prev.state_slot
+    tp = binding.TreeVerifier(prev)
+    tp.verify()
+    torch.cuda.synchronize()
+    S0_pool = prev.state.cpu()
+    tn = binding.TreeVerifier(nxt)
+    binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
+    torch.cuda.synchronize()
+    assert not tn.status.any() and not tp.status.any()
+    o = np32(tn.o)
+    pn, nn = prev.node_offset.cpu().numpy(), nxt.node_offset.cpu().numpy()
+    o_err = o_max = 0.0
+    for r in range(R):
+        slot = int(prev.state_slot[r])
+        S0 = f64(S0_pool[slot])
+        lo, hi = int(pn[r]), int(pn[r + 1])
+        ref_p = orc.verify_request(S0, prev.parent[lo:hi].cpu().numpy(), f64(prev.q[lo:hi]),
+                                   f64(prev.k[lo:hi]), f64(prev.v[lo:hi]), f64(prev.alpha[lo:hi]),
+                                   f64(prev.beta[lo:hi]))
+        S_a = orc.commit_request(S0, ref_p, p["acc"][r])
+        check_state(f64(prev.state[slot]), S_a, p["sd"])
+        S_pool = orc.commit_request(S0, ref_p, p["acc"][r], state_dtype=p["sd"])
+        lo, hi = int(nn[r]), int(nn[r + 1])
+        if hi == lo:
+            continue
+        ref = orc.verify_request(S_pool, nxt.parent[lo:hi].cpu().numpy(), f64(nxt.q[lo:hi]),
+                                 f64(nxt.k[lo:hi]), f64(nxt.v[lo:hi]), f64(nxt.alpha[lo:hi]),
+                                 f64(nxt.beta[lo:hi]))
+        o_err = max(o_err, float(np.abs(o[lo:hi] - ref.o).max()))
+        o_max = max(o_max, float(np.abs(ref.o).max()))
+    assert o_err <= 2e-3 * max(o_max, 1e-30), (p["dk"], p["dv"], p["qkv"], p["sd"], o_err, o_max)

@@ -267,3 +267,27 @@ def test_graph_replay_matches_eager(cuda_lib):
     torch.cuda.synchronize()
     assert torch.equal(tv.o.cpu(), torch.from_numpy(run.o))
     assert torch.equal(w.state.cpu(), run.S_after.cpu())
+
+
+def test_batch_of_empty_trees(cuda_lib):
+    """T = 0: every per-node tensor is empty (NULL data pointers); verify,
+    commit, the fused path and storeall accept it, a = -1 leaves the states
+    alone, and an accepted index in an empty tree is reported."""
+    w = custom([np.zeros(0, np.int32)] * 3, [-1, -1, -1], H=2, extra_slots=1)
+    assert w.T == 0
+    S0 = w.state.clone()
+    tv = binding.TreeVerifier(w)
+    tv.verify()
+    tv.commit()
+    binding.treewy_commit_verify(tv.batch, w.accepted, tv.batch)
+    snaps = torch.empty(0, w.H, w.dv, w.dk, device="cuda")
+    binding.treewy_storeall_verify(tv.batch, snaps)
+    binding.treewy_storeall_commit(tv.batch, snaps, w.accepted)
+    torch.cuda.synchronize()
+    assert not tv.status.any()
+    assert torch.equal(w.state, S0)
+    bad = torch.tensor([0, -1, -1], dtype=torch.int32, device="cuda")
+    tv.commit(bad)
+    torch.cuda.synchronize()
+    assert tv.status.cpu().tolist() == [binding.STATUS_BAD_ACCEPTED, 0, 0]
+    assert torch.equal(w.state, S0)
