@@ -131,3 +131,70 @@ def test_fuzz_fused_two_rounds(cuda_lib, seed):
         o_err = max(o_err, float(np.abs(o[lo:hi] - ref.o).max()))
         o_max = max(o_max, float(np.abs(ref.o).max()))
     assert o_err <= 2e-3 * max(o_max, 1e-30), (p["dk"], p["dv"], p["qkv"], p["sd"], o_err, o_max)
+
+
+# ------------------------------------------------------------ error reporting
+
+BT, TMN, BA, BS = (binding.STATUS_BAD_TREE, binding.STATUS_TOO_MANY_NODES,
+                   binding.STATUS_BAD_ACCEPTED, binding.STATUS_BAD_SLOT)
+
+
+@pytest.mark.parametrize("flags", [0, binding.FLAG_FORCE_GENERIC])
+@pytest.mark.parametrize("seed", range(12))
+def test_fuzz_error_reporting(cuda_lib, seed, flags):
+    """Requests carrying one planted error each (a parent index out of range,
+    a tree above the batch's capacity, a pool slot out of range, an accepted
+    index outside the tree) get exactly their status bits and keep their
+    outputs and state; every other request matches the oracle."""
+    rng = np.random.default_rng(5000 + seed)
+    cap = int(rng.choice([16, 32]))
+    R = int(rng.integers(4, 10))
+    kinds = [int(rng.integers(0, 5)) for _ in range(R)]   # 0 clean, 1 parent, 2 size, 3 slot, 4 accepted
+    trees, acc = [], []
+    for kind in kinds:
+        n = int(rng.integers(cap + 1, 65)) if kind == 2 else int(rng.integers(2, cap + 1))
+        t = np.array([-1] + [int(rng.integers(-1, i)) for i in range(1, n)], np.int32)
+        if kind == 1:
+            j = int(rng.integers(1, n))
+            t[j] = j                                   # a node is its own parent
+        trees.append(t)
+        acc.append(n if kind == 4 else int(rng.integers(0, n)))
+    sd = "bf16" if rng.integers(0, 2) else "f32"
+    w = wl.assemble(trees, np.asarray(acc, np.int32), 2, 128, 128, "bf16", 0.05, (0.85, 0.999),
+                    ("uniform", 0.05, 0.95), seed=seed, max_nodes=cap, extra_slots=1,
+                    state_dtype=sd).to("cuda")
+    slots = w.state_slot.clone()
+    for r, kind in enumerate(kinds):
+        if kind == 3:
+            slots[r] = w.num_slots                     # outside the pool
+    w.state_slot.copy_(slots)
+    S_before = w.state.clone()
+    tv = binding.TreeVerifier(w, flags=flags)
+    tv.o.fill_(float("nan"))
+    tv.U.fill_(float("nan"))
+    tv.verify()
+    tv.commit()
+    torch.cuda.synchronize()
+    expect = {0: 0, 1: BT, 2: TMN, 3: BS, 4: BA}
+    assert tv.status.cpu().tolist() == [expect[k] for k in kinds], (kinds, tv.status.tolist())
+    node = w.node_offset.cpu().numpy()
+    o, U = np32(tv.o), np32(tv.U)
+    S0_pool = S_before.cpu()
+    for r, kind in enumerate(kinds):
+        lo, hi = int(node[r]), int(node[r + 1])
+        if kind in (1, 2, 3):
+            assert np.isnan(o[lo:hi]).all() and np.isnan(U[lo:hi]).all(), (r, kind)
+            continue
+        slot = int(w.state_slot[r])
+        S0 = f64(S0_pool[slot])
+        ref = orc.verify_request(S0, w.parent[lo:hi].cpu().numpy(), f64(w.q[lo:hi]), f64(w.k[lo:hi]),
+                                 f64(w.v[lo:hi]), f64(w.alpha[lo:hi]), f64(w.beta[lo:hi]))
+        assert np.abs(o[lo:hi] - ref.o).max() <= 2e-3 * np.abs(ref.o).max(), (r, kind)
+        if kind == 4:
+            assert torch.equal(w.state[slot], S_before[slot])  # refused commit
+        else:
+            check_state(f64(w.state[slot]), orc.commit_request(S0, ref, acc[r]), sd)
+    for r, kind in enumerate(kinds):                          # states of refused requests
+        if kind in (1, 2):
+            s = int(w.state_slot[r])
+            assert torch.equal(w.state[s], S_before[s]), (r, kind)
