@@ -609,6 +609,38 @@ def study_widths(args, local):
                       "rows": rows}), flush=True)
 
 
+def study_fixed64(args, local):
+    """The wide workload with every tree at the capacity, N = 64 (random
+    trees of depth <= 8): verify, commit and the fused commit-into-verify
+    per layer, median of 20 launches each (a layer's inputs exceed L2)."""
+    from gdn_speculative_tree_gb300 import binding
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = read_peaks()
+    cfg = wl.CONFIGS[CONFIG_NAME].with_(tree="random64_d8")
+    w = wl.generate(cfg, device=torch.device("cuda", local))
+    tv = binding.TreeVerifier(w)
+    S0 = w.state.clone()
+    Ns, plen = tree_stats(w.trees, w.accepted.cpu().numpy())
+    vb, cb = verify_bytes(Ns, w.H), commit_bytes(plen, w.H)
+    fb = vb + cb - int(w.H * 65536 * int((plen > 0).sum()))
+    for _ in range(args.warmup):
+        tv.verify(stream)
+    v_ms = _median_ms(lambda: tv.verify(stream), stream, 20)
+    c_ms = _median_ms(lambda: tv.commit(None, stream), stream, 20, before=lambda: w.state.copy_(S0))
+    f_ms = _median_ms(lambda: binding.treewy_commit_verify(tv.batch, w.accepted, tv.batch, stream),
+                      stream, 20, before=lambda: w.state.copy_(S0))
+    if tv.status.any().item():
+        raise SystemExit("device status bits set in the N = 64 study")
+    g = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
+    print(json.dumps({
+        "study": "wide workload with N fixed at 64", "R": cfg.R, "H": cfg.H,
+        "nodes_per_layer": int(Ns.sum()), "peak_gbs": peak, "peak_kind": f"{peak_kind} hbm_gbs",
+        "verify": {"ms": v_ms, "algorithmic_bytes": vb, "gbs": g(vb, v_ms), "frac": g(vb, v_ms) / peak},
+        "commit": {"ms": c_ms, "algorithmic_bytes": cb, "gbs": g(cb, c_ms), "frac": g(cb, c_ms) / peak},
+        "fused": {"ms": f_ms, "algorithmic_bytes": fb, "gbs": g(fb, f_ms), "frac": g(fb, f_ms) / peak}}),
+        flush=True)
+
+
 def study_graph(args, local):
     """Launch overhead on the chain workload (64 requests x 32 heads, chains of
     4): 30 layers of verify + commit issued eagerly vs replayed as one CUDA
@@ -726,7 +758,7 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--cpu-requests", type=int, default=64)
     ap.add_argument("--no-storeall", action="store_true")
-    ap.add_argument("--study", choices=["widths", "graph", "bf16state"],
+    ap.add_argument("--study", choices=["widths", "graph", "bf16state", "fixed64"],
                     help="print one study line instead of the benchmark line (1 GPU)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -740,8 +772,8 @@ def main():
                 torch.cuda.set_device(local)
                 _build.build()
                 binding.load()
-                {"widths": study_widths, "graph": study_graph,
-                 "bf16state": study_bf16state}[args.study](args, local)
+                {"widths": study_widths, "graph": study_graph, "bf16state": study_bf16state,
+                 "fixed64": study_fixed64}[args.study](args, local)
         elif args.impl == "reference":
             run_reference(args, world, rank)
         else:

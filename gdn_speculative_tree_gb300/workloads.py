@@ -133,7 +133,7 @@ class WorkloadConfig:
     dk: int
     dv: int
     qkv_dtype: str          # "bf16" or "f32"
-    tree: str               # "chain4", "binary15", "random16_64_d8", "branches8x8", "widths"
+    tree: str               # "chain4", "binary15", "random16_64_d8", "random64_d8", "branches8x8", "widths"
     s0_std: float
     alpha_range: Tuple[float, float]
     beta: Tuple             # ("sigmoid",) or ("uniform", lo, hi)
@@ -179,6 +179,8 @@ def make_trees(cfg: WorkloadConfig, R: Optional[int] = None) -> Tuple[List[np.nd
         elif cfg.tree == "random16_64_d8":
             n = int(rng.integers(16, 65))
             trees.append(random_recursive_parents(rng, n, 8))
+        elif cfg.tree == "random64_d8":
+            trees.append(random_recursive_parents(rng, 64, 8))
         elif cfg.tree == "branches8x8":
             trees.append(branches_parents(8, 8))
         elif cfg.tree == "widths":
