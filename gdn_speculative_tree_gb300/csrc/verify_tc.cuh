@@ -75,24 +75,20 @@ struct TreeTC {
   int tok0, N, slot, flags;
 };
 
-// Load parents and gates, validate the tree, and build every node's path list
-// p_0 = n, p_1, ... with the decay products c_k = gamma_n / gamma_{p_k} formed
-// as products of alpha along the path (no division).  All threads must call
-// it; returns false uniformly when a parent index is out of range.
-__device__ __forceinline__ bool prepare_tree(TreeTC& ts, uint8_t* pidx, float* pc,
-                                             const treewy_batch& b, int h) {
+// Validate the tree from this thread's node (parent p, gates alpha, beta, as
+// loaded by the caller) and build every node's path list p_0 = n, p_1, ...
+// with the decay products c_k = gamma_n / gamma_{p_k} formed as products of
+// alpha along the path (no division).  All threads must call it; returns
+// false uniformly when a parent index is out of range.
+__device__ __forceinline__ bool prepare_tree(TreeTC& ts, uint8_t* pidx, float* pc, int p,
+                                             float alpha, float beta) {
   const int t = threadIdx.x;
   const int N = ts.N;
-  const int H = b.H;
   bool bad = false;
-  float beta = 0.f;
   if (t < N) {
-    const int64_t row = static_cast<int64_t>(ts.tok0) + t;
-    const int p = __ldg(b.parent + row);
     bad = !(p >= -1 && p < t);
     ts.parent[t] = bad ? -1 : p;
-    ts.alpha[t] = __ldg(b.alpha + row * H + h);
-    beta = __ldg(b.beta + row * H + h);
+    ts.alpha[t] = alpha;
   }
   if (__syncthreads_or(bad)) return false;
   if (t < N) {
@@ -288,13 +284,47 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   bool mma_issued = false;
   bool mma2_issued = false;
 
+  // Every thread reads the request's node range itself, so that its node of
+  // the tree and (warpgroup 1) its V columns are requested straight after
+  // the first memory round trip rather than after thread 0 has published
+  // the metadata.  Nothing loaded here is used unless the request's checks
+  // below pass; the range test only keeps the loads inside the batch.
+  const int lo_s = __ldg(b.node_offset + r), hi_s = __ldg(b.node_offset + r + 1);
+  const int n_s = hi_s - lo_s;
+  const bool range_ok = n_s > 0 && n_s <= b.max_nodes && lo_s >= 0 && static_cast<int64_t>(hi_s) <= b.T;
+  int tree_p = -1;
+  float tree_alpha = 0.f, tree_beta = 0.f;
+  if (range_ok && t < n_s) {
+    const int64_t row = static_cast<int64_t>(lo_s) + t;
+    tree_p = __ldg(b.parent + row);
+    tree_alpha = __ldg(b.alpha + row * H + h);
+    tree_beta = __ldg(b.beta + row * H + h);
+  }
+  // Column `lane` of V for the warpgroup that builds W.  Each thread loads the
+  // bf16 pair of columns (lane & ~1, lane | 1) of every other node (half the
+  // load requests of one 2-byte load per node), and neighbouring lanes swap
+  // halves after the tree is prepared.
+  uint32_t vpk[NPM / 2];
+#pragma unroll
+  for (int i = 0; i < NPM / 2; ++i) vpk[i] = 0u;
+  if (range_ok && wg == 1) {
+    const uint32_t* vg = reinterpret_cast<const uint32_t*>(b.v);
+    const int par = lane & 1;
+#pragma unroll
+    for (int i = 0; i < NPM / 2; ++i) {
+      const int n = 2 * i + par;
+      if (n < n_s && n < NPM)
+        vpk[i] = __ldg(vg + (((static_cast<int64_t>(lo_s) + n) * H + h) * kDim + (lane & ~1)) / 2);
+    }
+  }
+
   if (t == 0) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
     fence_mbarrier_init();
     s_fail = 0;
-    // every metadata load of this CTA is independent: one memory round trip
-    const int lo = b.node_offset[r], hi = b.node_offset[r + 1];
+    // every further metadata load of this CTA is independent: one round trip
+    const int lo = lo_s, hi = hi_s;
     const int slot = b.state_slot[r];
     int pa = -1, plo = 0, phi = 0;
     if constexpr (FUSED) {
@@ -372,23 +402,6 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   const bool have_s0 = issued || commit_a >= 0;
   const int64_t tok0 = ts.tok0;
 
-  // Column `lane` of V for the warpgroup that builds W.  Each thread loads the
-  // bf16 pair of columns (lane & ~1, lane | 1) of every other node (half the
-  // load requests of one 2-byte load per node), and neighbouring lanes swap
-  // halves after the tree is prepared.
-  uint32_t vpk[NPM / 2];
-#pragma unroll
-  for (int i = 0; i < NPM / 2; ++i) vpk[i] = 0u;
-  if (issued && wg == 1) {
-    const uint32_t* vg = reinterpret_cast<const uint32_t*>(b.v);
-    const int par = lane & 1;
-#pragma unroll
-    for (int i = 0; i < NPM / 2; ++i) {
-      const int n = 2 * i + par;
-      if (n < N) vpk[i] = __ldg(vg + (((tok0 + n) * H + h) * kDim + (lane & ~1)) / 2);
-    }
-  }
-
   // the previous tree's parents and gates, requested before this tree's so
   // that both round trips overlap
   int prev_p = -1;
@@ -402,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   }
 
   bool bad_tree = false;
-  if (issued) bad_tree = !prepare_tree(ts, pidx, pc, b, h);
+  if (issued) bad_tree = !prepare_tree(ts, pidx, pc, tree_p, tree_alpha, tree_beta);
 
   // Fused commit: validate the previous tree, walk the accepted node's path and
   // stage its first segment (k rows in shared memory, c_j u_j[lane] in registers).
