@@ -75,11 +75,15 @@ struct TreeTC {
   int tok0, N, slot, flags;
 };
 
-// Validate the tree from this thread's node (parent p, gates alpha, beta, as
-// loaded by the caller) and build every node's path list p_0 = n, p_1, ...
-// with the decay products c_k = gamma_n / gamma_{p_k} formed as products of
-// alpha along the path (no division).  All threads must call it; returns
-// false uniformly when a parent index is out of range.
+// Tree preparation by the 64 threads of warps 0 and 1 (thread n = node n;
+// a batch holds at most 64 nodes per tree), synchronised on hardware barrier
+// 3 so that the rest of the CTA is free meanwhile.  Validates the parents
+// (p, alpha, beta: this thread's node as loaded by the caller), then walks
+// each node's path once: gamma_n, the path length D_n, and the path list
+// p_0 = n, p_1, ... with the decay products c_k = gamma_n / gamma_{p_k}
+// formed as products of alpha along the path (no division); the first
+// kRegPath entries wait in registers for the CSR offsets.  Returns false
+// (uniformly over the 64 threads) when a parent index is out of range.
 __device__ __forceinline__ bool prepare_tree(TreeTC& ts, uint8_t* pidx, float* pc, int p,
                                              float alpha, float beta) {
   const int t = threadIdx.x;
@@ -90,19 +94,35 @@ __device__ __forceinline__ bool prepare_tree(TreeTC& ts, uint8_t* pidx, float* p
     ts.parent[t] = bad ? -1 : p;
     ts.alpha[t] = alpha;
   }
-  if (__syncthreads_or(bad)) return false;
+  if (named_bar_or<3, 64>(bad)) return false;
+  int anc[kRegPath];
+  float cc[kRegPath];
+  int D = 0;
   if (t < N) {
-    float g = ts.alpha[t];
-    int D = 1;
-    for (int p = ts.parent[t]; p >= 0; p = ts.parent[p]) {
-      g *= ts.alpha[p];
+    float c = 1.0f;
+    int cur = t;
+#pragma unroll
+    for (int k = 0; k < kRegPath; ++k) {
+      anc[k] = 0;
+      cc[k] = 0.f;
+      if (cur >= 0) {
+        anc[k] = cur;
+        cc[k] = c;
+        const float a = k == 0 ? alpha : ts.alpha[cur];
+        cur = k == 0 ? p : ts.parent[cur];
+        c *= a;
+        ++D;
+      }
+    }
+    for (; cur >= 0; cur = ts.parent[cur]) {
+      c *= ts.alpha[cur];
       ++D;
     }
-    ts.gamma[t] = g;
-    ts.bbg[t] = make_float2(beta, beta * g);
+    ts.gamma[t] = c;
+    ts.bbg[t] = make_float2(beta, beta * c);
     ts.D[t] = D;
   }
-  __syncthreads();
+  named_bar_sync<3, 64>();
   if (t < 32) {
     const int i0 = 2 * t, i1 = 2 * t + 1;
     const int a0 = i0 < N ? ts.D[i0] : 0;
@@ -118,15 +138,25 @@ __device__ __forceinline__ bool prepare_tree(TreeTC& ts, uint8_t* pidx, float* p
     ts.off[i1] = excl + a0;
     if (t == 31) ts.off[kMaxNodes] = s;
   }
-  __syncthreads();
+  named_bar_sync<3, 64>();
   if (t < N) {
     const int o = ts.off[t];
-    float c = 1.0f;
-    int k = 0;
-    for (int cur = t; cur >= 0; cur = ts.parent[cur], ++k) {
-      pidx[o + k] = static_cast<uint8_t>(cur);
-      pc[o + k] = c;
-      c *= ts.alpha[cur];
+#pragma unroll
+    for (int k = 0; k < kRegPath; ++k) {
+      if (k < D) {
+        pidx[o + k] = static_cast<uint8_t>(anc[k]);
+        pc[o + k] = cc[k];
+      }
+    }
+    if (D > kRegPath) {
+      const int last = anc[kRegPath - 1];
+      float c = cc[kRegPath - 1] * ts.alpha[last];
+      int k = kRegPath;
+      for (int cur = ts.parent[last]; cur >= 0; cur = ts.parent[cur], ++k) {
+        pidx[o + k] = static_cast<uint8_t>(cur);
+        pc[o + k] = c;
+        c *= ts.alpha[cur];
+      }
     }
   }
   return true;
@@ -259,6 +289,8 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   __shared__ __align__(8) uint64_t bars[8];
   __shared__ uint32_t tmem_holder;
   __shared__ int s_fail;
+  __shared__ int s_bad_tree;    // written by thread 0 after the tree preparation
+  __shared__ int s_mma_issued;  // written by the issuer of the first products
 
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
@@ -281,15 +313,21 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   const int wg = t >> 7;
   const int warp = t >> 5;
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  bool mma_issued = false;
   bool mma2_issued = false;
 
-  // Every thread reads the request's node range itself, so that its node of
+  // Every thread reads the request's metadata itself, so that its node of
   // the tree and (warpgroup 1) its V columns are requested straight after
   // the first memory round trip rather than after thread 0 has published
-  // the metadata.  Nothing loaded here is used unless the request's checks
+  // it.  Nothing loaded here is used unless the request's checks
   // below pass; the range test only keeps the loads inside the batch.
   const int lo_s = __ldg(b.node_offset + r), hi_s = __ldg(b.node_offset + r + 1);
+  const int slot_s = __ldg(b.state_slot + r);
+  int pa_s = -1, plo_s = 0, phi_s = 0;
+  if constexpr (FUSED) {
+    pa_s = __ldg(prev.accepted + r);
+    plo_s = __ldg(prev.node_offset + r);
+    phi_s = __ldg(prev.node_offset + r + 1);
+  }
   const int n_s = hi_s - lo_s;
   const bool range_ok = n_s > 0 && n_s <= b.max_nodes && lo_s >= 0 && static_cast<int64_t>(hi_s) <= b.T;
   int tree_p = -1;
@@ -318,19 +356,36 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
     }
   }
 
+  // Fused commit: this thread's node of the previous tree, requested the
+  // same way (used only when the previous request's checks pass).
+  int prev_p = -1;
+  float prev_al = 0.f;
+  if constexpr (FUSED) {
+    const int pn_s = phi_s - plo_s;
+    const bool prange_ok = pa_s >= 0 && pn_s > 0 && pn_s <= prev.max_nodes && plo_s >= 0 &&
+                           static_cast<int64_t>(phi_s) <= prev.T;
+    if (prange_ok && t < pn_s) {
+      const int64_t row = static_cast<int64_t>(plo_s) + t;
+      prev_p = __ldg(prev.parent + row);
+      prev_al = __ldg(prev.alpha + row * H + h);
+    }
+  }
+
   if (t == 0) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
     fence_mbarrier_init();
     s_fail = 0;
+    s_bad_tree = 0;
+    s_mma_issued = 0;
     // every further metadata load of this CTA is independent: one round trip
     const int lo = lo_s, hi = hi_s;
-    const int slot = b.state_slot[r];
+    const int slot = slot_s;
     int pa = -1, plo = 0, phi = 0;
     if constexpr (FUSED) {
-      pa = prev.accepted[r];
-      plo = prev.node_offset[r];
-      phi = prev.node_offset[r + 1];
+      pa = pa_s;
+      plo = plo_s;
+      phi = phi_s;
     }
     int flags = 0;
     const int N = hi - lo;
@@ -402,20 +457,6 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   const bool have_s0 = issued || commit_a >= 0;
   const int64_t tok0 = ts.tok0;
 
-  // the previous tree's parents and gates, requested before this tree's so
-  // that both round trips overlap
-  int prev_p = -1;
-  float prev_al = 0.f;
-  if constexpr (FUSED) {
-    if (commit_a >= 0 && t < pv.N) {
-      const int64_t row = static_cast<int64_t>(pv.tok0) + t;
-      prev_p = __ldg(prev.parent + row);
-      prev_al = __ldg(prev.alpha + row * H + h);
-    }
-  }
-
-  bool bad_tree = false;
-  if (issued) bad_tree = !prepare_tree(ts, pidx, pc, tree_p, tree_alpha, tree_beta);
 
   // Fused commit: validate the previous tree, walk the accepted node's path and
   // stage its first segment (k rows in shared memory, c_j u_j[lane] in registers).
@@ -622,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
     }
   }
   if constexpr (!SB) {
-    if (issued && !fail && !bad_tree && !bad_prev) {
+    if (issued && !fail && !bad_prev) {
       convert_row_hilo(s0 + (2 * wg) * kS0ChunkBytes + lane * 128, lane & 7);
       convert_row_hilo(s0 + (2 * wg + 1) * kS0ChunkBytes + lane * 128, lane & 7);
     }
@@ -630,8 +671,15 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   fence_proxy_async_smem();
   fail = __syncthreads_or(fail);
 
-  const bool work = issued && !bad_tree && !bad_prev;
-  if (work && !fail && t == 0) {
+  // The first products need only S0 and K/Q, not the tree: thread 64 issues
+  // them while warps 0 and 1 prepare the tree, so the walks run during the
+  // products.  (A tree found invalid leaves the products unused; they are
+  // waited for before the CTA ends.)
+  const bool go = issued && !bad_prev && !fail;
+  if (go && t < 64) {
+    const bool bad = !prepare_tree(ts, pidx, pc, tree_p, tree_alpha, tree_beta);
+    if (t == 0) s_bad_tree = bad;
+  } else if (go && t == 64) {
     if (!mbar_wait(&bars[4], 0)) {
       s_fail = 1;
     } else {
@@ -674,11 +722,13 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
         mma_bf16(tmem + 2 * NPM, dsc, dsc, id2, s ? 1u : 0u);
       }
       mma_commit(&bars[7]);
-      mma_issued = true;
+      s_mma_issued = 1;
     }
   }
   __syncthreads();
   fail |= s_fail;
+  const bool bad_tree = go && s_bad_tree;
+  const bool work = issued && !bad_tree && !bad_prev;
 
   if (work && !fail) {
     // warpgroup 1 (W^T) waits for S0 [K;Q]^T, warpgroup 0 for the Gram (both products)
@@ -858,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
       for (int i = 0; i < kChunks; ++i) mbar_wait(&bars[i], 0);
     if (issued) {
       mbar_wait(&bars[4], 0);
-      if (mma_issued) {
+      if (s_mma_issued) {
         mbar_wait(&bars[5], 0);
         mbar_wait(&bars[7], 0);
       }
