@@ -219,7 +219,8 @@ def sum_over_ranks(x: float, world: int) -> float:
 def oracle_sample(n_requests: int, seed_layer: int = 0):
     """Time the CPU oracle on the first n_requests of one layer (all heads).
 
-    Returns (nodes in the sample, seconds)."""
+    Returns (nodes in the sample, wall seconds, process CPU seconds over all
+    threads)."""
     from oracle import gdn_tree_oracle as orc
     cfg = wl.CONFIGS[CONFIG_NAME]
     w = wl.generate(cfg, R=n_requests, layer=seed_layer)
@@ -228,6 +229,7 @@ def oracle_sample(n_requests: int, seed_layer: int = 0):
     alpha, beta, parent = w.alpha.numpy(), w.beta.numpy(), w.parent.numpy()
     acc = w.accepted.numpy()
     t0 = time.perf_counter()
+    c0 = time.process_time()
     for r in range(w.R):
         lo, hi = int(node[r]), int(node[r + 1])
         S0 = w.state[int(w.state_slot[r])].numpy()
@@ -235,16 +237,21 @@ def oracle_sample(n_requests: int, seed_layer: int = 0):
                                  beta[lo:hi])
         orc.commit_request(S0, res, int(acc[r]))
     dt = time.perf_counter() - t0
-    return int(node[-1]), dt
+    return int(node[-1]), dt, time.process_time() - c0
 
 
-def cpu_baseline(n_requests: int = 64):
-    nodes, dt = oracle_sample(n_requests)
+def cores_used(wall: float, cpu: float) -> int:
+    """Threads the sample kept busy on average (CPU time over wall time)."""
+    return max(1, int(round(cpu / wall))) if wall > 0 else 1
+
+
+def cpu_baseline(n_requests: int = 160):
+    nodes, dt, cpu = oracle_sample(n_requests)
     # a full step needs every node through all 30 layers
     value = nodes / (dt * LAYERS)
-    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": value, "unit": UNIT, "cores": cores_used(dt, cpu), "kind": "oracle",
             "sample": f"fp64 numpy oracle, first {n_requests} requests x 32 heads of one layer "
-                      f"({nodes} nodes, {dt:.1f} s single-threaded), scaled to {LAYERS} layers"}
+                      f"({nodes} nodes, {dt:.1f} s wall, {cpu:.1f} s CPU), scaled to {LAYERS} layers"}
 
 
 def run_reference(args, world, rank):
@@ -253,11 +260,13 @@ def run_reference(args, world, rank):
     n_req = 8
     for _ in range(args.warmup):
         oracle_sample(n_req)
-    times, nodes = [], 0
+    times, cpus, nodes = [], [], 0
     for _ in range(args.steps):
-        nodes, dt = oracle_sample(n_req)
+        nodes, dt, cpu = oracle_sample(n_req)
         times.append(dt)
+        cpus.append(cpu)
     t = sum(times) / len(times)
+    cores = cores_used(sum(times), sum(cpus))
     value = nodes / (t * LAYERS)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1000.0 * LAYERS,
@@ -266,7 +275,7 @@ def run_reference(args, world, rank):
             "config": {"workload": "wide ragged trees (256 req x 32 heads, N 16..64, depth<=8, "
                                    "30 GDN layers); each timed step is a bounded sample",
                        "sample_requests": n_req},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"first {n_req} requests x 32 heads of one layer per step "
                                        f"({nodes} nodes), scaled to {LAYERS} layers"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -756,7 +765,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=LAYERS)
-    ap.add_argument("--cpu-requests", type=int, default=64)
+    ap.add_argument("--cpu-requests", type=int, default=160)
     ap.add_argument("--no-storeall", action="store_true")
     ap.add_argument("--study", choices=["widths", "graph", "bf16state", "fixed64"],
                     help="print one study line instead of the benchmark line (1 GPU)")
