@@ -48,7 +48,9 @@ LAYERS = 30
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_tc_wide_traffic.json")
 KERNEL_SOURCES = ["gdn_speculative_tree_gb300/csrc/verify_tc.cuh",
                   "gdn_speculative_tree_gb300/csrc/verify_tc.cu",
-                  "gdn_speculative_tree_gb300/csrc/treewy_device.cuh"]
+                  "gdn_speculative_tree_gb300/csrc/treewy_device.cuh",
+                  "gdn_speculative_tree_gb300/csrc/treewy_api.cu",
+                  "gdn_speculative_tree_gb300/csrc/treewy_internal.h"]
 
 
 def kernel_hash() -> str:

@@ -126,16 +126,19 @@ treewy_status make_maps(const treewy_batch* b, treewy::VerifyMaps* m) {
   if (st != TREEWY_OK) return st;
   const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(b->H), static_cast<cuuint64_t>(b->T)};
   const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(b->H) * 128 * 2};
-  const cuuint32_t box[3] = {64, 1, 8};
-  const void* ptrs[2] = {b->k, b->q};
-  CUtensorMap* maps[2] = {&m->k, &m->q};
-  for (int i = 0; i < 2; ++i) {
+  // boxes of 32 and 16 rows: a tree's rows, rounded up to 16, take at most
+  // two boxes per tensor and 64-column chunk
+  const cuuint32_t box16[3] = {64, 1, 16};
+  const cuuint32_t box32[3] = {64, 1, 32};
+  const void* ptrs[4] = {b->k, b->q, b->k, b->q};
+  CUtensorMap* maps[4] = {&m->k, &m->q, &m->k32, &m->q32};
+  for (int i = 0; i < 4; ++i) {
     CUresult rc = enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptrs[i]), dims,
-                      strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      strides, i < 2 ? box16 : box32, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (rc != CUDA_SUCCESS)
-      return fail(TREEWY_ERR_CUDA, "tensor map for %s failed (%d)", i ? "q" : "k", (int)rc);
+      return fail(TREEWY_ERR_CUDA, "tensor map for %s failed (%d)", (i & 1) ? "q" : "k", (int)rc);
   }
   return TREEWY_OK;
 }

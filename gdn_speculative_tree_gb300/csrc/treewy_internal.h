@@ -15,8 +15,10 @@ namespace treewy {
 struct VerifyMaps {
   CUtensorMap s0;  // state pool [rows = slots*H*128][128], box 128 rows x 128 bytes
                    // (32 fp32 or 64 bf16 columns), 128B swizzle
-  CUtensorMap k;   // keys, bf16 [T][H][128], box 64 x 1 x 8, 128B swizzle
-  CUtensorMap q;   // queries, same layout as keys
+  CUtensorMap k;    // keys, bf16 [T][H][128], box 64 x 1 x 16, 128B swizzle
+  CUtensorMap q;    // queries, same layout as keys
+  CUtensorMap k32;  // keys, box 64 x 1 x 32
+  CUtensorMap q32;  // queries, box 64 x 1 x 32
 };
 
 size_t verify_generic_smem(int dk, int dv, int npm);

@@ -277,7 +277,9 @@ template <int NPM, bool FUSED, bool SB>
 __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
     verify_tc_kernel(const __grid_constant__ CUtensorMap map_s0,
                      const __grid_constant__ CUtensorMap map_k,
-                     const __grid_constant__ CUtensorMap map_q, const treewy_batch b,
+                     const __grid_constant__ CUtensorMap map_q,
+                     const __grid_constant__ CUtensorMap map_k32,
+                     const __grid_constant__ CUtensorMap map_q32, const treewy_batch b,
                      const PrevRound prev) {
   using C = TcCfg<NPM>;
   constexpr int kChunks = SB ? 2 : 4;      // S0 boxes of 16 KB
@@ -417,26 +419,33 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
       }
     }
     if (flags == 0 && N > 0) {
-      // 2 tensors x 2 column chunks x N8 rows x 128 bytes
-      mbar_arrive_expect_tx(&bars[4], static_cast<uint32_t>((N + 7) & ~7) * 512u);
+      // 2 tensors x 2 column chunks x Np rows x 128 bytes (boxes past T are
+      // zero-filled and count in full)
+      mbar_arrive_expect_tx(&bars[4], static_cast<uint32_t>((N + 15) & ~15) * 512u);
     }
   }
   if (warp == 0) {
-    // the K and Q boxes (8 rows each) are issued by the lanes of warp 0 in
-    // parallel, after lane 0 has set up the barrier and the expected bytes
+    // the K and Q boxes are issued by the lanes of warp 0 in parallel, after
+    // lane 0 has set up the barrier and the expected bytes.  Each issue costs
+    // the issuing warp tens of cycles, so the Np = N rounded up to 16 rows of
+    // a (tensor, column chunk) come as 32-row boxes and at most one 16-row
+    // box: 4 boxes for N <= 32, 8 above, against 4 * N/8 boxes of 8 rows.
+    // Rows N..Np-1 (the next request's, or zero fill past T) are never used.
     __syncwarp();
     const int N = ts.N;
     if (ts.flags == 0 && N > 0) {
-      const int N8 = (N + 7) & ~7;
       const int Np = (N + 15) & ~15;
-      const int nbox = 4 * (N8 / 8);  // (tensor, column chunk, 8-row block)
-      for (int i = t; i < nbox; i += 32) {
-        const int c2 = (i >> 1) & 1, rb = 8 * (i >> 2);
+      const int n32 = Np >> 5;
+      const int per = n32 + ((Np >> 4) & 1);  // boxes per (tensor, column chunk)
+      for (int i = t; i < 4 * per; i += 32) {
+        const int c2 = (i >> 1) & 1, j = i >> 2, rb = 32 * j;
+        const bool big = j < n32;
         unsigned char* chunk = kq + c2 * kKQChunkBytes;
         if (i & 1)
-          tma_load_3d(chunk + (Np + rb) * 128, &map_q, &bars[4], 64 * c2, h, ts.tok0 + rb);
+          tma_load_3d(chunk + (Np + rb) * 128, big ? &map_q32 : &map_q, &bars[4], 64 * c2, h,
+                      ts.tok0 + rb);
         else
-          tma_load_3d(chunk + rb * 128, &map_k, &bars[4], 64 * c2, h, ts.tok0 + rb);
+          tma_load_3d(chunk + rb * 128, big ? &map_k32 : &map_k, &bars[4], 64 * c2, h, ts.tok0 + rb);
       }
     }
   } else if (warp == 1) {
@@ -931,8 +940,8 @@ cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, const PrevRou
       static_cast<int>(TcCfg<NPM>::kDynSmem));
   if (attr != cudaSuccess) return attr;
   const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
-  verify_tc_kernel<NPM, FUSED, SB><<<grid, kThreads, TcCfg<NPM>::kDynSmem, stream>>>(m.s0, m.k, m.q,
-                                                                                     b, prev);
+  verify_tc_kernel<NPM, FUSED, SB><<<grid, kThreads, TcCfg<NPM>::kDynSmem, stream>>>(
+      m.s0, m.k, m.q, m.k32, m.q32, b, prev);
   return cudaGetLastError();
 }
 
