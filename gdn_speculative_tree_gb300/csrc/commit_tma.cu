@@ -120,13 +120,29 @@ __global__ void __launch_bounds__(kThreads)
   const bool kbf16 = b.qkv_dtype == TREEWY_DTYPE_BF16;
   const bool lead = (h == 0 && part == 0);           // reports request-level flags
 
+  // Every thread reads the request's metadata itself (one round trip), so
+  // that threads < N request their node's parent and gate straight after it
+  // rather than after thread 0 has published it; the loads stay inside the
+  // batch and are used only when thread 0's checks pass.
+  const int a_s = __ldg(accepted + r);
+  const int lo_s = __ldg(b.node_offset + r), hi_s = __ldg(b.node_offset + r + 1);
+  const int slot_s = __ldg(b.state_slot + r);
+  const int n_s = hi_s - lo_s;
+  const bool range_ok =
+      a_s >= 0 && n_s > 0 && n_s <= b.max_nodes && lo_s >= 0 && static_cast<int64_t>(hi_s) <= b.T;
+  int node_p = -1;
+  float node_alpha = 0.f;
+  if (range_ok && t < n_s) {
+    node_p = __ldg(b.parent + lo_s + t);
+    node_alpha = __ldg(b.alpha + (static_cast<int64_t>(lo_s) + t) * H + h);
+  }
+
   if (t == 0) {
     mbar_init(&bar, 1);
     fence_mbarrier_init();
-    // independent loads: one round trip
-    const int a = accepted[r];
-    const int lo = b.node_offset[r], hi = b.node_offset[r + 1];
-    const int slot = b.state_slot[r];
+    const int a = a_s;
+    const int lo = lo_s, hi = hi_s;
+    const int slot = slot_s;
     const int N = hi - lo;
     int flags = 0;
     if (a != -1) {
@@ -161,10 +177,9 @@ __global__ void __launch_bounds__(kThreads)
   // the whole tree is validated (U of an invalid tree was never written)
   bool bad = false;
   if (t < N) {
-    const int p = __ldg(b.parent + tok0 + t);
-    bad = !(p >= -1 && p < t);
-    cs.parent[t] = static_cast<int8_t>(bad ? -1 : p);
-    cs.alpha[t] = __ldg(b.alpha + (tok0 + t) * H + h);
+    bad = !(node_p >= -1 && node_p < t);
+    cs.parent[t] = static_cast<int8_t>(bad ? -1 : node_p);
+    cs.alpha[t] = node_alpha;
   }
   bad = __syncthreads_or(bad);
   if (!bad && t == 0) {
