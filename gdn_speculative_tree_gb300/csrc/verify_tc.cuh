@@ -7,7 +7,9 @@
 //
 //  TMA      S0 (fp32 state: 64 KB as 4 boxes of 128 rows x 32 columns; bf16
 //           state: 32 KB as 2 boxes of 128 rows x 64 columns; 128B swizzle)
-//           and the tree's K and Q rows (bf16, 8-row boxes).
+//           and the tree's K and Q rows (bf16, boxes of 32 and 16 rows).
+//  tree     warps 0-1, while thread 64 issues MMA 1: gamma_n and each node's
+//           root path with the decay ratios gamma_n / gamma_{p_k}.
 //  split    fp32 state: each thread turns its own 128-byte S0 row segments in
 //           place into [hi | lo] bf16 halves, S0 ~= hi + lo (16 significant
 //           bits).  A bf16 state arrives in the operand layout as it is.
