@@ -136,6 +136,21 @@ def test_smaller_tree_capacity(cuda_lib, max_nodes, sizes):
     assert_within(compare(w, run, range(w.R)), f"max_nodes={max_nodes}")
 
 
+@pytest.mark.parametrize("sizes", [[5, 33], [40, 1, 63], [17], [64, 49]])
+def test_key_rows_padded_past_the_batch(cuda_lib, sizes):
+    """The key/query boxes cover each tree's rows rounded up to 16: the padding
+    rows are the next request's (or zero fill past the batch's last node) and
+    must not reach any output."""
+    rng = np.random.default_rng(sum(sizes))
+    trees = random_trees(rng, sizes)
+    acc = [len(t) - 1 for t in trees]
+    w = custom(trees, acc, H=2, max_nodes=64)
+    assert int(w.node_offset[-1]) % 16 != 0  # the last tree reads past the batch
+    run = GpuRun(w)
+    assert not run.status.any()
+    assert_within(compare(w, run, range(w.R)), f"padding rows {sizes}")
+
+
 @pytest.mark.parametrize("dk,dv,qkv", [(128, 128, "f32"), (48, 80, "bf16"), (16, 16, "bf16"),
                                        (128, 64, "bf16"), (3, 5, "f32")])
 def test_generic_head_sizes(cuda_lib, dk, dv, qkv):
