@@ -568,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
     }
     fail = wg ? named_bar_or<2, 128>(fail) : named_bar_or<1, 128>(fail);
   }
+  bool stored = false;  // the fused commit has stored S_a (uniform)
   if constexpr (FUSED) {
     // S_a = gamma_a S0 + sum_j c_j u_j k_j^T on this thread's own part of row
     // `lane` (columns 64wg .. 64wg+63: chunks 2wg, 2wg+1 of an fp32 tile,
@@ -650,32 +651,50 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
           for (int g = 0; g < 8; ++g)
             *reinterpret_cast<float4*>(row + ((g ^ (lane & 7)) << 4)) =
                 make_float4(x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
+          // an fp32 chunk goes back to the pool by a bulk tensor store while
+          // the next one is computed (the tile layout in shared memory is
+          // the one the loads produced; per-thread stores straight from the
+          // registers, 32 rows per warp instruction, were measured slower)
+          fence_proxy_async_smem();
+          if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+          if (lane == 0) {
+            tma_store_2d(&map_s0, s0 + (2 * wg + hb) * kS0ChunkBytes, 32 * (2 * wg + hb),
+                         (ts.slot * H + h) * kDim);
+            bulk_commit_group();
+          }
         }
       }
-      // S_a goes back to the pool by bulk tensor stores of this warpgroup's
-      // chunks (the tile layout in shared memory is the one the loads
-      // produced; per-thread stores straight from the registers, 32 rows per
-      // warp instruction, were measured slower); the chunks are converted in
-      // place only after the stores have read them
-      fence_proxy_async_smem();
-      if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
-      if (lane == 0) {
-        const int y = (ts.slot * H + h) * kDim;
-        if constexpr (SB) {
-          tma_store_2d(&map_s0, s0 + wg * kS0ChunkBytes, 64 * wg, y);
-        } else {
-          tma_store_2d(&map_s0, s0 + (2 * wg) * kS0ChunkBytes, 32 * (2 * wg), y);
-          tma_store_2d(&map_s0, s0 + (2 * wg + 1) * kS0ChunkBytes, 32 * (2 * wg + 1), y);
+      if constexpr (SB) {
+        // the bf16 chunk holds both column blocks: stored once both are done
+        fence_proxy_async_smem();
+        if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+        if (lane == 0) {
+          tma_store_2d(&map_s0, s0 + wg * kS0ChunkBytes, 64 * wg, (ts.slot * H + h) * kDim);
+          bulk_commit_group();
+          bulk_wait_group_read0();
         }
-        bulk_commit_group();
-        bulk_wait_group_read0();
+        if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+      } else if (!issued) {
+        // nothing to convert: the stores still finish reading before the CTA ends
+        if (lane == 0) bulk_wait_group_read0();
+        if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
       }
-      if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+      stored = true;
     }
   }
   if constexpr (!SB) {
     if (issued && !fail && !bad_prev) {
+      // a chunk is converted in place only after the fused commit's store has
+      // read it: the first store is waited for while the second may still run
+      if (FUSED && stored) {
+        if (lane == 0) bulk_wait_group_read1();
+        if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+      }
       convert_row_hilo(s0 + (2 * wg) * kS0ChunkBytes + lane * 128, lane & 7);
+      if (FUSED && stored) {
+        if (lane == 0) bulk_wait_group_read0();
+        if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+      }
       convert_row_hilo(s0 + (2 * wg + 1) * kS0ChunkBytes + lane * 128, lane & 7);
     }
   }
