@@ -503,7 +503,7 @@ def run_e2e(args, work, stream, world):
 
     step()
     torch.cuda.synchronize()
-    steps = max(2, min(args.steps, 5))
+    steps = max(2, min(args.steps, 10))
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
