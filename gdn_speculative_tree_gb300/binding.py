@@ -74,7 +74,8 @@ class TreewyBatch(ctypes.Structure):
 _lib: Optional[ctypes.CDLL] = None
 
 ENTRY_POINTS = ("treewy_verify", "treewy_commit", "treewy_commit_verify", "treewy_storeall_verify",
-                "treewy_storeall_commit", "treewy_last_error", "treewy_version")
+                "treewy_storeall_commit", "treewy_selftest_wait_timeout", "treewy_last_error",
+                "treewy_version")
 
 
 def load(path: Optional[str] = None) -> ctypes.CDLL:
@@ -95,8 +96,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.treewy_commit_verify.argtypes = [bp, vp, bp, vp]
     lib.treewy_storeall_verify.argtypes = [bp, vp, vp]
     lib.treewy_storeall_commit.argtypes = [bp, vp, vp, vp]
+    lib.treewy_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint32, vp]
     for name in ("treewy_verify", "treewy_commit", "treewy_commit_verify", "treewy_storeall_verify",
-                 "treewy_storeall_commit"):
+                 "treewy_storeall_commit", "treewy_selftest_wait_timeout"):
         getattr(lib, name).restype = ctypes.c_int
     lib.treewy_last_error.argtypes = []
     lib.treewy_last_error.restype = ctypes.c_char_p
@@ -135,6 +137,13 @@ def treewy_last_error() -> str:
 
 def treewy_version() -> str:
     return load().treewy_version().decode()
+
+
+def treewy_selftest_wait_timeout(status, limit_us: int, stream=None) -> None:
+    """Diagnostic of the bounded barrier wait: ``status`` is a device int32
+    tensor of 3 words (status[0] gets TREEWY_STATUS_TIMEOUT, status[1:3] the
+    wait in nanoseconds, low and high word)."""
+    _check(load().treewy_selftest_wait_timeout(_ptr(status), int(limit_us), _stream_handle(stream)))
 
 
 def treewy_verify(batch: TreewyBatch, stream=None) -> None:

@@ -168,6 +168,17 @@ const char* treewy_last_error(void) { return g_last_error.c_str(); }
 
 const char* treewy_version(void) { return "treewy-gb300 0.1 (sm_103a)"; }
 
+treewy_status treewy_selftest_wait_timeout(int32_t* status, uint32_t limit_us, cudaStream_t stream) {
+  g_last_error.clear();
+  if (status == nullptr) return fail(TREEWY_ERR_INVALID_ARG, "status is NULL");
+  if ((reinterpret_cast<uintptr_t>(status) & 3u) != 0)
+    return fail(TREEWY_ERR_INVALID_ARG, "status is not 4-byte aligned");
+  if (limit_us < 1u || limit_us > 10000000u)
+    return fail(TREEWY_ERR_INVALID_ARG, "limit_us %u outside 1 .. 10,000,000", limit_us);
+  const cudaError_t err = treewy::launch_wait_selftest(status, limit_us, stream);
+  return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_selftest_wait_timeout launch");
+}
+
 treewy_status treewy_verify(const treewy_batch* batch, cudaStream_t stream) {
   g_last_error.clear();
   treewy_status st = validate(batch, true, true, true);

@@ -57,4 +57,7 @@ cudaError_t launch_storeall_verify(const treewy_batch& b, float* snapshots, cuda
 cudaError_t launch_storeall_commit(const treewy_batch& b, const float* snapshots,
                                    const int32_t* accepted, cudaStream_t stream);
 
+// One thread waiting for a barrier phase nothing completes (bounded).
+cudaError_t launch_wait_selftest(int32_t* status, uint32_t limit_us, cudaStream_t stream);
+
 }  // namespace treewy

@@ -221,6 +221,21 @@ treewy_status treewy_storeall_verify(const treewy_batch* batch, float* snapshots
 treewy_status treewy_storeall_commit(const treewy_batch* batch, const float* snapshots,
                                      const int32_t* accepted, cudaStream_t stream);
 
+/*
+ * treewy_selftest_wait_timeout -- diagnostic of the kernels' bounded waits.
+ *
+ * Launches one thread that waits, with the same bounded wait every kernel
+ * uses on its barriers, for a barrier phase that nothing completes, giving
+ * up after limit_us microseconds (1 .. 10,000,000).  It then ORs
+ * TREEWY_STATUS_TIMEOUT into status[0] and writes the measured wait in
+ * nanoseconds to the two int32 words status[1] (low) and status[2] (high).
+ * status: device int32 [3], caller-owned; the caller zeroes status[0].
+ * Shows that a wait which never completes returns control, reports through
+ * the status word and leaves the CUDA context usable.
+ */
+treewy_status treewy_selftest_wait_timeout(int32_t* status, uint32_t limit_us,
+                                           cudaStream_t stream);
+
 /* Message for the last non-OK return on the calling host thread ("" if none). */
 const char* treewy_last_error(void);
 

@@ -19,6 +19,8 @@ static void expect(int cond, const char* what) {
 int main(void) {
   expect(strstr(treewy_version(), "sm_103a") != NULL, "version names sm_103a");
   expect(treewy_verify(NULL, 0) == TREEWY_ERR_INVALID_ARG, "NULL batch rejected");
+  expect(treewy_selftest_wait_timeout(NULL, 1000, 0) == TREEWY_ERR_INVALID_ARG,
+         "wait self-test without a status word rejected");
 
   treewy_batch b;
   memset(&b, 0, sizeof b);

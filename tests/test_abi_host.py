@@ -169,3 +169,12 @@ def test_too_many_request_head_pairs(lib):
     b.R, b.H = 1 << 20, 1 << 12
     assert lib.treewy_verify(ctypes.byref(b), None) == binding.TREEWY_ERR_UNSUPPORTED
     assert b"R * H" in lib.treewy_last_error()
+
+
+def test_wait_selftest_validates_before_launch(lib):
+    # rejected on the host: no status word, a misaligned one, limits outside 1 .. 1e7 us
+    assert lib.treewy_selftest_wait_timeout(None, 1000, None) == binding.TREEWY_ERR_INVALID_ARG
+    assert lib.treewy_selftest_wait_timeout(0x10002, 1000, None) == binding.TREEWY_ERR_INVALID_ARG
+    assert lib.treewy_selftest_wait_timeout(0x10000, 0, None) == binding.TREEWY_ERR_INVALID_ARG
+    assert lib.treewy_selftest_wait_timeout(0x10000, 10_000_001, None) == binding.TREEWY_ERR_INVALID_ARG
+    assert "limit_us" in lib.treewy_last_error().decode()
