@@ -24,7 +24,7 @@ def np32(x: torch.Tensor) -> np.ndarray:
     return x.detach().to("cpu").to(torch.float32).numpy()
 
 
-class GpuRun:
+class CudaRun:
     """Verify + commit of one Workload on the GPU (Workload tensors on cuda).
 
     Keeps a CPU copy of the state pool as it was before the in-place commit.
@@ -54,7 +54,7 @@ def oracle_request(wl, r, S0_pool):
     return lo, hi, S0, res
 
 
-def compare(wl, run: GpuRun, requests, accepted=None, check_commit=True):
+def compare(wl, run: CudaRun, requests, accepted=None, check_commit=True):
     """Error ratios of o, U, gamma and the committed state over `requests`."""
     acc = (wl.accepted if accepted is None else accepted).cpu().numpy()
     slot = wl.state_slot.cpu().numpy()

@@ -17,7 +17,7 @@ import torch
 from gdn_speculative_tree_gb300 import binding
 from gdn_speculative_tree_gb300 import workloads as wl
 from oracle import gdn_tree_oracle as orc
-from tests.gpu_helpers import GpuRun, O_TOL, U_TOL, G_TOL, np32, oracle_request
+from tests.gpu_helpers import CudaRun, O_TOL, U_TOL, G_TOL, np32, oracle_request
 
 pytestmark = pytest.mark.gpu
 
@@ -72,7 +72,7 @@ def test_bf16_state_mixed_trees(cuda_lib, flags):
     acc[10] = 63
     acc[3] = -1
     w = custom(trees, acc)
-    run = GpuRun(w, flags=flags)
+    run = CudaRun(w, flags=flags)
     assert not run.status.any()
     check_run(w, run, range(w.R))
 
@@ -86,7 +86,7 @@ def test_bf16_state_generic_head_sizes(cuda_lib, dk, dv, qkv):
     trees = random_trees(rng, [9, 23, 1, 40]) + [wl.chain_parents(40)]
     acc = [4, 22, 0, -1, 39]
     w = custom(trees, acc, dk=dk, dv=dv, qkv=qkv, H=2)
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     check_run(w, run, range(w.R))
 
@@ -94,7 +94,7 @@ def test_bf16_state_generic_head_sizes(cuda_lib, dk, dv, qkv):
 def test_bf16_state_wide_full_size_sampled(cuda_lib):
     cfg = wl.CONFIGS["wide"]
     w = wl.generate(cfg, device="cuda", state_dtype="bf16")
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     rng = np.random.default_rng(77)
     reqs = sorted(set(rng.choice(w.R, 4, replace=False).tolist()) | {w.R - 1})

@@ -10,7 +10,7 @@ import torch
 
 from gdn_speculative_tree_gb300 import binding
 from gdn_speculative_tree_gb300 import workloads as wl
-from tests.gpu_helpers import GpuRun, assert_within, compare
+from tests.gpu_helpers import CudaRun, assert_within, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -51,7 +51,7 @@ def test_commit_kernels_bit_identical(cuda_lib, state_dtype):
 
 def test_commit_tma_wide_oracle(cuda_lib):
     w = wl.generate(wl.CONFIGS["wide"], R=16).to("cuda")
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     assert_within(compare(w, run, range(w.R)), "wide R=16, bulk-copy commit")
 
@@ -62,6 +62,6 @@ def test_commit_tma_f32_keys(cuda_lib):
     trees, acc = trees_with_long_paths(rng)
     w = wl.assemble(trees, np.asarray(acc, np.int32), 2, 128, 128, "f32", 0.05, (0.9, 0.999),
                     ("sigmoid",), seed=4, max_nodes=64).to("cuda")
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     assert_within(compare(w, run, range(w.R)), "f32 keys")

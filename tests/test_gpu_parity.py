@@ -11,7 +11,7 @@ import torch
 from gdn_speculative_tree_gb300 import binding
 from gdn_speculative_tree_gb300 import workloads as wl
 from oracle import gdn_tree_oracle as orc
-from tests.gpu_helpers import GpuRun, assert_within, compare, np32, oracle_request
+from tests.gpu_helpers import CudaRun, assert_within, compare, np32, oracle_request
 
 pytestmark = pytest.mark.gpu
 
@@ -25,14 +25,14 @@ def cpu_then_cuda(name, R=None, **over):
 
 def test_tiny_chain_fp32(cuda_lib):
     w = cpu_then_cuda("tiny")
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert run.status.tolist() == [0]
     assert_within(compare(w, run, [0]), "tiny")
 
 
 def test_chain_full(cuda_lib):
     w = cpu_then_cuda("chain")
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     assert (w.accepted == -1).any()  # the no-op commit is exercised
     assert_within(compare(w, run, range(w.R)), "chain")
@@ -40,21 +40,21 @@ def test_chain_full(cuda_lib):
 
 def test_binary_full(cuda_lib):
     w = cpu_then_cuda("binary")
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     assert_within(compare(w, run, range(w.R)), "binary")
 
 
 def test_wide_reduced_all_requests(cuda_lib):
     w = cpu_then_cuda("wide", R=12)
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     assert_within(compare(w, run, range(w.R)), "wide R=12")
 
 
 def test_stress_reduced_all_requests(cuda_lib):
     w = cpu_then_cuda("stress", R=3)
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert_within(compare(w, run, range(w.R)), "stress R=3")
 
 
@@ -64,7 +64,7 @@ def test_full_size_sampled(cuda_lib, name, nsample):
     the oracle checks a sample of requests (all heads each) one by one."""
     cfg = wl.CONFIGS[name]
     w = wl.generate(cfg, device="cuda")
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     rng = np.random.default_rng(1234)
     reqs = sorted(set(rng.choice(w.R, nsample - 1, replace=False).tolist()) | {w.R - 1})
@@ -109,7 +109,7 @@ def test_random_and_degenerate_trees(cuda_lib, flags):
     rng = np.random.default_rng(5)
     trees, acc = mixed_trees(rng)
     w = custom(trees, acc)
-    run = GpuRun(w, flags=flags)
+    run = CudaRun(w, flags=flags)
     assert not run.status.any()
     assert_within(compare(w, run, range(w.R)), f"mixed flags={flags}")
 
@@ -121,7 +121,7 @@ def test_gate_edges(cuda_lib, alpha, beta):
     rng = np.random.default_rng(9)
     trees, acc = mixed_trees(rng)
     w = custom(trees, acc, alpha=alpha, beta=beta, seed=31)
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert_within(compare(w, run, range(w.R)), f"gates {alpha} {beta}")
 
 
@@ -131,7 +131,7 @@ def test_smaller_tree_capacity(cuda_lib, max_nodes, sizes):
     trees = random_trees(rng, sizes)
     acc = [len(t) - 1 for t in trees]
     w = custom(trees, acc, max_nodes=max_nodes, H=3)
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     assert_within(compare(w, run, range(w.R)), f"max_nodes={max_nodes}")
 
@@ -146,7 +146,7 @@ def test_key_rows_padded_past_the_batch(cuda_lib, sizes):
     acc = [len(t) - 1 for t in trees]
     w = custom(trees, acc, H=2, max_nodes=64)
     assert int(w.node_offset[-1]) % 16 != 0  # the last tree reads past the batch
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     assert_within(compare(w, run, range(w.R)), f"padding rows {sizes}")
 
@@ -158,7 +158,7 @@ def test_generic_head_sizes(cuda_lib, dk, dv, qkv):
     trees = random_trees(rng, [9, 23, 1, 40])
     acc = [4, 22, 0, -1]
     w = custom(trees, acc, dk=dk, dv=dv, qkv=qkv, H=2)
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     assert_within(compare(w, run, range(w.R)), f"dk={dk} dv={dv} {qkv}")
 
@@ -218,7 +218,7 @@ def test_storeall_matches_oracle(cuda_lib, name, R, chunks):
 def test_storeall_and_treewy_commit_agree(cuda_lib):
     w1 = cpu_then_cuda("binary", R=10)
     w2 = cpu_then_cuda("binary", R=10)
-    GpuRun(w1)
+    CudaRun(w1)
     run_storeall(w2)
     d = (w1.state - w2.state).abs().max().item()
     assert d <= 1e-3 * w2.state.abs().max().item()
@@ -262,7 +262,7 @@ def test_bad_inputs_set_status_and_spare_others(cuda_lib):
 
 def test_graph_replay_matches_eager(cuda_lib):
     w_eager = cpu_then_cuda("wide", R=16)
-    run = GpuRun(w_eager)
+    run = CudaRun(w_eager)
     w = cpu_then_cuda("wide", R=16)
     S0 = w.state.clone()
     tv = binding.TreeVerifier(w)

@@ -8,7 +8,7 @@ import torch
 
 from gdn_speculative_tree_gb300 import binding
 from gdn_speculative_tree_gb300 import workloads as wl
-from tests.gpu_helpers import GpuRun, assert_within, compare
+from tests.gpu_helpers import CudaRun, assert_within, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -25,6 +25,6 @@ def test_wait_gives_up_and_reports(cuda_lib, limit_us):
 
     # the context still runs the hot path correctly afterwards
     w = wl.generate(wl.CONFIGS["binary"], R=4).to("cuda")
-    run = GpuRun(w)
+    run = CudaRun(w)
     assert not run.status.any()
     assert_within(compare(w, run, range(w.R)), "after a timed-out wait")
