@@ -6,8 +6,6 @@ seeded data), and the timing reductions take the max (time) and the sum
 import os
 import socket
 
-import pytest
-import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 

@@ -1,5 +1,4 @@
 """Host-side checks of the seeded workload generator (tree shapes, layouts)."""
-import numpy as np
 import torch
 
 from gdn_speculative_tree_gb300 import workloads as wl
