@@ -17,7 +17,7 @@ import torch
 from gdn_speculative_tree_gb300 import binding
 from gdn_speculative_tree_gb300 import workloads as wl
 from oracle import gdn_tree_oracle as orc
-from tests.gpu_helpers import CudaRun, O_TOL, U_TOL, G_TOL, np32, oracle_request
+from tests.gpu_helpers import CudaRun, FLT_MIN, O_TOL, U_TOL, G_TOL, np32, oracle_request
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,8 @@ def check_run(w, run, requests):
             o_max = max(o_max, float(np.abs(ref.o).max()))
             u_err = max(u_err, float(np.abs(run.U[lo:hi] - ref.U).max()))
             u_max = max(u_max, float(np.abs(ref.U).max()))
-            g_err = max(g_err, float((np.abs(run.gamma[lo:hi] - ref.gamma) / ref.gamma).max()))
+            g_err = max(g_err, float((np.abs(run.gamma[lo:hi] - ref.gamma) /
+                                      np.maximum(ref.gamma, FLT_MIN)).max()))
         S_ref = orc.commit_request(S0, ref, int(acc[r]))
         S_gpu = np32(w.state[int(slot[r])]).astype(np.float64)
         bound = S_REL * np.abs(S_ref) + S_ABS * np.abs(S_ref).max()

@@ -125,6 +125,23 @@ def test_gate_edges(cuda_lib, alpha, beta):
     assert_within(compare(w, run, range(w.R)), f"gates {alpha} {beta}")
 
 
+@pytest.mark.parametrize("alpha,beta", [((1.0, 1.0), ("const", 1.0)),     # no decay, full writes
+                                        ((0.9, 0.999), ("const", 0.0)),   # no writes: U = 0
+                                        ((0.01, 0.05), ("uniform", 0.05, 0.95))])  # strong decay
+def test_degenerate_gates_on_chains_and_trees(cuda_lib, alpha, beta):
+    """Gates at the ends of their range, on 64-node chains (paths past the
+    register-held length of 8) beside random trees: alpha at 1 (clamped to the
+    largest float below 1), beta exactly 1 or 0, and decays that underflow
+    gamma along a long chain."""
+    rng = np.random.default_rng(23)
+    trees = [wl.chain_parents(64), wl.chain_parents(9)] + random_trees(rng, [64, 33, 5])
+    acc = [63, 8, int(rng.integers(0, 64)), 32, 0]
+    w = custom(trees, acc, alpha=alpha, beta=beta, seed=37, H=3)
+    run = CudaRun(w)
+    assert not run.status.any()
+    assert_within(compare(w, run, range(w.R)), f"gates {alpha} {beta}")
+
+
 @pytest.mark.parametrize("max_nodes,sizes", [(16, [1, 7, 16, 9, 16, 3]), (32, [17, 32, 1, 30])])
 def test_smaller_tree_capacity(cuda_lib, max_nodes, sizes):
     rng = np.random.default_rng(max_nodes)
