@@ -29,6 +29,7 @@ STATUS_TOO_MANY_NODES = 2
 STATUS_BAD_ACCEPTED = 4
 STATUS_BAD_SLOT = 8
 STATUS_TIMEOUT = 16
+STATUS_COMMIT_REFUSED = 32
 
 DTYPE_BF16 = 0
 DTYPE_F32 = 1

@@ -64,7 +64,7 @@ struct StateVec {
 // registers (a three-block cap spills them and was measured slower).
 template <bool SB>
 __global__ void __launch_bounds__(kThreads, 2)
-    commit_kernel(const treewy_batch b, const int32_t* __restrict__ accepted) {
+    commit_kernel(const treewy_batch b, const int32_t* __restrict__ accepted, int refused_bit) {
   using SV = StateVec<SB>;
   constexpr int E = SV::E;
   constexpr int kNV = 128 * 128 / (E * kThreads);  // vectors per thread for a 128 x 128 state
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int a = s_info[3];
   if (a == -1) return;  // nothing accepted: the state is neither read nor written
   if (s_info[4]) {
-    if (t == 0 && h == 0) atomicOr(b.status + r, s_info[4]);
+    if (t == 0 && h == 0) atomicOr(b.status + r, s_info[4] | refused_bit);
     return;
   }
   const int64_t tok0 = s_info[0];
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     s_alpha[t] = __ldg(b.alpha + (tok0 + t) * H + h);
   }
   if (__syncthreads_or(bad_parent)) {
-    if (t == 0 && h == 0) atomicOr(b.status + r, TREEWY_STATUS_BAD_TREE);
+    if (t == 0 && h == 0) atomicOr(b.status + r, TREEWY_STATUS_BAD_TREE | refused_bit);
     return;
   }
   if (t == 0) {
@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   const int len = s_info[5];
   if (len < 0) {
-    if (t == 0 && h == 0) atomicOr(b.status + r, TREEWY_STATUS_BAD_TREE);
+    if (t == 0 && h == 0) atomicOr(b.status + r, TREEWY_STATUS_BAD_TREE | refused_bit);
     return;
   }
   const float ga = s_gamma_a;
@@ -285,12 +285,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 }  // namespace
 
-cudaError_t launch_commit(const treewy_batch& b, const int32_t* accepted, cudaStream_t stream) {
+cudaError_t launch_commit(const treewy_batch& b, const int32_t* accepted, int refused_bit,
+                          cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
   if (b.flags & TREEWY_FLAG_STATE_BF16)
-    commit_kernel<true><<<grid, kThreads, 0, stream>>>(b, accepted);
+    commit_kernel<true><<<grid, kThreads, 0, stream>>>(b, accepted, refused_bit);
   else
-    commit_kernel<false><<<grid, kThreads, 0, stream>>>(b, accepted);
+    commit_kernel<false><<<grid, kThreads, 0, stream>>>(b, accepted, refused_bit);
   return cudaGetLastError();
 }
 

@@ -102,7 +102,7 @@ __device__ __forceinline__ void store_block(unsigned char* tile, int d, int blk,
 template <bool SB>
 __global__ void __launch_bounds__(kThreads)
     commit_tma_kernel(const __grid_constant__ CUtensorMap map_s, const treewy_batch b,
-                      const int32_t* __restrict__ accepted) {
+                      const int32_t* __restrict__ accepted, int refused_bit) {
   using C = CommitCfg<SB>;
   __shared__ __align__(1024) unsigned char tile[kTileBytes];
   __shared__ CommitSmem cs;
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads)
   const int a = cs.a;
   if (a < 0) {
     // nothing accepted (state neither read nor written) or a bad request
-    if (t == 0 && lead && cs.flags) atomicOr(b.status + r, cs.flags);
+    if (t == 0 && lead && cs.flags) atomicOr(b.status + r, cs.flags | refused_bit);
     return;
   }
   const int64_t tok0 = cs.tok0;
@@ -229,7 +229,8 @@ __global__ void __launch_bounds__(kThreads)
   if (bad || fail) {
     if (t == 0) {
       if (fail) mbar_wait(&bar, 0);  // nothing may still target this CTA's memory
-      const int bits = (fail ? kStatusTimeout : 0) | ((bad && lead) ? TREEWY_STATUS_BAD_TREE : 0);
+      int bits = (fail ? kStatusTimeout : 0) | ((bad && lead) ? TREEWY_STATUS_BAD_TREE : 0);
+      if (bits) bits |= refused_bit;
       if (bits) atomicOr(b.status + r, bits);
     }
     return;
@@ -286,24 +287,26 @@ __global__ void __launch_bounds__(kThreads)
 
 template <bool SB>
 cudaError_t launch(const treewy_batch& b, const CUtensorMap& map, const int32_t* accepted,
-                   cudaStream_t stream) {
+                   int refused_bit, cudaStream_t stream) {
   // the whole unified L1/shared array as shared memory: six 38 KB CTAs per SM
-  static cudaError_t attr = cudaFuncSetAttribute(
-      commit_tma_kernel<SB>, cudaFuncAttributePreferredSharedMemoryCarveout,
-      static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t attr = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(commit_tma_kernel<SB>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  });
   if (attr != cudaSuccess) return attr;
   const unsigned grid =
       static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H) * CommitCfg<SB>::kSplit;
-  commit_tma_kernel<SB><<<grid, kThreads, 0, stream>>>(map, b, accepted);
+  commit_tma_kernel<SB><<<grid, kThreads, 0, stream>>>(map, b, accepted, refused_bit);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_commit_tma(const treewy_batch& b, const CUtensorMap& state_map,
-                              const int32_t* accepted, cudaStream_t stream) {
-  if (b.flags & TREEWY_FLAG_STATE_BF16) return launch<true>(b, state_map, accepted, stream);
-  return launch<false>(b, state_map, accepted, stream);
+                              const int32_t* accepted, int refused_bit, cudaStream_t stream) {
+  if (b.flags & TREEWY_FLAG_STATE_BF16) return launch<true>(b, state_map, accepted, refused_bit, stream);
+  return launch<false>(b, state_map, accepted, refused_bit, stream);
 }
 
 }  // namespace treewy

@@ -331,8 +331,11 @@ cudaError_t launch_storeall_verify(const treewy_batch& b, float* snapshots, cuda
   const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
   if (b.dk == 128 && b.dv == 128) {
     const size_t smem = sizeof(float) * 3 * kMaxNodes * 128;
-    static cudaError_t attr = cudaFuncSetAttribute(
-        storeall_verify_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    static std::atomic<uint64_t> attr_done{0};
+    const cudaError_t attr = once_per_device(attr_done, [smem] {
+      return cudaFuncSetAttribute(storeall_verify_rows_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    });
     if (attr != cudaSuccess) return attr;
     storeall_verify_rows_kernel<<<grid, kThreads, smem, stream>>>(b, snapshots);
     return cudaGetLastError();

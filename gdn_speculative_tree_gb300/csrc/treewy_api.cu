@@ -145,17 +145,17 @@ treewy_status make_maps(const treewy_batch* b, treewy::VerifyMaps* m) {
 
 // Commit with the bulk-copy kernel for dk = dv = 128 (unless the portable
 // kernels are forced), with the register-streaming kernel otherwise.
-treewy_status launch_commit_any(const treewy_batch* b, const int32_t* accepted, cudaStream_t stream,
-                                const char* what) {
+treewy_status launch_commit_any(const treewy_batch* b, const int32_t* accepted, int refused_bit,
+                                cudaStream_t stream, const char* what) {
   cudaError_t err;
   if (b->dk == 128 && b->dv == 128 && (b->flags & TREEWY_FLAG_FORCE_GENERIC) == 0) {
     // tiles of 64 rows for an f32 pool (two CTAs per head), 128 rows for bf16
     CUtensorMap map;
     treewy_status st = make_state_map(b, &map, (b->flags & TREEWY_FLAG_STATE_BF16) ? 128u : 64u);
     if (st != TREEWY_OK) return st;
-    err = treewy::launch_commit_tma(*b, map, accepted, stream);
+    err = treewy::launch_commit_tma(*b, map, accepted, refused_bit, stream);
   } else {
-    err = treewy::launch_commit(*b, accepted, stream);
+    err = treewy::launch_commit(*b, accepted, refused_bit, stream);
   }
   return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, what);
 }
@@ -203,7 +203,7 @@ treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted, 
   if (st != TREEWY_OK || batch->R == 0) return st;
   if (!batch->U && batch->T > 0) return fail(TREEWY_ERR_INVALID_ARG, "U is NULL");
   if (!accepted) return fail(TREEWY_ERR_INVALID_ARG, "accepted is NULL");
-  return launch_commit_any(batch, accepted, stream, "treewy_commit launch");
+  return launch_commit_any(batch, accepted, 0, stream, "treewy_commit launch");
 }
 
 treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev_accepted,
@@ -245,7 +245,8 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
   // commit's status bits going to next->status as on the fused path
   treewy_batch pc = *prev;
   pc.status = next->status;
-  st = launch_commit_any(&pc, prev_accepted, stream, "treewy_commit_verify (commit) launch");
+  st = launch_commit_any(&pc, prev_accepted, TREEWY_STATUS_COMMIT_REFUSED, stream,
+                         "treewy_commit_verify (commit) launch");
   if (st != TREEWY_OK) return st;
   return treewy_verify(next, stream);
 }

@@ -2,13 +2,31 @@
 // translation units (launchers); not part of the public C ABI.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
+#include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "treewy.h"
 
 namespace treewy {
+
+// Runs `set` (a cudaFuncSetAttribute call) once per device: the attributes
+// are per device and function, so a process driving several GPUs needs them
+// on each.  `done` is a per-call-site bit mask of the devices already set
+// (ordinals >= 64 are set on every call).
+template <typename F>
+cudaError_t once_per_device(std::atomic<uint64_t>& done, F&& set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Tensor maps the tensor-core verify kernel reads through (built on the host
 // per call; passed by value as kernel parameters).
@@ -48,10 +66,14 @@ cudaError_t launch_commit_verify_tc(const treewy_batch& next, const PrevRound& p
 cudaError_t launch_verify_tc_bf16state(const treewy_batch& b, const VerifyMaps& maps,
                                        const PrevRound* prev, int npm, cudaStream_t stream);
 
-cudaError_t launch_commit(const treewy_batch& b, const int32_t* accepted, cudaStream_t stream);
+// refused_bit: extra status bit OR-ed in, beside the reason, when a request's
+// commit is refused (TREEWY_STATUS_COMMIT_REFUSED inside treewy_commit_verify,
+// 0 for treewy_commit).
+cudaError_t launch_commit(const treewy_batch& b, const int32_t* accepted, int refused_bit,
+                          cudaStream_t stream);
 // dk = dv = 128: the state tile moved by bulk tensor copies (state_map as VerifyMaps::s0).
 cudaError_t launch_commit_tma(const treewy_batch& b, const CUtensorMap& state_map,
-                              const int32_t* accepted, cudaStream_t stream);
+                              const int32_t* accepted, int refused_bit, cudaStream_t stream);
 
 cudaError_t launch_storeall_verify(const treewy_batch& b, float* snapshots, cudaStream_t stream);
 cudaError_t launch_storeall_commit(const treewy_batch& b, const float* snapshots,

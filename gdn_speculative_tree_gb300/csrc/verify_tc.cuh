@@ -74,7 +74,9 @@ struct TreeTC {
   float2 bbg[kMaxNodes];                // (beta_n, beta_n * gamma_n)
   int D[kMaxNodes];                     // path length root..n, n included
   int off[kMaxNodes + 1];               // CSR offsets of the path lists
-  int tok0, N, slot, flags;
+  int tok0, N, slot;
+  int flags;   // this round's request errors (node range, slot): verification skipped
+  int cflags;  // fused commit refused: the previous round's errors | COMMIT_REFUSED
 };
 
 // Tree preparation by the 64 threads of warps 0 and 1 (thread n = node n;
@@ -391,28 +393,35 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
       plo = plo_s;
       phi = phi_s;
     }
+    // errors of this round's request (they skip its verification) and of the
+    // previous round (they refuse the fused commit) are kept apart, so that
+    // either half runs exactly when the corresponding separate call would
     int flags = 0;
     const int N = hi - lo;
     if (N < 0 || N > b.max_nodes) flags |= TREEWY_STATUS_TOO_MANY_NODES;
     else if (lo < 0 || static_cast<int64_t>(hi) > b.T) flags |= TREEWY_STATUS_BAD_TREE;
-    if (slot < 0 || static_cast<int64_t>(slot) >= b.num_slots) flags |= TREEWY_STATUS_BAD_SLOT;
+    const bool bad_slot = slot < 0 || static_cast<int64_t>(slot) >= b.num_slots;
+    if (bad_slot) flags |= TREEWY_STATUS_BAD_SLOT;
+    int cflags = 0;
     if constexpr (FUSED) {
       // the previous round's accepted node and tree range for this request
       if (pa != -1) {
         const int pn = phi - plo;
-        if (pn < 0 || pn > prev.max_nodes) flags |= TREEWY_STATUS_TOO_MANY_NODES;
-        else if (plo < 0 || static_cast<int64_t>(phi) > prev.T) flags |= TREEWY_STATUS_BAD_TREE;
-        if (pa < -1 || pa >= pn) flags |= TREEWY_STATUS_BAD_ACCEPTED;
+        if (pn < 0 || pn > prev.max_nodes) cflags |= TREEWY_STATUS_TOO_MANY_NODES;
+        else if (plo < 0 || static_cast<int64_t>(phi) > prev.T) cflags |= TREEWY_STATUS_BAD_TREE;
+        if (pa < -1 || pa >= pn) cflags |= TREEWY_STATUS_BAD_ACCEPTED;
+        if (cflags || bad_slot) cflags |= TREEWY_STATUS_COMMIT_REFUSED;
         pv.tok0 = plo;
         pv.N = pn;
       }
-      pv.a = flags ? -1 : pa;
+      pv.a = cflags ? -1 : pa;
     }
     ts.tok0 = lo;
     ts.N = flags ? 0 : N;
     ts.slot = slot;
     ts.flags = flags;
-    if (flags == 0 && (N > 0 || pa >= 0)) {
+    ts.cflags = cflags;
+    if (!bad_slot && ((flags == 0 && N > 0) || (FUSED && cflags == 0 && pa >= 0))) {
       const int y = (slot * H + h) * kDim;
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
@@ -561,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   // Waits on an mbarrier are done by one thread per warpgroup; the others
   // sleep at a hardware barrier instead of spinning.
   int fail = 0;
-  if (have_s0 && !bad_prev) {
+  if (have_s0) {
     if (lane == 0) {
       if constexpr (SB) fail = !mbar_wait(&bars[wg], 0);
       else fail = !(mbar_wait(&bars[2 * wg], 0) && mbar_wait(&bars[2 * wg + 1], 0));
@@ -683,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
     }
   }
   if constexpr (!SB) {
-    if (issued && !fail && !bad_prev) {
+    if (issued && !fail) {
       // a chunk is converted in place only after the fused commit's store has
       // read it: the first store is waited for while the second may still run
       if (FUSED && stored) {
@@ -705,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   // them while warps 0 and 1 prepare the tree, so the walks run during the
   // products.  (A tree found invalid leaves the products unused; they are
   // waited for before the CTA ends.)
-  const bool go = issued && !bad_prev && !fail;
+  const bool go = issued && !fail;
   if (go && t < 64) {
     const bool bad = !prepare_tree(ts, pidx, pc, tree_p, tree_alpha, tree_beta);
     if (t == 0) s_bad_tree = bad;
@@ -758,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   __syncthreads();
   fail |= s_fail;
   const bool bad_tree = go && s_bad_tree;
-  const bool work = issued && !bad_tree && !bad_prev;
+  const bool work = issued && !bad_tree;
 
   if (work && !fail) {
     // warpgroup 1 (W^T) waits for S0 [K;Q]^T, warpgroup 0 for the Gram (both products)
@@ -931,7 +940,11 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
 
   if (t == 0) {
     int bits = (fail ? kStatusTimeout : 0);
-    if (h == 0) bits |= ts.flags | ((bad_tree || bad_prev) ? TREEWY_STATUS_BAD_TREE : 0);
+    if (h == 0) bits |= ts.flags | ts.cflags | (bad_tree ? TREEWY_STATUS_BAD_TREE : 0);
+    // the previous round's tree failed its checks, or a wait gave up before
+    // S_a was stored: that request's commit did not happen
+    if (bad_prev && h == 0) bits |= TREEWY_STATUS_BAD_TREE | TREEWY_STATUS_COMMIT_REFUSED;
+    if (fail && commit_now && !stored) bits |= TREEWY_STATUS_COMMIT_REFUSED;
     if (bits) atomicOr(b.status + r, bits);
     // No async copy or MMA may still target this CTA's memory at exit.
     if (have_s0)
@@ -956,9 +969,12 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
 template <int NPM, bool FUSED, bool SB>
 cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, const PrevRound& prev,
                        cudaStream_t stream) {
-  static cudaError_t attr = cudaFuncSetAttribute(
-      verify_tc_kernel<NPM, FUSED, SB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-      static_cast<int>(TcCfg<NPM>::kDynSmem));
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t attr = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(verify_tc_kernel<NPM, FUSED, SB>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(TcCfg<NPM>::kDynSmem));
+  });
   if (attr != cudaSuccess) return attr;
   const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
   verify_tc_kernel<NPM, FUSED, SB><<<grid, kThreads, TcCfg<NPM>::kDynSmem, stream>>>(

@@ -62,8 +62,12 @@ enum {
   TREEWY_STATUS_TOO_MANY_NODES = 2, /* N_r > max_nodes (or N_r < 0) */
   TREEWY_STATUS_BAD_ACCEPTED = 4,   /* accepted[r] outside [-1, N_r) (commit only) */
   TREEWY_STATUS_BAD_SLOT = 8,       /* state_slot[r] outside [0, num_slots) */
-  TREEWY_STATUS_TIMEOUT = 16        /* an internal wait gave up after ~1 s; that
+  TREEWY_STATUS_TIMEOUT = 16,       /* an internal wait gave up after ~1 s; that
                                        (request, head) was skipped */
+  TREEWY_STATUS_COMMIT_REFUSED = 32 /* treewy_commit_verify only: the previous
+                                       round's commit of this request was refused
+                                       (its state is unchanged); the bits beside
+                                       it say why */
 };
 
 /* Element type of q, k and v. */
@@ -188,12 +192,18 @@ treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted,
  * with no node in `next` still gets its commit.  prev and next must have the
  * same R, H, dk, dv, state pool pointer, num_slots, state_slot pointer and
  * TREEWY_FLAG_STATE_BF16.
- * Errors in the previous round's tree or accepted index set status bits in
- * next->status and leave the request's state untouched; on the tensor-core
- * path (dk = dv = 128, bf16 q/k/v) the request is then skipped entirely (its
- * outputs untouched).  Other shapes run the two kernels back to back, and
- * there a request whose commit was refused is still verified, from its
- * unchanged state.
+ * Errors, as for the two calls made one after the other, with every status
+ * bit going to next->status:
+ *   - an error in the previous round (its tree, node range or accepted index)
+ *     refuses that request's commit: its state is left unchanged, the bits of
+ *     the reason are set together with TREEWY_STATUS_COMMIT_REFUSED, and `next`
+ *     is still verified, from the unchanged state;
+ *   - an error in `next` (its tree or node range) skips that request's
+ *     verification (outputs untouched) but not its commit: S_a is written;
+ *   - a state slot outside the pool refuses both (TREEWY_STATUS_BAD_SLOT |
+ *     TREEWY_STATUS_COMMIT_REFUSED when a node was accepted).
+ * So S_a was written for request r exactly when prev_accepted[r] >= 0 and
+ * TREEWY_STATUS_COMMIT_REFUSED is clear in next->status[r].
  */
 treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev_accepted,
                                    const treewy_batch* next, cudaStream_t stream);

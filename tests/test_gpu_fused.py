@@ -118,7 +118,22 @@ def test_fused_matches_separate_calls(cuda_lib):
     assert do <= 1e-3 * tnb.o.abs().max().item(), do
 
 
-def test_fused_bad_previous_round_skips_request(cuda_lib):
+def check_next_from_unchanged(nxt, tn, S_before, r):
+    """Request r's next round verified from its unchanged state (refused commit)."""
+    nn = nxt.node_offset.cpu().numpy()
+    lo, hi = int(nn[r]), int(nn[r + 1])
+    ref = orc.verify_request(np32(S_before[int(nxt.state_slot[r])]), nxt.parent[lo:hi].cpu().numpy(),
+                             np32(nxt.q[lo:hi]), np32(nxt.k[lo:hi]), np32(nxt.v[lo:hi]),
+                             np32(nxt.alpha[lo:hi]), np32(nxt.beta[lo:hi]))
+    o_err = float(np.abs(np32(tn.o[lo:hi]) - ref.o).max())
+    assert o_err <= 2e-3 * float(np.abs(ref.o).max()), o_err
+
+
+def test_fused_bad_previous_round_refuses_commit_only(cuda_lib):
+    """Tensor-core path: an accepted index outside the previous tree refuses
+    that request's commit (state unchanged, COMMIT_REFUSED beside the reason)
+    and the request is verified from its unchanged state, as the separate
+    calls would do."""
     rng = np.random.default_rng(5)
     prev_trees = [random_tree(rng, 10), random_tree(rng, 12), random_tree(rng, 8)]
     next_trees = [random_tree(rng, 9), random_tree(rng, 11), random_tree(rng, 7)]
@@ -128,17 +143,59 @@ def test_fused_bad_previous_round_skips_request(cuda_lib):
     torch.cuda.synchronize()
     S_before = prev.state.clone()
     tn = binding.TreeVerifier(nxt)
-    tn.o.fill_(float("nan"))
     binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
     torch.cuda.synchronize()
     st = tn.status.cpu().tolist()
     assert st[0] == 0 and st[2] == 0
-    assert st[1] & binding.STATUS_BAD_ACCEPTED
+    assert st[1] == binding.STATUS_BAD_ACCEPTED | binding.STATUS_COMMIT_REFUSED, st
     s1 = int(prev.state_slot[1])
     assert torch.equal(prev.state[s1], S_before[s1])
-    node = nxt.node_offset.cpu().tolist()
-    assert torch.isnan(tn.o[node[1]:node[2]]).all()
     check(prev, nxt, tn, S_before.cpu(), [0, 2])
+    check_next_from_unchanged(nxt, tn, S_before.cpu(), 1)
+
+
+@pytest.mark.parametrize("dk,dv,qkv", [(128, 128, "bf16"), (128, 128, "f32"), (64, 48, "bf16")])
+def test_fused_bad_next_tree_still_commits(cuda_lib, dk, dv, qkv):
+    """An error in the next round's tree skips that request's verification
+    but not the previous round's commit: a tree above the batch's capacity,
+    a parent index out of range and a node range past T each leave S_a
+    written (no COMMIT_REFUSED) and the request's outputs untouched, on the
+    tensor-core kernel and on the fallback shapes."""
+    rng = np.random.default_rng(dk + dv)
+    prev_trees = [random_tree(rng, n) for n in (10, 14, 9, 12)]
+    next_trees = [random_tree(rng, n) for n in (6, 40, 9, 7)]
+    next_trees[2] = next_trees[2].copy()
+    next_trees[2][5] = 7                      # parent after the node
+    prev, nxt = rounds(prev_trees, next_trees, [4, 13, 8, 11], H=3, dk=dk, dv=dv, qkv=qkv)
+    nxt.max_nodes = 32                        # request 1 (40 nodes) exceeds the capacity
+    T = int(nxt.node_offset[-1])
+    tp = binding.TreeVerifier(prev)
+    tp.verify()
+    torch.cuda.synchronize()
+    S0_pool = prev.state.cpu()
+    tn = binding.TreeVerifier(nxt, max_nodes=32)
+    tn.o.fill_(float("nan"))
+    # request 3's node range runs past the rows the batch declares
+    tn.batch.T = T - 2
+    binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
+    torch.cuda.synchronize()
+    st = tn.status.cpu().tolist()
+    assert st[0] == 0, st
+    assert st[1] == binding.STATUS_TOO_MANY_NODES, st
+    assert st[2] == binding.STATUS_BAD_TREE, st
+    assert st[3] == binding.STATUS_BAD_TREE, st
+    nn = nxt.node_offset.cpu().tolist()
+    for r in (1, 2, 3):
+        assert torch.isnan(tn.o[nn[r]:min(nn[r + 1], T)]).all(), r
+    # every request's commit happened
+    s_err = s_max = 0.0
+    for r in range(4):
+        Sa, _, _ = oracle_two_rounds(prev, nxt, S0_pool, r)
+        S_gpu = np32(prev.state[int(prev.state_slot[r])])
+        s_err = max(s_err, float(np.abs(S_gpu - Sa).max()))
+        s_max = max(s_max, float(np.abs(Sa).max()))
+    assert s_err <= 1e-3 * s_max, (s_err, s_max)
+    check(prev, nxt, tn, S0_pool, [0])
 
 
 @pytest.mark.parametrize("dk,dv,qkv", [(128, 128, "f32"), (64, 48, "bf16")])
@@ -184,8 +241,9 @@ def test_fused_fallback_bad_previous_round(cuda_lib):
     binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
     torch.cuda.synchronize()
     st = tn.status.cpu().tolist()
-    assert st[0] == 0 and st[1] & binding.STATUS_BAD_ACCEPTED
+    assert st[0] == 0 and st[1] == binding.STATUS_BAD_ACCEPTED | binding.STATUS_COMMIT_REFUSED, st
     assert not tp.status.any()
     s1 = int(prev.state_slot[1])
     assert torch.equal(prev.state[s1], S_before[s1])
     check(prev, nxt, tn, S_before.cpu(), [0])
+    check_next_from_unchanged(nxt, tn, S_before.cpu(), 1)
