@@ -46,8 +46,8 @@ UNIT = "nodes/s"
 CONFIG_NAME = "wide"
 LAYERS = 30
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_tc_wide_traffic.json")
-KERNEL_SOURCES = ["gdn_speculative_tree_gb300/csrc/verify_tc.cuh",
-                  "gdn_speculative_tree_gb300/csrc/verify_tc.cu",
+KERNEL_SOURCES = ["gdn_speculative_tree_gb300/csrc/verify_pipe.cuh",
+                  "gdn_speculative_tree_gb300/csrc/verify_pipe.cu",
                   "gdn_speculative_tree_gb300/csrc/treewy_device.cuh",
                   "gdn_speculative_tree_gb300/csrc/treewy_api.cu",
                   "gdn_speculative_tree_gb300/csrc/treewy_internal.h"]
@@ -218,75 +218,78 @@ def sum_over_ranks(x: float, world: int) -> float:
 
 # ---------------------------------------------------------------- CPU oracle leg
 
-def oracle_sample(n_requests: int, seed_layer: int = 0):
-    """Time the CPU oracle on the first n_requests of one layer (all heads).
+def oracle_jobs(cfg, n_requests: int, layers: int):
+    """Oracle jobs for the first n_requests of every layer (CPU tensors).
 
-    Returns (nodes in the sample, wall seconds, process CPU seconds over all
-    threads)."""
-    from oracle import gdn_tree_oracle as orc
-    cfg = wl.CONFIGS[CONFIG_NAME]
-    w = wl.generate(cfg, R=n_requests, layer=seed_layer)
-    node = w.node_offset.numpy()
-    q, k, v = w.q.float().numpy(), w.k.float().numpy(), w.v.float().numpy()
-    alpha, beta, parent = w.alpha.numpy(), w.beta.numpy(), w.parent.numpy()
-    acc = w.accepted.numpy()
+    Trees depend only on the workload's seed and the request count, so every
+    layer of the sample has the same trees; returns (jobs, draft nodes of the
+    sample)."""
+    from oracle import pool as opool
+    jobs, nodes = [], 0
+    for l in range(layers):
+        w = wl.generate(cfg, R=n_requests, layer=l)
+        f32 = lambda x: x.float().numpy()  # noqa: E731
+        jobs += opool.jobs_from_arrays(w.node_offset.numpy(), w.parent.numpy(), f32(w.q), f32(w.k),
+                                       f32(w.v), w.alpha.numpy(), w.beta.numpy(), w.state.numpy(),
+                                       w.state_slot.numpy(), w.accepted.numpy(), range(w.R))
+        nodes = int(w.node_offset[-1])
+    return jobs, nodes
+
+
+def oracle_sample(pool, cfg, n_requests: int, layers: int):
+    """Time the oracle (verify + commit of every request in every layer of
+    the sample) on the pool's workers.  Returns (nodes, wall seconds)."""
+    jobs, nodes = oracle_jobs(cfg, n_requests, layers)
     t0 = time.perf_counter()
-    c0 = time.process_time()
-    for r in range(w.R):
-        lo, hi = int(node[r]), int(node[r + 1])
-        S0 = w.state[int(w.state_slot[r])].numpy()
-        res = orc.verify_request(S0, parent[lo:hi], q[lo:hi], k[lo:hi], v[lo:hi], alpha[lo:hi],
-                                 beta[lo:hi])
-        orc.commit_request(S0, res, int(acc[r]))
-    dt = time.perf_counter() - t0
-    return int(node[-1]), dt, time.process_time() - c0
+    pool.map(jobs, keep=False)
+    return nodes, time.perf_counter() - t0
 
 
-def cores_used(wall: float, cpu: float) -> int:
-    """Threads the sample kept busy on average (CPU time over wall time)."""
-    return max(1, int(round(cpu / wall))) if wall > 0 else 1
+def cpu_baseline(pool, n_requests: int):
+    cfg = wl.CONFIGS[CONFIG_NAME]
+    nodes, dt = oracle_sample(pool, cfg, n_requests, LAYERS)
+    return {"value": nodes / dt, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, first {n_requests} requests x {cfg.H} heads of the "
+                      f"workload through all {LAYERS} layers ({nodes} nodes, {dt:.2f} s wall), "
+                      f"one request-layer per job on {pool.workers} worker processes"}
 
 
-def cpu_baseline(n_requests: int = 160):
-    nodes, dt, cpu = oracle_sample(n_requests)
-    # a full step needs every node through all 30 layers
-    value = nodes / (dt * LAYERS)
-    return {"value": value, "unit": UNIT, "cores": cores_used(dt, cpu), "kind": "oracle",
-            "sample": f"fp64 numpy oracle, first {n_requests} requests x 32 heads of one layer "
-                      f"({nodes} nodes, {dt:.1f} s wall, {cpu:.1f} s CPU), scaled to {LAYERS} layers"}
-
-
-def run_reference(args, world, rank):
+def run_reference(args, world, rank, pool):
+    """The oracle as the reference arm: every step verifies and commits a
+    bounded sample of the workload (its first requests, all heads) through
+    all 30 layers on every host core, timed as it runs."""
     if rank != 0:
         return
-    n_req = 8
+    cfg = wl.CONFIGS[CONFIG_NAME]
+    n_req = args.ref_requests
+    jobs, nodes = oracle_jobs(cfg, n_req, LAYERS)
     for _ in range(args.warmup):
-        oracle_sample(n_req)
-    times, cpus, nodes = [], [], 0
+        pool.map(jobs, keep=False)
+    times = []
     for _ in range(args.steps):
-        nodes, dt, cpu = oracle_sample(n_req)
-        times.append(dt)
-        cpus.append(cpu)
+        t0 = time.perf_counter()
+        pool.map(jobs, keep=False)
+        times.append(time.perf_counter() - t0)
     t = sum(times) / len(times)
-    cores = cores_used(sum(times), sum(cpus))
-    value = nodes / (t * LAYERS)
+    value = nodes / t
+    sample = (f"first {n_req} requests x {cfg.H} heads of the workload ({nodes} nodes) through all "
+              f"{LAYERS} layers per step, one request-layer per job on {pool.workers} worker processes")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1000.0 * LAYERS,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1000.0,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": "wide ragged trees (256 req x 32 heads, N 16..64, depth<=8, "
                                    "30 GDN layers); each timed step is a bounded sample",
-                       "sample_requests": n_req},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"first {n_req} requests x 32 heads of one layer per step "
-                                       f"({nodes} nodes), scaled to {LAYERS} layers"},
+                       "sample_requests": n_req, "layers": LAYERS},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ---------------------------------------------------------------- GPU leg
 
-def run_ours(args, world, rank, local):
+def run_ours(args, world, rank, local, pool=None):
     from gdn_speculative_tree_gb300 import binding
     from gdn_speculative_tree_gb300 import build as _build
 
@@ -377,7 +380,7 @@ def run_ours(args, world, rank, local):
     fused = run_fused(args, work, stream, world, vb, cb, plen, H, peak)
 
     storeall = run_storeall(work[0], stream) if rank == 0 and not args.no_storeall else None
-    cpu = cpu_baseline(args.cpu_requests) if rank == 0 and args.cpu_requests > 0 else None
+    cpu = cpu_baseline(pool, args.cpu_requests) if pool is not None else None
 
     if rank != 0:
         return
@@ -392,7 +395,7 @@ def run_ours(args, world, rank, local):
                    "l2": "no flush: each layer's inputs (~1.1 GB) exceed the 129 MB L2"},
         "roofline": {"bound": "hbm", "achieved": v_gbs, "peak": peak, "unit": "GB/s",
                      "frac": v_gbs / peak, "traffic": traffic,
-                     "kernel": "verify_tc_kernel<64>", "algorithmic_bytes_per_launch": vb,
+                     "kernel": "verify_pipe_kernel<64, false, false>", "algorithmic_bytes_per_launch": vb,
                      "avg_launch_ms": v_avg, "peak_kind": f"{peak_kind} hbm_gbs"},
         "commit": {"achieved_gbs": c_gbs, "frac": c_gbs / peak, "avg_launch_ms": c_avg,
                    "algorithmic_bytes_per_launch": cb},
@@ -653,51 +656,56 @@ def study_fixed64(args, local):
 
 
 def study_graph(args, local):
-    """Launch overhead on the chain workload (64 requests x 32 heads, chains of
-    4): 30 layers of verify + commit issued eagerly vs replayed as one CUDA
-    graph captured from the same calls."""
+    """Launch overhead of 30 layers of verify + commit issued eagerly against
+    the same calls captured once as a CUDA graph and replayed, on the chain
+    workload (64 requests x 32 heads, chains of 4) and on the wide ragged
+    tree workload (256 requests x 32 heads, N 16..64): the pages say the tree
+    path could not be captured in their engine."""
     from gdn_speculative_tree_gb300 import binding
     dev = torch.device("cuda", local)
-    cfg = wl.CONFIGS["chain"]
     layers = args.layers
-    work = [binding.TreeVerifier(wl.generate(cfg, layer=l, device=dev)) for l in range(layers)]
-    stream = torch.cuda.Stream(device=dev)
-    nodes = int(work[0].wl.node_offset[-1])
+    for name in ("chain", "wide"):
+        cfg = wl.CONFIGS[name]
+        work = [binding.TreeVerifier(wl.generate(cfg, layer=l, device=dev)) for l in range(layers)]
+        stream = torch.cuda.Stream(device=dev)
+        nodes = int(work[0].wl.node_offset[-1])
 
-    def step():
-        for tv in work:
-            tv.verify(stream)
-        for tv in work:
-            tv.commit(None, stream)
+        def step():
+            for tv in work:
+                tv.verify(stream)
+            for tv in work:
+                tv.commit(None, stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    torch.cuda.synchronize()
-    reps = max(args.steps, 20)
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        eager_ms = _median_ms(step, stream, reps)
-    host_eager = (time.perf_counter() - t0) / reps * 1e3
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        step()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            g.replay()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                step()
         torch.cuda.synchronize()
-        graph_ms = _median_ms(g.replay, stream, reps)
-    for tv in work:
-        if tv.status.any().item():
-            raise SystemExit("device status bits set in the graph study")
-    print(json.dumps({"study": "CUDA-graph capture of batched tree verify+commit",
-                      "workload": f"chain of 4, {cfg.R} requests x {cfg.H} heads, {layers} layers",
-                      "launches_per_step": 2 * layers, "eager_ms_per_step": eager_ms,
-                      "graph_ms_per_step": graph_ms, "eager_host_ms_per_step": host_eager,
-                      "eager_nodes_per_s": nodes * 1e3 / eager_ms,
-                      "graph_nodes_per_s": nodes * 1e3 / graph_ms,
-                      "graph_speedup": eager_ms / graph_ms}), flush=True)
+        reps = max(args.steps, 20)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            eager_ms = _median_ms(step, stream, reps)
+        host_eager = (time.perf_counter() - t0) / reps * 1e3
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                g.replay()
+            torch.cuda.synchronize()
+            graph_ms = _median_ms(g.replay, stream, reps)
+        for tv in work:
+            if tv.status.any().item():
+                raise SystemExit("device status bits set in the graph study")
+        print(json.dumps({"study": "CUDA-graph capture of batched tree verify+commit",
+                          "workload": f"{name}: {cfg.R} requests x {cfg.H} heads, {layers} layers",
+                          "launches_per_step": 2 * layers, "eager_ms_per_step": eager_ms,
+                          "graph_ms_per_step": graph_ms, "eager_host_ms_per_step": host_eager,
+                          "eager_nodes_per_s": nodes * 1e3 / eager_ms,
+                          "graph_nodes_per_s": nodes * 1e3 / graph_ms,
+                          "graph_speedup": eager_ms / graph_ms}), flush=True)
+        del work, g
+        torch.cuda.empty_cache()
 
 
 def study_bf16state(args, local):
@@ -760,6 +768,136 @@ def study_bf16state(args, local):
         flush=True)
 
 
+def storeall_chunked(w, o, stream, reps=3, max_bytes=34e9):
+    """The storeall comparator over a whole batch, verified and rolled back in
+    request chunks whose snapshots fit in max_bytes; returns summed median
+    times of the chunks and the snapshot bytes (the state is restored after
+    every rollback, untimed)."""
+    from gdn_speculative_tree_gb300 import binding
+    node = w.node_offset.cpu().numpy().astype(np.int64)
+    per_node = w.H * w.dv * w.dk * 4
+    chunks, r0 = [], 0
+    while r0 < w.R:
+        r1 = r0 + 1
+        while r1 < w.R and (node[r1 + 1] - node[r0]) * per_node <= max_bytes:
+            r1 += 1
+        chunks.append((r0, r1))
+        r0 = r1
+    most = max(int(node[b] - node[a]) for a, b in chunks)
+    snaps = torch.empty(most, w.H, w.dv, w.dk, device=w.q.device, dtype=torch.float32)
+    S_save = w.state.clone()
+    status = torch.zeros(w.R, device=w.q.device, dtype=torch.int32)
+    v_tot = c_tot = 0.0
+    for a, b in chunks:
+        bt = binding.make_batch(node_offset=w.node_offset[a:b + 1], parent=w.parent, q=w.q, k=w.k,
+                                v=w.v, alpha=w.alpha, beta=w.beta, state=w.state,
+                                state_slot=w.state_slot[a:b], o=o, U=o, status=status[a:b],
+                                max_nodes=w.max_nodes, T=w.T)
+        vt, ct = [], []
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for i in range(reps + 1):
+            ev[0].record(stream)
+            binding.treewy_storeall_verify(bt, snaps, stream)
+            ev[1].record(stream)
+            binding.treewy_storeall_commit(bt, snaps, w.accepted[a:b], stream)
+            ev[2].record(stream)
+            ev[2].synchronize()
+            w.state.copy_(S_save)
+            if i:
+                vt.append(ev[0].elapsed_time(ev[1]))
+                ct.append(ev[1].elapsed_time(ev[2]))
+        v_tot += statistics.median(vt)
+        c_tot += statistics.median(ct)
+    torch.cuda.synchronize()
+    if status.any().item():
+        raise SystemExit("device status bits set in the storeall comparator")
+    del snaps
+    torch.cuda.empty_cache()
+    return v_tot, c_tot, int(node[-1]) * per_node, len(chunks)
+
+
+def study_configs(args, local, pool):
+    """Every workload of the benchmark family, one JSON line each: verify,
+    commit and the fused commit-into-verify per launch (median of 20 launches,
+    L2 flushed before each, the state restored untimed before each commit),
+    their algorithmic bytes, GB/s and fraction of the measured HBM peak, the
+    node counters, the storeall comparator on the same inputs (in request
+    chunks) and the oracle on a bounded sample on every host core."""
+    from gdn_speculative_tree_gb300 import binding
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = read_peaks()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 2x the 129 MB L2
+    flush = flush_buf.zero_
+    g = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
+    specs = [("chain", wl.CONFIGS["chain"], 32),
+             ("binary", wl.CONFIGS["binary"], 16),
+             ("wide", wl.CONFIGS["wide"], 16),
+             ("wide_fixed64", wl.CONFIGS["wide"].with_(tree="random64_d8"), 8),
+             ("stress", wl.CONFIGS["stress"], 4)]
+    only = set(args.configs.split(",")) if args.configs else None
+    for name, cfg, n_oracle in specs:
+        if only is not None and name not in only:
+            continue
+        w = wl.generate(cfg, device=dev)
+        tv = binding.TreeVerifier(w)
+        S0 = w.state.clone()
+        Ns, plen = tree_stats(w.trees, w.accepted.cpu().numpy())
+        H = w.H
+        vb, cb = verify_bytes(Ns, H), commit_bytes(plen, H)
+        fb = vb + cb - int(H * 65536 * int((plen > 0).sum()))
+        nodes = int(Ns.sum())
+        for _ in range(args.warmup):
+            tv.verify(stream)
+
+        def restore_flush():
+            w.state.copy_(S0)
+            flush()
+
+        v_ms = _median_ms(lambda: tv.verify(stream), stream, 20, before=flush)
+        c_ms = _median_ms(lambda: tv.commit(None, stream), stream, 20, before=restore_flush)
+        f_ms = _median_ms(lambda: binding.treewy_commit_verify(tv.batch, w.accepted, tv.batch, stream),
+                          stream, 20, before=restore_flush)
+        w.state.copy_(S0)
+        torch.cuda.synchronize()
+        if tv.status.any().item():
+            raise SystemExit(f"device status bits set in config {name}")
+        line = {"study": "configs", "config": name, "R": w.R, "H": H, "nodes_per_layer": nodes,
+                "N_mean": float(Ns.mean()), "N_max": int(Ns.max()),
+                "peak_gbs": peak, "peak_kind": f"{peak_kind} hbm_gbs",
+                "verify": {"ms": v_ms, "algorithmic_bytes": vb, "gbs": g(vb, v_ms),
+                           "frac": g(vb, v_ms) / peak,
+                           "tree_nodes_per_s": nodes / (v_ms * 1e-3),
+                           "head_node_verifies_per_s": nodes * H / (v_ms * 1e-3),
+                           "head_verifies_per_s": w.R * H / (v_ms * 1e-3)},
+                "commit": {"ms": c_ms, "algorithmic_bytes": cb, "gbs": g(cb, c_ms),
+                           "frac": g(cb, c_ms) / peak,
+                           "committing_heads": int((plen > 0).sum()) * H},
+                "fused": {"ms": f_ms, "algorithmic_bytes": fb, "gbs": g(fb, f_ms),
+                          "frac": g(fb, f_ms) / peak,
+                          "vs_separate": (v_ms + c_ms) / f_ms},
+                "l2": "flushed (256 MB written) before every timed launch"}
+        if not args.no_storeall:
+            o = torch.empty_like(tv.o)
+            sv, sc, sbytes, nch = storeall_chunked(w, o, stream)
+            sv_bytes = sbytes + vb - nodes * H * 516
+            line["storeall"] = {"verify_ms": sv, "commit_ms": sc, "snapshot_bytes": sbytes,
+                                "verify_bytes": sv_bytes, "verify_gbs": g(sv_bytes, sv),
+                                "verify_frac": g(sv_bytes, sv) / peak, "chunks": nch,
+                                "treewy_verify_speedup": sv / v_ms,
+                                "state_blocks_per_request": "N+1 (treewy: 1)"}
+            del o
+        if pool is not None:
+            cnodes, dt = oracle_sample(pool, cfg, n_oracle, 1)
+            line["oracle"] = {"requests": n_oracle, "nodes": cnodes, "wall_s": dt,
+                              "nodes_per_s": cnodes / dt, "cores": pool.workers,
+                              "gpu_speedup_verify_commit": (cnodes / dt) ** -1 * nodes /
+                              ((v_ms + c_ms) * 1e-3)}
+        print(json.dumps(line), flush=True)
+        del tv, w, S0
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -767,13 +905,29 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=LAYERS)
-    ap.add_argument("--cpu-requests", type=int, default=160)
+    ap.add_argument("--cpu-requests", type=int, default=16,
+                    help="requests of the oracle's CPU-baseline sample (0: skip it)")
+    ap.add_argument("--ref-requests", type=int, default=8,
+                    help="requests per step of the reference arm's sample")
     ap.add_argument("--no-storeall", action="store_true")
-    ap.add_argument("--study", choices=["widths", "graph", "bf16state", "fixed64"],
-                    help="print one study line instead of the benchmark line (1 GPU)")
+    ap.add_argument("--configs", default="",
+                    help="--study configs: comma-separated subset of chain,binary,wide,"
+                         "wide_fixed64,stress")
+    ap.add_argument("--study", choices=["widths", "graph", "bf16state", "fixed64", "configs"],
+                    help="print study lines instead of the benchmark line (1 GPU)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    # The oracle's worker pool is forked here, before this process makes any
+    # GPU call (its workers only run numpy).
+    pool = None
+    wants_pool = (args.impl == "reference" or args.study == "configs" or
+                  (args.study is None and args.cpu_requests > 0))
+    if wants_pool and rank == 0 and world == 1:
+        from oracle.pool import OraclePool
+        pool = OraclePool(method="fork")
     world, rank, local = dist_setup(args.gpus)
     try:
         if args.study is not None:
@@ -783,13 +937,21 @@ def main():
                 torch.cuda.set_device(local)
                 _build.build()
                 binding.load()
-                {"widths": study_widths, "graph": study_graph, "bf16state": study_bf16state,
-                 "fixed64": study_fixed64}[args.study](args, local)
+                if args.study == "configs":
+                    study_configs(args, local, pool)
+                else:
+                    {"widths": study_widths, "graph": study_graph, "bf16state": study_bf16state,
+                     "fixed64": study_fixed64}[args.study](args, local)
         elif args.impl == "reference":
-            run_reference(args, world, rank)
+            if rank == 0 and pool is None:
+                from oracle.pool import OraclePool
+                pool = OraclePool(method="spawn")
+            run_reference(args, world, rank, pool)
         else:
-            run_ours(args, world, rank, local)
+            run_ours(args, world, rank, local, pool)
     finally:
+        if pool is not None:
+            pool.close()
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()

@@ -22,3 +22,12 @@ def cuda_lib():
     from gdn_speculative_tree_gb300 import binding
     binding.load()
     return binding
+
+
+@pytest.fixture(scope="session")
+def oracle_pool():
+    """The oracle on every host core (worker processes started with spawn,
+    which is safe after the GPU has been used)."""
+    from oracle.pool import OraclePool
+    with OraclePool() as pool:
+        yield pool

@@ -57,22 +57,42 @@ def oracle_request(wl, r, S0_pool):
     return lo, hi, S0, res
 
 
-def compare(wl, run: CudaRun, requests, accepted=None, check_commit=True):
-    """Error ratios of o, U, gamma and the committed state over `requests`."""
+def _oracle_results(wl, run, requests, acc, pool):
+    """(lo, hi, S0, o, U, gamma, S_commit) per request: one by one here, or as
+    jobs of an oracle process pool."""
+    node = wl.node_offset.cpu().numpy()
+    slot = wl.state_slot.cpu().numpy()
+    requests = list(requests)
+    if pool is None:
+        for r in requests:
+            lo, hi, S0, ref = oracle_request(wl, r, run.S0_pool)
+            yield lo, hi, S0, ref.o, ref.U, ref.gamma, orc.commit_request(S0, ref, int(acc[r]))
+        return
+    from oracle import pool as opool
+    jobs = opool.jobs_from_arrays(node, wl.parent.cpu().numpy(), np32(wl.q), np32(wl.k), np32(wl.v),
+                                  np32(wl.alpha), np32(wl.beta), np32(run.S0_pool), slot, acc,
+                                  requests)
+    for r, (o, U, g, S_c) in zip(requests, pool.map(jobs)):
+        lo, hi = int(node[r]), int(node[r + 1])
+        yield lo, hi, None, o, U, g, S_c
+
+
+def compare(wl, run: CudaRun, requests, accepted=None, check_commit=True, pool=None):
+    """Error ratios of o, U, gamma and the committed state over `requests`
+    (``pool``: an oracle.pool.OraclePool that runs the requests in parallel)."""
     acc = (wl.accepted if accepted is None else accepted).cpu().numpy()
     slot = wl.state_slot.cpu().numpy()
     o_err = o_max = u_err = u_max = g_err = s_err = s_max = 0.0
-    for r in requests:
-        lo, hi, S0, ref = oracle_request(wl, r, run.S0_pool)
-        o_err = max(o_err, float(np.abs(run.o[lo:hi] - ref.o).max(initial=0)))
-        o_max = max(o_max, float(np.abs(ref.o).max(initial=0)))
-        u_err = max(u_err, float(np.abs(run.U[lo:hi] - ref.U).max(initial=0)))
-        u_max = max(u_max, float(np.abs(ref.U).max(initial=0)))
+    for r, (lo, hi, _S0, ref_o, ref_U, ref_g, S_ref) in zip(
+            list(requests), _oracle_results(wl, run, requests, acc, pool)):
+        o_err = max(o_err, float(np.abs(run.o[lo:hi] - ref_o).max(initial=0)))
+        o_max = max(o_max, float(np.abs(ref_o).max(initial=0)))
+        u_err = max(u_err, float(np.abs(run.U[lo:hi] - ref_U).max(initial=0)))
+        u_max = max(u_max, float(np.abs(ref_U).max(initial=0)))
         if hi > lo:
-            g_err = max(g_err, float((np.abs(run.gamma[lo:hi] - ref.gamma) /
-                                      np.maximum(ref.gamma, FLT_MIN)).max()))
+            g_err = max(g_err, float((np.abs(run.gamma[lo:hi] - ref_g) /
+                                      np.maximum(ref_g, FLT_MIN)).max()))
         if check_commit:
-            S_ref = orc.commit_request(S0, ref, int(acc[r]))
             S_gpu = np32(run.S_after[int(slot[r])])
             s_err = max(s_err, float(np.abs(S_gpu - S_ref).max()))
             s_max = max(s_max, float(np.abs(S_ref).max()))
