@@ -46,8 +46,8 @@ UNIT = "nodes/s"
 CONFIG_NAME = "wide"
 LAYERS = 30
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_tc_wide_traffic.json")
-KERNEL_SOURCES = ["gdn_speculative_tree_gb300/csrc/verify_pipe.cuh",
-                  "gdn_speculative_tree_gb300/csrc/verify_pipe.cu",
+KERNEL_SOURCES = ["gdn_speculative_tree_gb300/csrc/verify_tc.cuh",
+                  "gdn_speculative_tree_gb300/csrc/verify_tc.cu",
                   "gdn_speculative_tree_gb300/csrc/treewy_device.cuh",
                   "gdn_speculative_tree_gb300/csrc/treewy_api.cu",
                   "gdn_speculative_tree_gb300/csrc/treewy_internal.h"]
@@ -395,7 +395,7 @@ def run_ours(args, world, rank, local, pool=None):
                    "l2": "no flush: each layer's inputs (~1.1 GB) exceed the 129 MB L2"},
         "roofline": {"bound": "hbm", "achieved": v_gbs, "peak": peak, "unit": "GB/s",
                      "frac": v_gbs / peak, "traffic": traffic,
-                     "kernel": "verify_pipe_kernel<64, false, false>", "algorithmic_bytes_per_launch": vb,
+                     "kernel": "verify_tc_kernel<64>", "algorithmic_bytes_per_launch": vb,
                      "avg_launch_ms": v_avg, "peak_kind": f"{peak_kind} hbm_gbs"},
         "commit": {"achieved_gbs": c_gbs, "frac": c_gbs / peak, "avg_launch_ms": c_avg,
                    "algorithmic_bytes_per_launch": cb},
