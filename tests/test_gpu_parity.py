@@ -235,6 +235,28 @@ def test_storeall_matches_oracle(cuda_lib, name, R, chunks):
         assert np.abs(S_gpu - S_ref).max() <= 1e-3 * np.abs(S_ref).max()
 
 
+@pytest.mark.parametrize("qkv", ["bf16", "f32"])
+def test_storeall_tree_shapes(cuda_lib, qkv):
+    """The 128 x 128 comparator walks each tree in DFS pre-order and reloads a
+    parent's snapshot only after a branch point: a 64-deep chain, 64 nodes
+    off S0, the (3,3,3) width tree, 8 branches of 8, random trees and a
+    single node, against the oracle's per-node states."""
+    rng = np.random.default_rng(29)
+    trees = [wl.chain_parents(64), np.full(64, -1, np.int32), wl.width_tree_parents((3, 3, 3)),
+             wl.branches_parents(8, 8), np.zeros(1, np.int32) - 1] + random_trees(rng, [17, 40, 64])
+    acc = [int(rng.integers(-1, len(t))) for t in trees]
+    w = custom(trees, acc, H=2, qkv=qkv, max_nodes=64)
+    snaps, o, status, S0 = run_storeall(w, 2)
+    assert not status.any()
+    for r in range(w.R):
+        lo, hi, S0r, ref = oracle_request(w, r, S0)
+        scale_s = np.abs(ref.states).max()
+        assert np.abs(np32(snaps[lo:hi]) - ref.states).max() <= 1e-3 * scale_s, r
+        assert np.abs(np32(o[lo:hi]) - ref.o).max() <= 2e-3 * np.abs(ref.o).max(), r
+        S_ref = orc.commit_request(S0r, ref, int(w.accepted[r]))
+        assert np.abs(np32(w.state[int(w.state_slot[r])]) - S_ref).max() <= 1e-3 * np.abs(S_ref).max()
+
+
 def test_storeall_and_treewy_commit_agree(cuda_lib):
     w1 = cpu_then_cuda("binary", R=10)
     w2 = cpu_then_cuda("binary", R=10)
