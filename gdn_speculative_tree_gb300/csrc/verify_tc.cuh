@@ -46,8 +46,6 @@ constexpr int kThreads = 256;
 constexpr int kDim = 128;
 constexpr uint32_t kS0ChunkBytes = 128u * 128u;     // 128 rows x 128 bytes (32 fp32 / 64 bf16)
 constexpr uint32_t kS0Bytes = 4u * kS0ChunkBytes;   // 64 KB: S0, then W^T and [T;B]
-constexpr uint32_t kKQChunkBytes = 128u * 128u;     // 128 rows x 64 bf16
-constexpr uint32_t kKQBytes = 2u * kKQChunkBytes;   // 32 KB: K,Q, then coefficient lists
 // Operands of the second MMA, placed in the S0 region once the first is done:
 // each is 128 rows x 128 bytes (K-major, 128B swizzle, K <= 64 bf16).
 constexpr uint32_t kWhiOff = 0, kWloOff = 16384, kThiOff = 32768, kTloOff = 49152;
@@ -62,18 +60,30 @@ struct TcCfg {
   static constexpr uint32_t kListBytes = 4u * kE;
   static constexpr uint32_t kPidxBytes = (kE + 15u) & ~15u;
   static constexpr uint32_t kR2Bytes = kPidxBytes + kListBytes;  // pidx + (pc | B scratch)
-  static constexpr uint32_t kDynSmem = kS0Bytes + kKQBytes + kR2Bytes + 1024u;
-  static_assert(3u * kListBytes <= kKQBytes, "A, M and T-scratch lists must fit the K/Q region");
+  // K/Q: two 64-column chunks of 128 rows (the Gram's M = 128 operand).  A
+  // 16-node tree uses 32 rows, so its chunks are 32 rows and the region sits
+  // before the S0 tile: the Gram's reads of rows 32..127 stay inside the
+  // CTA's shared memory (their products land in TMEM lanes that are never
+  // read), and the smaller footprint fits three CTAs per SM.
+  static constexpr uint32_t kKQRows = NPM == 16 ? 32u : 128u;
+  static constexpr uint32_t kKQChunk = kKQRows * 128u;
+  static constexpr uint32_t kKQ = 2u * kKQChunk;
+  static constexpr uint32_t kKQOff = NPM == 16 ? 0u : kS0Bytes;
+  static constexpr uint32_t kS0Off = NPM == 16 ? kKQ : 0u;
+  static constexpr uint32_t kR2Off = kS0Bytes + kKQ;
+  static constexpr uint32_t kDynSmem = kR2Off + kR2Bytes + 1024u;
+  static_assert(3u * kListBytes <= kKQ, "A, M and T-scratch lists must fit the K/Q region");
 };
 
-// Per-CTA tree data for one (request, head).
+// Per-CTA tree data for one (request, head), sized by the capacity bucket.
+template <int NPM>
 struct TreeTC {
-  int parent[kMaxNodes];
-  float alpha[kMaxNodes];
-  float gamma[kMaxNodes];
-  float2 bbg[kMaxNodes];                // (beta_n, beta_n * gamma_n)
-  int D[kMaxNodes];                     // path length root..n, n included
-  int off[kMaxNodes + 1];               // CSR offsets of the path lists
+  int parent[NPM];
+  float alpha[NPM];
+  float gamma[NPM];
+  float2 bbg[NPM];                      // (beta_n, beta_n * gamma_n)
+  int D[NPM];                           // path length root..n, n included
+  int off[NPM + 1];                     // CSR offsets of the path lists
   int tok0, N, slot;
   int flags;   // this round's request errors (node range, slot): verification skipped
   int cflags;  // fused commit refused: the previous round's errors | COMMIT_REFUSED
@@ -88,7 +98,8 @@ struct TreeTC {
 // formed as products of alpha along the path (no division); the first
 // kRegPath entries wait in registers for the CSR offsets.  Returns false
 // (uniformly over the 64 threads) when a parent index is out of range.
-__device__ __forceinline__ bool prepare_tree(TreeTC& ts, uint8_t* pidx, float* pc, int p,
+template <int NPM>
+__device__ __forceinline__ bool prepare_tree(TreeTC<NPM>& ts, uint8_t* pidx, float* pc, int p,
                                              float alpha, float beta) {
   const int t = threadIdx.x;
   const int N = ts.N;
@@ -138,9 +149,9 @@ __device__ __forceinline__ bool prepare_tree(TreeTC& ts, uint8_t* pidx, float* p
       if (t >= o) s += y;
     }
     const int excl = s - a0 - a1;
-    ts.off[i0] = excl;
-    ts.off[i1] = excl + a0;
-    if (t == 31) ts.off[kMaxNodes] = s;
+    if (i0 < NPM) ts.off[i0] = excl;
+    if (i1 < NPM) ts.off[i1] = excl + a0;
+    if (t == 31) ts.off[NPM] = s;
   }
   named_bar_sync<3, 64>();
   if (t < N) {
@@ -216,7 +227,8 @@ __device__ __forceinline__ void put_operand(unsigned char* hi, unsigned char* lo
 // p_a's strict-ancestor list at position q - a, and writes x_q (hi/lo bf16) at
 // column p_q of operand row `row`.  `scratch` holds x for paths longer than
 // kRegPath (registers otherwise).
-__device__ __forceinline__ void build_path_row(const TreeTC& ts, int n, int row,
+template <int NPM>
+__device__ __forceinline__ void build_path_row(const TreeTC<NPM>& ts, int n, int row,
                                                const uint8_t* pidx, const float* aco,
                                                const float* rhs, float* scratch,
                                                unsigned char* thi, unsigned char* tlo) {
@@ -278,7 +290,7 @@ struct PrevSmem<true> {
 // state it so the register allocation avoids spills, that one (0: no
 // minimum) was measured faster with the default allocation.
 template <int NPM, bool FUSED, bool SB>
-__global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
+__global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || FUSED || NPM < 64) ? 2 : 0))
     verify_tc_kernel(const __grid_constant__ CUtensorMap map_s0,
                      const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_q,
@@ -289,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   constexpr int kChunks = SB ? 2 : 4;      // S0 boxes of 16 KB
   constexpr int kChunkCols = SB ? 64 : 32;
   extern __shared__ unsigned char smem_raw[];
-  __shared__ TreeTC ts;
+  __shared__ TreeTC<NPM> ts;
   __shared__ PrevSmem<FUSED> pv;
   // 0-3: S0 chunks, 4: K/Q, 5: S0 [K;Q]^T done, 6: second MMA done, 7: Gram done
   __shared__ __align__(8) uint64_t bars[8];
@@ -300,9 +312,9 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
 
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
-  unsigned char* s0 = base;
-  unsigned char* kq = base + kS0Bytes;
-  uint8_t* pidx = base + kS0Bytes + kKQBytes;
+  unsigned char* s0 = base + C::kS0Off;
+  unsigned char* kq = base + C::kKQOff;
+  uint8_t* pidx = base + C::kR2Off;
   float* pc = reinterpret_cast<float*>(pidx + C::kPidxBytes);
   float* xB = pc;  // long-path B rows reuse the decay products once consumed
   float* aco = reinterpret_cast<float*>(kq);
@@ -451,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
       for (int i = t; i < 4 * per; i += 32) {
         const int c2 = (i >> 1) & 1, j = i >> 2, rb = 32 * j;
         const bool big = j < n32;
-        unsigned char* chunk = kq + c2 * kKQChunkBytes;
+        unsigned char* chunk = kq + c2 * C::kKQChunk;
         if (i & 1)
           tma_load_3d(chunk + (Np + rb) * 128, big ? &map_q32 : &map_q, &bars[4], 64 * c2, h,
                       ts.tok0 + rb);
@@ -735,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
         for (int c = 0; c < 2; ++c) {
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
-            const uint64_t bd = db + ((c * kKQChunkBytes + s * 32) >> 4);
+            const uint64_t bd = db + ((c * C::kKQChunk + s * 32) >> 4);
             const uint64_t a = da + ((c * kS0ChunkBytes + s * 32) >> 4);
             mma_bf16(tmem, a, bd, id1, (c | s) ? 1u : 0u);
           }
@@ -745,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
-            const uint64_t bd = db + (((c >> 1) * kKQChunkBytes + (c & 1) * 64 + s * 32) >> 4);
+            const uint64_t bd = db + (((c >> 1) * C::kKQChunk + (c & 1) * 64 + s * 32) >> 4);
             const uint64_t ahi = da + ((c * kS0ChunkBytes + s * 32) >> 4);
             const uint64_t alo = da + ((c * kS0ChunkBytes + 64 + s * 32) >> 4);
             mma_bf16(tmem, ahi, bd, id1, (c | s) ? 1u : 0u);
@@ -757,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
       const uint32_t id2 = idesc_bf16_f32(128, Np);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const uint64_t dsc = db + (((s >> 2) * kKQChunkBytes + (s & 3) * 32) >> 4);
+        const uint64_t dsc = db + (((s >> 2) * C::kKQChunk + (s & 3) * 32) >> 4);
         mma_bf16(tmem + 2 * NPM, dsc, dsc, id2, s ? 1u : 0u);
       }
       mma_commit(&bars[7]);
@@ -971,9 +983,16 @@ cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, const PrevRou
                        cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t attr = once_per_device(attr_done, [] {
-    return cudaFuncSetAttribute(verify_tc_kernel<NPM, FUSED, SB>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(TcCfg<NPM>::kDynSmem));
+    cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel<NPM, FUSED, SB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(TcCfg<NPM>::kDynSmem));
+    // the whole unified L1/shared array as shared memory, so that the
+    // resident CTAs (two, three for 16-node trees) fit
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(verify_tc_kernel<NPM, FUSED, SB>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    return e;
   });
   if (attr != cudaSuccess) return attr;
   const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
