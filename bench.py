@@ -906,7 +906,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--cpu-requests", type=int, default=16,
-                    help="requests of the oracle's CPU-baseline sample (0: skip it)")
+                    help="requests of the oracle's CPU-baseline sample (0: skip it, and the "
+                         "oracle samples of --study configs)")
     ap.add_argument("--ref-requests", type=int, default=8,
                     help="requests per step of the reference arm's sample")
     ap.add_argument("--no-storeall", action="store_true")
@@ -923,8 +924,7 @@ def main():
     # The oracle's worker pool is forked here, before this process makes any
     # GPU call (its workers only run numpy).
     pool = None
-    wants_pool = (args.impl == "reference" or args.study == "configs" or
-                  (args.study is None and args.cpu_requests > 0))
+    wants_pool = args.impl == "reference" or (args.study in (None, "configs") and args.cpu_requests > 0)
     if wants_pool and rank == 0 and world == 1:
         from oracle.pool import OraclePool
         pool = OraclePool(method="fork")
