@@ -686,15 +686,16 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
         }
       }
       if constexpr (SB) {
-        // the bf16 chunk holds both column blocks: stored once both are done
+        // the bf16 chunk holds both column blocks: stored once both are done.
+        // The products only read the tile, so they are issued while the
+        // store is still reading it; the store's read is waited for further
+        // down, before anything overwrites the region.
         fence_proxy_async_smem();
         if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
         if (lane == 0) {
           tma_store_2d(&map_s0, s0 + wg * kS0ChunkBytes, 64 * wg, (ts.slot * H + h) * kDim);
           bulk_commit_group();
-          bulk_wait_group_read0();
         }
-        if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
       } else if (!issued) {
         // nothing to convert: the stores still finish reading before the CTA ends
         if (lane == 0) bulk_wait_group_read0();
@@ -775,6 +776,13 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
       mma_commit(&bars[7]);
       s_mma_issued = 1;
     }
+  }
+  if constexpr (FUSED && SB) {
+    // a bf16 pool's S_a tile went out by bulk stores issued by lane 0 of each
+    // warpgroup: they finish reading it here, while the products run and
+    // before the second product's operands overwrite the region (and before
+    // the CTA can end)
+    if (lane == 0) bulk_wait_group_read0();
   }
   __syncthreads();
   fail |= s_fail;
