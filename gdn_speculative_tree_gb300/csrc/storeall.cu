@@ -8,10 +8,12 @@
 // behaviour TreeWY removes; it is kept as an in-library baseline.
 //
 // One CTA of 256 threads per (request, head), the state held in registers.  For
-// dk = dv = 128 each warp owns whole 512-byte rows (coalesced snapshot stores);
-// other head sizes use a half-row-per-thread layout.  A node whose parent is
-// not the previous node reloads the parent's snapshot (which the same thread
-// wrote) from global memory.
+// dk = dv = 128 (storeall_verify_rows_kernel) each thread owns 4 rows x 16
+// columns, the nodes are walked in depth-first pre-order and a parent's
+// snapshot is read back only after a branch point; other head sizes
+// (storeall_verify_kernel) use a half-row-per-thread layout in index order,
+// where a node whose parent is not the previous node reloads the parent's
+// snapshot (which the same thread wrote) from global memory.
 #include "treewy_device.cuh"
 #include "treewy_internal.h"
 
