@@ -798,12 +798,13 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
       // skip this warpgroup's work; the join below reports the failure
     } else if (wg == 0) {
       // ---- ancestor coefficients from this lane's Gram row.  The row is
-      //      dumped to shared memory (thread-private, XOR-swizzled, in the
-      //      [T;B] area that is written only later), then each lane walks its
-      //      own node's path: A entries for lanes < N, M entries for lanes
-      //      Np..Np+N-1.
+      //      dumped to shared memory (thread-private, in the [T;B] area that
+      //      is written only later) as 16-byte groups of four columns, group
+      //      g of row `lane` at position g ^ (lane & 7) (conflict-free across
+      //      each eight lanes), then each lane walks its own node's path: A
+      //      entries for lanes < N, M entries for lanes Np..Np+N-1.
       float* gdump = reinterpret_cast<float*>(s0 + kThiOff);  // 128 rows x 64 floats
-      const int gsw = lane & 31;
+      const int gsw = lane & 7;
 #pragma unroll
       for (int c = 0; c < NPM / 16; ++c) {
         if (c < nch) {
@@ -813,8 +814,9 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
           tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * c, cur);
           tmem_wait16(cur);
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            gdump[lane * 64 + ((16 * c + j) ^ gsw)] = __uint_as_float(cur[j]);
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(gdump + lane * 64 + (((4 * c + q) ^ gsw) << 2)) =
+                make_uint4(cur[4 * q], cur[4 * q + 1], cur[4 * q + 2], cur[4 * q + 3]);
         }
       }
       const bool isA = lane < N;
@@ -829,13 +831,13 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
           for (int k = 0; k < kRegPath; ++k) {
             if (k >= k0 && k < Dn) {
               const int i = pidx[offn + k];
-              dst[offn + k] = scale * pc[offn + k] * gdump[lane * 64 + (i ^ gsw)];
+              dst[offn + k] = scale * pc[offn + k] * gdump[lane * 64 + ((((i >> 2) ^ gsw) << 2) | (i & 3))];
             }
           }
         } else {
           for (int k = k0; k < Dn; ++k) {
             const int i = pidx[offn + k];
-            dst[offn + k] = scale * pc[offn + k] * gdump[lane * 64 + (i ^ gsw)];
+            dst[offn + k] = scale * pc[offn + k] * gdump[lane * 64 + ((((i >> 2) ^ gsw) << 2) | (i & 3))];
           }
         }
       }
