@@ -77,7 +77,7 @@ struct TcCfg {
 
 // Per-CTA tree data for one (request, head), sized by the capacity bucket.
 template <int NPM>
-struct TreeTC {
+struct __align__(16) TreeTC {
   int parent[NPM];
   float alpha[NPM];
   float gamma[NPM];
@@ -854,12 +854,14 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
           tmem_wait16(cur);
           float w[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 16; j += 2) {
+            // (beta, beta gamma) of nodes n and n + 1 in one 16-byte broadcast
             const int n = 16 * c + j;
             const uint32_t pair = vpk[n >> 1];
-            const float vv = bf16_bits_to_float(static_cast<uint16_t>((n & 1) ? (pair >> 16) : pair));
-            const float2 bb = ts.bbg[n];
-            w[j] = (n < N) ? fmaf(-bb.y, __uint_as_float(cur[j]), bb.x * vv) : 0.f;
+            const float4 bb = *reinterpret_cast<const float4*>(&ts.bbg[n]);
+            const float v0 = __uint_as_float(pair << 16), v1 = __uint_as_float(pair & 0xFFFF0000u);
+            w[j] = (n < N) ? fmaf(-bb.y, __uint_as_float(cur[j]), bb.x * v0) : 0.f;
+            w[j + 1] = (n + 1 < N) ? fmaf(-bb.w, __uint_as_float(cur[j + 1]), bb.z * v1) : 0.f;
           }
           uint32_t hi[8], lo[8];
 #pragma unroll
@@ -944,12 +946,17 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
             uint32_t(&oo)[8] = k ? ob : oa;
             uint32_t(&pq)[8] = k ? qb : qa;
             if (k == 0 || two) {
+              // gamma of the eight nodes in two 16-byte broadcasts
+              const int n0 = 16 * (c0 + k) + half;
+              const float4 g0 = *reinterpret_cast<const float4*>(&ts.gamma[n0]);
+              const float4 g1 = *reinterpret_cast<const float4*>(&ts.gamma[n0 + 4]);
+              const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const int n = 16 * (c0 + k) + half + j;
+                const int n = n0 + j;
                 if (n < N) {
                   ug[n * stride] = __uint_as_float(u[j]);
-                  og[n * stride] = fmaf(ts.gamma[n], __uint_as_float(pq[j]), __uint_as_float(oo[j]));
+                  og[n * stride] = fmaf(gm[j], __uint_as_float(pq[j]), __uint_as_float(oo[j]));
                 }
               }
             }
