@@ -789,6 +789,36 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
   const bool bad_tree = go && s_bad_tree;
   const bool work = issued && !bad_tree;
 
+  // Thread 0's last duties: the request's status bits, and (waits = true) a
+  // check that no copy or product still targets this CTA's memory.  On the
+  // full path every barrier has already been waited for by the thread that
+  // consumed it, so only the status is written, before the stores of U and o
+  // (which would otherwise hold it, and the CTA's exit, back); on every other
+  // path both run at the end.
+  bool finished = false;
+  auto finish = [&](bool waits) {
+    int bits = (fail ? kStatusTimeout : 0);
+    if (h == 0) bits |= ts.flags | ts.cflags | (bad_tree ? TREEWY_STATUS_BAD_TREE : 0);
+    // the previous round's tree failed its checks, or a wait gave up before
+    // S_a was stored: that request's commit did not happen
+    if (bad_prev && h == 0) bits |= TREEWY_STATUS_BAD_TREE | TREEWY_STATUS_COMMIT_REFUSED;
+    if (fail && commit_now && !stored) bits |= TREEWY_STATUS_COMMIT_REFUSED;
+    if (bits) atomicOr(b.status + r, bits);
+    finished = true;
+    if (!waits) return;
+    // No async copy or MMA may still target this CTA's memory at exit.
+    if (have_s0)
+      for (int i = 0; i < kChunks; ++i) mbar_wait(&bars[i], 0);
+    if (issued) {
+      mbar_wait(&bars[4], 0);
+      if (s_mma_issued) {
+        mbar_wait(&bars[5], 0);
+        mbar_wait(&bars[7], 0);
+      }
+      if (mma2_issued) mbar_wait(&bars[6], 0);
+    }
+  };
+
   if (work && !fail) {
     // warpgroup 1 (W^T) waits for S0 [K;Q]^T, warpgroup 0 for the Gram (both products)
     if (lane == 0 && !mbar_wait(&bars[wg ? 5 : 7], 0)) fail = 1;
@@ -914,6 +944,7 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
     fail = __syncthreads_or(fail);
     if (!fail) {
       tc_fence_after_sync();
+      if (t == 0) finish(false);
       // ---- U[n] and o_n = gamma_n S0 q_n + O[n], column d = lane; warpgroup
       //      wg stores nodes 16c + 8wg .. 16c + 8wg + 7 of every 16-node chunk,
       //      reading only those 8 columns of U, O and S0 q, two chunks per
@@ -967,26 +998,7 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
     }
   }
 
-  if (t == 0) {
-    int bits = (fail ? kStatusTimeout : 0);
-    if (h == 0) bits |= ts.flags | ts.cflags | (bad_tree ? TREEWY_STATUS_BAD_TREE : 0);
-    // the previous round's tree failed its checks, or a wait gave up before
-    // S_a was stored: that request's commit did not happen
-    if (bad_prev && h == 0) bits |= TREEWY_STATUS_BAD_TREE | TREEWY_STATUS_COMMIT_REFUSED;
-    if (fail && commit_now && !stored) bits |= TREEWY_STATUS_COMMIT_REFUSED;
-    if (bits) atomicOr(b.status + r, bits);
-    // No async copy or MMA may still target this CTA's memory at exit.
-    if (have_s0)
-      for (int i = 0; i < kChunks; ++i) mbar_wait(&bars[i], 0);
-    if (issued) {
-      mbar_wait(&bars[4], 0);
-      if (s_mma_issued) {
-        mbar_wait(&bars[5], 0);
-        mbar_wait(&bars[7], 0);
-      }
-      if (mma2_issued) mbar_wait(&bars[6], 0);
-    }
-  }
+  if (t == 0 && !finished) finish(true);
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
