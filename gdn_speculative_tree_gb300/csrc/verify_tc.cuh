@@ -225,15 +225,14 @@ __device__ __forceinline__ void put_operand(unsigned char* hi, unsigned char* lo
 // M coefficients along its path) on node n's path p_0 = n, p_1, ...: solves
 // x_q = r_q - sum_{a<q} x_a A[p_a, p_q], where A[p_a, p_q] is the entry of
 // p_a's strict-ancestor list at position q - a, and writes x_q (hi/lo bf16) at
-// column p_q of operand row `row`.  `scratch` holds x for paths longer than
-// kRegPath (registers otherwise).
+// column p_q of operand row `row`, which the caller has cleared.  `scratch`
+// holds x for paths longer than kRegPath (registers otherwise).
 template <int NPM>
 __device__ __forceinline__ void build_path_row(const TreeTC<NPM>& ts, int n, int row,
                                                const uint8_t* pidx, const float* aco,
                                                const float* rhs, float* scratch,
                                                unsigned char* thi, unsigned char* tlo) {
   const int Dn = ts.D[n], o = ts.off[n];
-  zero_operand_row(thi, tlo, row);
   if (Dn <= kRegPath) {
     int col[kRegPath], opa[kRegPath];
     float x[kRegPath];
@@ -828,12 +827,15 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
       // skip this warpgroup's work; the join below reports the failure
     } else if (wg == 0) {
       // ---- ancestor coefficients from this lane's Gram row.  The row is
-      //      dumped to shared memory (thread-private, in the [T;B] area that
-      //      is written only later) as 16-byte groups of four columns, group
-      //      g of row `lane` at position g ^ (lane & 7) (conflict-free across
-      //      each eight lanes), then each lane walks its own node's path: A
-      //      entries for lanes < N, M entries for lanes Np..Np+N-1.
-      float* gdump = reinterpret_cast<float*>(s0 + kThiOff);  // 128 rows x 64 floats
+      //      dumped to shared memory where this lane's own row of [T;B] will
+      //      go (columns 0-31 in the hi operand row, 32-63 in the lo row, as
+      //      16-byte groups of four columns, group g of a half at position
+      //      g ^ (lane & 7): conflict-free across each eight lanes), then each
+      //      lane walks its own node's path: A entries for lanes < N, M
+      //      entries for lanes Np..Np+N-1.  No other lane reads the dump, so
+      //      each lane clears its operand row as soon as its own walk is done.
+      float* dhi = reinterpret_cast<float*>(thi + lane * 128);
+      float* dlo = reinterpret_cast<float*>(tlo + lane * 128);
       const int gsw = lane & 7;
 #pragma unroll
       for (int c = 0; c < NPM / 16; ++c) {
@@ -844,11 +846,17 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
           tmem_ld16_async(tmem + lane_base + 2 * NPM + 16 * c, cur);
           tmem_wait16(cur);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(gdump + lane * 64 + (((4 * c + q) ^ gsw) << 2)) =
+          for (int q = 0; q < 4; ++q) {
+            const int g = 4 * c + q;  // column group 0..15
+            *reinterpret_cast<uint4*>((g < 8 ? dhi : dlo) + (((g & 7) ^ gsw) << 2)) =
                 make_uint4(cur[4 * q], cur[4 * q + 1], cur[4 * q + 2], cur[4 * q + 3]);
+          }
         }
       }
+      // column i of the dumped row
+      auto gram = [&](int i) {
+        return ((i & 32) ? dlo : dhi)[((((i >> 2) & 7) ^ gsw) << 2) | (i & 3)];
+      };
       const bool isA = lane < N;
       const int myn = isA ? lane : ((lane >= Np && lane < Np + N) ? lane - Np : -1);
       if (myn >= 0) {
@@ -860,17 +868,14 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
 #pragma unroll
           for (int k = 0; k < kRegPath; ++k) {
             if (k >= k0 && k < Dn) {
-              const int i = pidx[offn + k];
-              dst[offn + k] = scale * pc[offn + k] * gdump[lane * 64 + ((((i >> 2) ^ gsw) << 2) | (i & 3))];
+              dst[offn + k] = scale * pc[offn + k] * gram(pidx[offn + k]);
             }
           }
         } else {
-          for (int k = k0; k < Dn; ++k) {
-            const int i = pidx[offn + k];
-            dst[offn + k] = scale * pc[offn + k] * gdump[lane * 64 + ((((i >> 2) ^ gsw) << 2) | (i & 3))];
-          }
+          for (int k = k0; k < Dn; ++k) dst[offn + k] = scale * pc[offn + k] * gram(pidx[offn + k]);
         }
       }
+      if (lane < 2 * Np) zero_operand_row(thi, tlo, lane);
     } else {
       // ---- row `lane` of W^T: W[n][d] = beta_n v_n[d] - beta_n gamma_n (S0 k_n)[d]
       unsigned char* whi = s0 + kWhiOff + lane * 128;
@@ -909,11 +914,11 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
     }
     if (wg == 0 && !fail) {
       named_bar_sync<1, 128>();
-      // ---- T rows (threads 0..N-1) and B rows (threads 64..64+N-1) together;
-      //      the padding rows of [T;B] are zeroed by the lanes that own them
-      if ((t >= N && t < Np) || (t >= Np + N && t < 2 * Np)) zero_operand_row(thi, tlo, t);
-      if (t < N) build_path_row(ts, t, t, pidx, aco, nullptr, xT, thi, tlo);
-      if (t >= 64 && t - 64 < N) build_path_row(ts, t - 64, Np + t - 64, pidx, aco, mco, xB, thi, tlo);
+      // ---- row t of [T;B] by thread t (the lane whose walk produced that
+      //      node's coefficients): T rows for t < N, B rows for Np <= t < Np+N
+      const bool isT = t < N, isB = t >= Np && t < Np + N;
+      if (isT || isB)
+        build_path_row(ts, isT ? t : t - Np, t, pidx, aco, isB ? mco : nullptr, isB ? xB : xT, thi, tlo);
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
