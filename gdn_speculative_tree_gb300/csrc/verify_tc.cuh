@@ -299,6 +299,9 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
   using C = TcCfg<NPM>;
   constexpr int kChunks = SB ? 2 : 4;      // S0 boxes of 16 KB
   constexpr int kChunkCols = SB ? 64 : 32;
+  // a fused commit on a bf16 state forms its rank-|path| update on the tensor
+  // cores into TMEM columns 0..127, before the first products need them
+  constexpr uint32_t kTmemCols = (FUSED && SB && C::kCols < 128u) ? 128u : C::kCols;
   extern __shared__ unsigned char smem_raw[];
   __shared__ TreeTC<NPM> ts;
   __shared__ PrevSmem<FUSED> pv;
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
     }
   } else if (warp == 1) {
     // TMEM is allocated by a warp that does not wait on the metadata loads
-    tmem_alloc(&tmem_holder, C::kCols);
+    tmem_alloc(&tmem_holder, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -493,8 +496,40 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
   // stage its first segment (k rows in shared memory, c_j u_j[lane] in registers).
   bool bad_prev = false;
   float cu[kPrevSeg];
+  uint32_t kb[kPrevSeg / 2];  // bf16 state: k_j[lane] of this thread's path entries, in pairs
 #pragma unroll
   for (int j = 0; j < kPrevSeg; ++j) cu[j] = 0.f;
+#pragma unroll
+  for (int j = 0; j < kPrevSeg / 2; ++j) kb[j] = 0u;
+  // bf16 state: this thread's part of a 16-entry path segment starting at
+  // seg, entries seg + 8wg .. seg + 8wg + 7: c_j u_j[lane] (row `lane` of the
+  // update's left operand) and k_j[lane] (row `lane` of its right operand),
+  // zero past the path's end; all loads issued before any result is used.
+  auto stage_tc = [&](int seg) {
+    if constexpr (FUSED && SB) {
+      const unsigned short* kg = reinterpret_cast<const unsigned short*>(prev.k);
+      uint32_t kh[kPrevSeg];
+      float uv[kPrevSeg];
+#pragma unroll
+      for (int j = 0; j < kPrevSeg; ++j) {
+        const int pos = seg + kPrevSeg * wg + j;
+        kh[j] = 0u;
+        uv[j] = 0.f;
+        if (pos < pv.len) {
+          const int64_t row = (static_cast<int64_t>(pv.tok0) + pv.path[pos]) * H + h;
+          kh[j] = __ldg(kg + row * kDim + lane);
+          uv[j] = __ldg(prev.U + row * kDim + lane);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kPrevSeg; ++j) {
+        const int pos = seg + kPrevSeg * wg + j;
+        cu[j] = (pos < pv.len) ? pv.c[pos] * uv[j] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kPrevSeg / 2; ++j) kb[j] = kh[2 * j] | (kh[2 * j + 1] << 16);
+    }
+  };
   auto stage_prev = [&](int seg) {
     if constexpr (FUSED) {
       // every load of the pass is issued before any of its results is used
@@ -555,7 +590,10 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
         pv.gamma_a = c;
       }
       __syncthreads();
-      if (!bad_prev) stage_prev(0);
+      if (!bad_prev) {
+        if constexpr (SB) stage_tc(0);
+        else stage_prev(0);
+      }
       __syncthreads();
     }
   }
@@ -589,6 +627,7 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
     fail = wg ? named_bar_or<2, 128>(fail) : named_bar_or<1, 128>(fail);
   }
   bool stored = false;  // the fused commit has stored S_a (uniform)
+  int reb_pending = -1;  // thread 0: parity of an update product not yet waited for
   if constexpr (FUSED) {
     // S_a = gamma_a S0 + sum_j c_j u_j k_j^T on this thread's own part of row
     // `lane` (columns 64wg .. 64wg+63: chunks 2wg, 2wg+1 of an fp32 tile,
@@ -598,24 +637,93 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
     if (commit_now && !__syncthreads_or(fail)) {
       const float ga = pv.gamma_a;
       const int len = pv.len;
+      if constexpr (SB) {
+        // The update sum_j c_j u_j k_j^T on the tensor cores: per 16-entry
+        // path segment, D += [c u]_hi K_p^T + [c u]_lo K_p^T (M = N = 128,
+        // K = 16) into TMEM columns 0..127, both operands in one 128-row tile
+        // of the free upper half of the state region (K-major, 128-byte
+        // swizzle): k-slot 0 holds (c_j u_j[d])_hi, slot 1 the _lo parts, slot
+        // 2 k_j[c]; thread (wg, lane) writes entries 8wg..8wg+7 of row `lane`
+        // of each.  Then S_a = gamma_a S0 + D row by row, rounded once.
+        unsigned char* opt = s0 + 2 * kS0ChunkBytes;
+        unsigned char* orow = opt + lane * 128;
+        const int r7 = lane & 7;
+        const int nseg = (len + 2 * kPrevSeg - 1) / (2 * kPrevSeg);
+        for (int sg = 0; sg < nseg; ++sg) {
+          uint32_t hi[kPrevSeg / 2], lo[kPrevSeg / 2];
+#pragma unroll
+          for (int j = 0; j < kPrevSeg / 2; ++j) split_pair(cu[2 * j], cu[2 * j + 1], hi[j], lo[j]);
+          *reinterpret_cast<uint4*>(orow + (((0 + wg) ^ r7) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(orow + (((2 + wg) ^ r7) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(orow + (((4 + wg) ^ r7) << 4)) = make_uint4(kb[0], kb[1], kb[2], kb[3]);
+          fence_proxy_async_smem();
+          __syncthreads();
+          if (t == 0) {
+            tc_fence_after_sync();
+            const uint64_t dt = smem_desc_sw128(smem_addr(opt), 1024);
+            const uint32_t idr = idesc_bf16_f32(128, 128);
+            mma_bf16(tmem, dt, dt + (64 >> 4), idr, sg ? 1u : 0u);
+            mma_bf16(tmem, dt + (32 >> 4), dt + (64 >> 4), idr, 1u);
+            mma_commit(&bars[3]);
+            reb_pending = sg & 1;
+          }
+          // the next segment's values are requested while the products run
+          if (sg + 1 < nseg) stage_tc(2 * kPrevSeg * (sg + 1));
+          // the tile is rewritten (or D read) only once the products are done
+          bool ok = true;
+          if (t == 0) {
+            ok = mbar_wait(&bars[3], sg & 1);
+            if (ok) reb_pending = -1;
+          }
+          fail = __syncthreads_or(!ok);
+          if (fail) break;
+        }
+        if (!fail) {
+          tc_fence_after_sync();
+          unsigned char* row = s0 + wg * kS0ChunkBytes + lane * 128;
+          for (int hb = 0; hb < 2; ++hb) {
+            uint32_t d0[16], d1[16];
+            tmem_ld16_async(tmem + lane_base + 64 * wg + 32 * hb, d0);
+            tmem_ld16_async(tmem + lane_base + 64 * wg + 32 * hb + 16, d1);
+            tmem_wait16(d0);
+            tmem_wait16(d1);
+#pragma unroll
+            for (int g4 = 0; g4 < 4; ++g4) {
+              unsigned char* gp = row + (((4 * hb + g4) ^ r7) << 4);
+              const uint4 raw = *reinterpret_cast<const uint4*>(gp);
+              const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+              uint32_t o[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int j = 8 * g4 + 2 * i;  // column 64wg + 32hb + j
+                const float u0 = __uint_as_float(j < 16 ? d0[j] : d1[j - 16]);
+                const float u1 = __uint_as_float(j < 16 ? d0[j + 1] : d1[j - 15]);
+                const __nv_bfloat162 p = __floats2bfloat162_rn(fmaf(ga, __uint_as_float(w[i] << 16), u0),
+                                                               fmaf(ga, __uint_as_float(w[i] & 0xFFFF0000u), u1));
+                o[i] = *reinterpret_cast<const uint32_t*>(&p);
+              }
+              *reinterpret_cast<uint4*>(gp) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+          // the bf16 chunk holds both column blocks: stored once both are
+          // done.  The products only read the tile, so they are issued while
+          // the store is still reading it; the store's read is waited for
+          // further down, before anything overwrites the region.
+          fence_proxy_async_smem();
+          if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+          if (lane == 0) {
+            tma_store_2d(&map_s0, s0 + wg * kS0ChunkBytes, 64 * wg, (ts.slot * H + h) * kDim);
+            bulk_commit_group();
+          }
+          stored = true;
+        }
+      } else {
       const int nseg = (len + kPrevSeg - 1) / kPrevSeg;
       int staged = 0;
       for (int hb = 0; hb < 2; ++hb) {
         const int col0 = 64 * wg + 32 * hb;
         float x[32];
-        if constexpr (SB) {
-          const unsigned char* row = s0 + wg * kS0ChunkBytes + lane * 128;
-#pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(row + (((4 * hb + g4) ^ (lane & 7)) << 4));
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              x[8 * g4 + 2 * i] = ga * __uint_as_float(w[i] << 16);
-              x[8 * g4 + 2 * i + 1] = ga * __uint_as_float(w[i] & 0xFFFF0000u);
-            }
-          }
-        } else {
+        {
           const unsigned char* row = s0 + (2 * wg + hb) * kS0ChunkBytes + lane * 128;
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
@@ -652,20 +760,7 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
             }
           }
         }
-        if constexpr (SB) {
-          unsigned char* row = s0 + wg * kS0ChunkBytes + lane * 128;
-#pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const __nv_bfloat162 p = __floats2bfloat162_rn(x[8 * g4 + 2 * i], x[8 * g4 + 2 * i + 1]);
-              w[i] = *reinterpret_cast<const uint32_t*>(&p);
-            }
-            *reinterpret_cast<uint4*>(row + (((4 * hb + g4) ^ (lane & 7)) << 4)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        } else {
+        {
           unsigned char* row = s0 + (2 * wg + hb) * kS0ChunkBytes + lane * 128;
 #pragma unroll
           for (int g = 0; g < 8; ++g)
@@ -684,23 +779,13 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
           }
         }
       }
-      if constexpr (SB) {
-        // the bf16 chunk holds both column blocks: stored once both are done.
-        // The products only read the tile, so they are issued while the
-        // store is still reading it; the store's read is waited for further
-        // down, before anything overwrites the region.
-        fence_proxy_async_smem();
-        if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
-        if (lane == 0) {
-          tma_store_2d(&map_s0, s0 + wg * kS0ChunkBytes, 64 * wg, (ts.slot * H + h) * kDim);
-          bulk_commit_group();
+        if (!issued) {
+          // nothing to convert: the stores still finish reading before the CTA ends
+          if (lane == 0) bulk_wait_group_read0();
+          if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
         }
-      } else if (!issued) {
-        // nothing to convert: the stores still finish reading before the CTA ends
-        if (lane == 0) bulk_wait_group_read0();
-        if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+        stored = true;
       }
-      stored = true;
     }
   }
   if constexpr (!SB) {
@@ -806,6 +891,9 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
     finished = true;
     if (!waits) return;
     // No async copy or MMA may still target this CTA's memory at exit.
+    if constexpr (FUSED && SB) {
+      if (reb_pending >= 0) mbar_wait(&bars[3], reb_pending);
+    }
     if (have_s0)
       for (int i = 0; i < kChunks; ++i) mbar_wait(&bars[i], 0);
     if (issued) {
@@ -1008,7 +1096,7 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, C::kCols);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
