@@ -299,14 +299,22 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
   using C = TcCfg<NPM>;
   constexpr int kChunks = SB ? 2 : 4;      // S0 boxes of 16 KB
   constexpr int kChunkCols = SB ? 64 : 32;
-  // a fused commit on a bf16 state forms its rank-|path| update on the tensor
-  // cores into TMEM columns 0..127, before the first products need them
-  constexpr uint32_t kTmemCols = (FUSED && SB && C::kCols < 128u) ? 128u : C::kCols;
+  // The fused commit forms its rank-|path| update on the tensor cores into
+  // TMEM columns 0..127 (before the first products need them), with its
+  // operands in a 16 KB tile: the free upper half of the state region for a
+  // bf16 state, the K/Q region for an fp32 one (whose K/Q boxes are then
+  // requested once the update has read it; a 16-node tree's K/Q region is too
+  // small, so that instance updates on the CUDA cores).
+  constexpr bool kTcUpd = FUSED && (SB || NPM >= 32);
+  constexpr bool kDeferKQ = kTcUpd && !SB;
+  constexpr uint32_t kTmemCols = (kTcUpd && C::kCols < 128u) ? 128u : C::kCols;
   extern __shared__ unsigned char smem_raw[];
   __shared__ TreeTC<NPM> ts;
   __shared__ PrevSmem<FUSED> pv;
-  // 0-3: S0 chunks, 4: K/Q, 5: S0 [K;Q]^T done, 6: second MMA done, 7: Gram done
-  __shared__ __align__(8) uint64_t bars[8];
+  // 0-3: S0 chunks, 4: K/Q, 5: S0 [K;Q]^T done, 6: second MMA done, 7: Gram
+  // done, 8: the fused commit's update products done
+  __shared__ __align__(8) uint64_t bars[9];
+  __shared__ int s_kq_issued;   // the K/Q boxes have been requested
   __shared__ uint32_t tmem_holder;
   __shared__ int s_fail;
   __shared__ int s_bad_tree;    // written by thread 0 after the tree preparation
@@ -393,7 +401,8 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
 
   if (t == 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 9; ++i) mbar_init(&bars[i], 1);
+    s_kq_issued = 0;
     fence_mbarrier_init();
     s_fail = 0;
     s_bad_tree = 0;
@@ -449,14 +458,13 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
       mbar_arrive_expect_tx(&bars[4], static_cast<uint32_t>((N + 15) & ~15) * 512u);
     }
   }
-  if (warp == 0) {
-    // the K and Q boxes are issued by the lanes of warp 0 in parallel, after
-    // lane 0 has set up the barrier and the expected bytes.  Each issue costs
-    // the issuing warp tens of cycles, so the Np = N rounded up to 16 rows of
-    // a (tensor, column chunk) come as 32-row boxes and at most one 16-row
-    // box: 4 boxes for N <= 32, 8 above, against 4 * N/8 boxes of 8 rows.
-    // Rows N..Np-1 (the next request's, or zero fill past T) are never used.
-    __syncwarp();
+  // The K and Q boxes, issued by the lanes of warp 0 in parallel (thread 0
+  // has set up the barrier and the expected bytes).  Each issue costs the
+  // issuing warp tens of cycles, so the Np = N rounded up to 16 rows of a
+  // (tensor, column chunk) come as 32-row boxes and at most one 16-row box:
+  // 4 boxes for N <= 32, 8 above, against 4 * N/8 boxes of 8 rows.  Rows
+  // N..Np-1 (the next request's, or zero fill past T) are never used.
+  auto issue_kq = [&]() {
     const int N = ts.N;
     if (ts.flags == 0 && N > 0) {
       const int Np = (N + 15) & ~15;
@@ -472,7 +480,15 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
         else
           tma_load_3d(chunk + rb * 128, big ? &map_k32 : &map_k, &bars[4], 64 * c2, h, ts.tok0 + rb);
       }
+      if (t == 0) s_kq_issued = 1;
     }
+  };
+  // an fp32 fused commit that will run keeps the K/Q region for its update
+  bool kq_deferred = false;
+  if (warp == 0) {
+    __syncwarp();
+    if constexpr (kDeferKQ) kq_deferred = pv.a >= 0;
+    if (!kq_deferred) issue_kq();
   } else if (warp == 1) {
     // TMEM is allocated by a warp that does not wait on the metadata loads
     tmem_alloc(&tmem_holder, kTmemCols);
@@ -506,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
   // update's left operand) and k_j[lane] (row `lane` of its right operand),
   // zero past the path's end; all loads issued before any result is used.
   auto stage_tc = [&](int seg) {
-    if constexpr (FUSED && SB) {
+    if constexpr (kTcUpd) {
       const unsigned short* kg = reinterpret_cast<const unsigned short*>(prev.k);
       uint32_t kh[kPrevSeg];
       float uv[kPrevSeg];
@@ -591,13 +607,17 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
       }
       __syncthreads();
       if (!bad_prev) {
-        if constexpr (SB) stage_tc(0);
+        if constexpr (kTcUpd) stage_tc(0);
         else stage_prev(0);
       }
       __syncthreads();
     }
   }
   const bool commit_now = commit_a >= 0 && !bad_prev;
+  if constexpr (kDeferKQ) {
+    // a refused commit does not need the K/Q region: its boxes go now
+    if (warp == 0 && kq_deferred && !commit_now) issue_kq();
+  }
   if (wg == 1) {
     const int par = lane & 1;
 #pragma unroll
@@ -637,15 +657,15 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
     if (commit_now && !__syncthreads_or(fail)) {
       const float ga = pv.gamma_a;
       const int len = pv.len;
-      if constexpr (SB) {
+      if constexpr (kTcUpd) {
         // The update sum_j c_j u_j k_j^T on the tensor cores: per 16-entry
         // path segment, D += [c u]_hi K_p^T + [c u]_lo K_p^T (M = N = 128,
         // K = 16) into TMEM columns 0..127, both operands in one 128-row tile
-        // of the free upper half of the state region (K-major, 128-byte
-        // swizzle): k-slot 0 holds (c_j u_j[d])_hi, slot 1 the _lo parts, slot
-        // 2 k_j[c]; thread (wg, lane) writes entries 8wg..8wg+7 of row `lane`
-        // of each.  Then S_a = gamma_a S0 + D row by row, rounded once.
-        unsigned char* opt = s0 + 2 * kS0ChunkBytes;
+        // (K-major, 128-byte swizzle): k-slot 0 holds (c_j u_j[d])_hi, slot 1
+        // the _lo parts, slot 2 k_j[c]; thread (wg, lane) writes entries
+        // 8wg..8wg+7 of row `lane` of each.  Then S_a = gamma_a S0 + D row by
+        // row (rounded once for a bf16 state).
+        unsigned char* opt = SB ? s0 + 2 * kS0ChunkBytes : kq;
         unsigned char* orow = opt + lane * 128;
         const int r7 = lane & 7;
         const int nseg = (len + 2 * kPrevSeg - 1) / (2 * kPrevSeg);
@@ -664,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
             const uint32_t idr = idesc_bf16_f32(128, 128);
             mma_bf16(tmem, dt, dt + (64 >> 4), idr, sg ? 1u : 0u);
             mma_bf16(tmem, dt + (32 >> 4), dt + (64 >> 4), idr, 1u);
-            mma_commit(&bars[3]);
+            mma_commit(&bars[8]);
             reb_pending = sg & 1;
           }
           // the next segment's values are requested while the products run
@@ -672,113 +692,155 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
           // the tile is rewritten (or D read) only once the products are done
           bool ok = true;
           if (t == 0) {
-            ok = mbar_wait(&bars[3], sg & 1);
+            ok = mbar_wait(&bars[8], sg & 1);
             if (ok) reb_pending = -1;
           }
           fail = __syncthreads_or(!ok);
           if (fail) break;
         }
+        if constexpr (kDeferKQ) {
+          // the update has read its tile: the K/Q boxes may land there now
+          if (!fail && warp == 0) issue_kq();
+        }
         if (!fail) {
           tc_fence_after_sync();
-          unsigned char* row = s0 + wg * kS0ChunkBytes + lane * 128;
-          for (int hb = 0; hb < 2; ++hb) {
-            uint32_t d0[16], d1[16];
-            tmem_ld16_async(tmem + lane_base + 64 * wg + 32 * hb, d0);
-            tmem_ld16_async(tmem + lane_base + 64 * wg + 32 * hb + 16, d1);
-            tmem_wait16(d0);
-            tmem_wait16(d1);
+          if constexpr (SB) {
+            unsigned char* row = s0 + wg * kS0ChunkBytes + lane * 128;
+            for (int hb = 0; hb < 2; ++hb) {
+              uint32_t d0[16], d1[16];
+              tmem_ld16_async(tmem + lane_base + 64 * wg + 32 * hb, d0);
+              tmem_ld16_async(tmem + lane_base + 64 * wg + 32 * hb + 16, d1);
+              tmem_wait16(d0);
+              tmem_wait16(d1);
 #pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4) {
-              unsigned char* gp = row + (((4 * hb + g4) ^ r7) << 4);
-              const uint4 raw = *reinterpret_cast<const uint4*>(gp);
-              const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-              uint32_t o[4];
+              for (int g4 = 0; g4 < 4; ++g4) {
+                unsigned char* gp = row + (((4 * hb + g4) ^ r7) << 4);
+                const uint4 raw = *reinterpret_cast<const uint4*>(gp);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                uint32_t o[4];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int j = 8 * g4 + 2 * i;  // column 64wg + 32hb + j
-                const float u0 = __uint_as_float(j < 16 ? d0[j] : d1[j - 16]);
-                const float u1 = __uint_as_float(j < 16 ? d0[j + 1] : d1[j - 15]);
-                const __nv_bfloat162 p = __floats2bfloat162_rn(fmaf(ga, __uint_as_float(w[i] << 16), u0),
-                                                               fmaf(ga, __uint_as_float(w[i] & 0xFFFF0000u), u1));
-                o[i] = *reinterpret_cast<const uint32_t*>(&p);
+                for (int i = 0; i < 4; ++i) {
+                  const int j = 8 * g4 + 2 * i;  // column 64wg + 32hb + j
+                  const float u0 = __uint_as_float(j < 16 ? d0[j] : d1[j - 16]);
+                  const float u1 = __uint_as_float(j < 16 ? d0[j + 1] : d1[j - 15]);
+                  const __nv_bfloat162 p = __floats2bfloat162_rn(fmaf(ga, __uint_as_float(w[i] << 16), u0),
+                                                                 fmaf(ga, __uint_as_float(w[i] & 0xFFFF0000u), u1));
+                  o[i] = *reinterpret_cast<const uint32_t*>(&p);
+                }
+                *reinterpret_cast<uint4*>(gp) = make_uint4(o[0], o[1], o[2], o[3]);
               }
-              *reinterpret_cast<uint4*>(gp) = make_uint4(o[0], o[1], o[2], o[3]);
             }
-          }
-          // the bf16 chunk holds both column blocks: stored once both are
-          // done.  The products only read the tile, so they are issued while
-          // the store is still reading it; the store's read is waited for
-          // further down, before anything overwrites the region.
-          fence_proxy_async_smem();
-          if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
-          if (lane == 0) {
-            tma_store_2d(&map_s0, s0 + wg * kS0ChunkBytes, 64 * wg, (ts.slot * H + h) * kDim);
-            bulk_commit_group();
+            // the bf16 chunk holds both column blocks: stored once both are
+            // done.  The products only read the tile, so they are issued while
+            // the store is still reading it; the store's read is waited for
+            // further down, before anything overwrites the region.
+            fence_proxy_async_smem();
+            if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+            if (lane == 0) {
+              tma_store_2d(&map_s0, s0 + wg * kS0ChunkBytes, 64 * wg, (ts.slot * H + h) * kDim);
+              bulk_commit_group();
+            }
+          } else {
+            // fp32: chunk 2wg + hb of row `lane` = columns 64wg + 32hb ..; each
+            // chunk goes back to the pool by a bulk tensor store while the
+            // next one is formed
+            for (int hb = 0; hb < 2; ++hb) {
+              uint32_t d0[16], d1[16];
+              tmem_ld16_async(tmem + lane_base + 64 * wg + 32 * hb, d0);
+              tmem_ld16_async(tmem + lane_base + 64 * wg + 32 * hb + 16, d1);
+              tmem_wait16(d0);
+              tmem_wait16(d1);
+              unsigned char* row = s0 + (2 * wg + hb) * kS0ChunkBytes + lane * 128;
+#pragma unroll
+              for (int g = 0; g < 8; ++g) {
+                float4* gp = reinterpret_cast<float4*>(row + ((g ^ r7) << 4));
+                const float4 v = *gp;
+                const int j = 4 * g;  // column 64wg + 32hb + j
+                const float a0 = __uint_as_float(j < 16 ? d0[j] : d1[j - 16]);
+                const float a1 = __uint_as_float(j < 16 ? d0[j + 1] : d1[j - 15]);
+                const float a2 = __uint_as_float(j < 16 ? d0[j + 2] : d1[j - 14]);
+                const float a3 = __uint_as_float(j < 16 ? d0[j + 3] : d1[j - 13]);
+                *gp = make_float4(fmaf(ga, v.x, a0), fmaf(ga, v.y, a1), fmaf(ga, v.z, a2),
+                                  fmaf(ga, v.w, a3));
+              }
+              fence_proxy_async_smem();
+              if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+              if (lane == 0) {
+                tma_store_2d(&map_s0, s0 + (2 * wg + hb) * kS0ChunkBytes, 32 * (2 * wg + hb),
+                             (ts.slot * H + h) * kDim);
+                bulk_commit_group();
+              }
+            }
+            if (!issued) {
+              // nothing to convert: the stores still finish reading before the CTA ends
+              if (lane == 0) bulk_wait_group_read0();
+              if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+            }
           }
           stored = true;
         }
       } else {
-      const int nseg = (len + kPrevSeg - 1) / kPrevSeg;
-      int staged = 0;
-      for (int hb = 0; hb < 2; ++hb) {
-        const int col0 = 64 * wg + 32 * hb;
-        float x[32];
-        {
-          const unsigned char* row = s0 + (2 * wg + hb) * kS0ChunkBytes + lane * 128;
+        const int nseg = (len + kPrevSeg - 1) / kPrevSeg;
+        int staged = 0;
+        for (int hb = 0; hb < 2; ++hb) {
+          const int col0 = 64 * wg + 32 * hb;
+          float x[32];
+          {
+            const unsigned char* row = s0 + (2 * wg + hb) * kS0ChunkBytes + lane * 128;
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const float4 v = *reinterpret_cast<const float4*>(row + ((g ^ (lane & 7)) << 4));
-            x[4 * g] = ga * v.x;
-            x[4 * g + 1] = ga * v.y;
-            x[4 * g + 2] = ga * v.z;
-            x[4 * g + 3] = ga * v.w;
+            for (int g = 0; g < 8; ++g) {
+              const float4 v = *reinterpret_cast<const float4*>(row + ((g ^ (lane & 7)) << 4));
+              x[4 * g] = ga * v.x;
+              x[4 * g + 1] = ga * v.y;
+              x[4 * g + 2] = ga * v.z;
+              x[4 * g + 3] = ga * v.w;
+            }
           }
-        }
-        for (int sg = 0; sg < nseg; ++sg) {
-          if (sg != staged) {
-            __syncthreads();
-            stage_prev(sg * kPrevSeg);
-            __syncthreads();
-            staged = sg;
-          }
-          const int ns = min(kPrevSeg, len - sg * kPrevSeg);
+          for (int sg = 0; sg < nseg; ++sg) {
+            if (sg != staged) {
+              __syncthreads();
+              stage_prev(sg * kPrevSeg);
+              __syncthreads();
+              staged = sg;
+            }
+            const int ns = min(kPrevSeg, len - sg * kPrevSeg);
 #pragma unroll
-          for (int j = 0; j < kPrevSeg; ++j) {
-            if (j < ns) {
-              const float u = cu[j];
-              const uint4* kr = reinterpret_cast<const uint4*>(&pv.k[j][col0]);
+            for (int j = 0; j < kPrevSeg; ++j) {
+              if (j < ns) {
+                const float u = cu[j];
+                const uint4* kr = reinterpret_cast<const uint4*>(&pv.k[j][col0]);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint4 raw = kr[q];
-                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                for (int q = 0; q < 4; ++q) {
+                  const uint4 raw = kr[q];
+                  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  x[8 * q + 2 * i] = fmaf(u, __uint_as_float(w[i] << 16), x[8 * q + 2 * i]);
-                  x[8 * q + 2 * i + 1] = fmaf(u, __uint_as_float(w[i] & 0xFFFF0000u), x[8 * q + 2 * i + 1]);
+                  for (int i = 0; i < 4; ++i) {
+                    x[8 * q + 2 * i] = fmaf(u, __uint_as_float(w[i] << 16), x[8 * q + 2 * i]);
+                    x[8 * q + 2 * i + 1] = fmaf(u, __uint_as_float(w[i] & 0xFFFF0000u), x[8 * q + 2 * i + 1]);
+                  }
                 }
               }
             }
           }
-        }
-        {
-          unsigned char* row = s0 + (2 * wg + hb) * kS0ChunkBytes + lane * 128;
+          {
+            unsigned char* row = s0 + (2 * wg + hb) * kS0ChunkBytes + lane * 128;
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
-            *reinterpret_cast<float4*>(row + ((g ^ (lane & 7)) << 4)) =
-                make_float4(x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
-          // an fp32 chunk goes back to the pool by a bulk tensor store while
-          // the next one is computed (the tile layout in shared memory is
-          // the one the loads produced; per-thread stores straight from the
-          // registers, 32 rows per warp instruction, were measured slower)
-          fence_proxy_async_smem();
-          if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
-          if (lane == 0) {
-            tma_store_2d(&map_s0, s0 + (2 * wg + hb) * kS0ChunkBytes, 32 * (2 * wg + hb),
-                         (ts.slot * H + h) * kDim);
-            bulk_commit_group();
+            for (int g = 0; g < 8; ++g)
+              *reinterpret_cast<float4*>(row + ((g ^ (lane & 7)) << 4)) =
+                  make_float4(x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
+            // an fp32 chunk goes back to the pool by a bulk tensor store while
+            // the next one is computed (the tile layout in shared memory is
+            // the one the loads produced; per-thread stores straight from the
+            // registers, 32 rows per warp instruction, were measured slower)
+            fence_proxy_async_smem();
+            if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
+            if (lane == 0) {
+              tma_store_2d(&map_s0, s0 + (2 * wg + hb) * kS0ChunkBytes, 32 * (2 * wg + hb),
+                           (ts.slot * H + h) * kDim);
+              bulk_commit_group();
+            }
           }
         }
-      }
         if (!issued) {
           // nothing to convert: the stores still finish reading before the CTA ends
           if (lane == 0) bulk_wait_group_read0();
@@ -891,13 +953,13 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
     finished = true;
     if (!waits) return;
     // No async copy or MMA may still target this CTA's memory at exit.
-    if constexpr (FUSED && SB) {
-      if (reb_pending >= 0) mbar_wait(&bars[3], reb_pending);
+    if constexpr (kTcUpd) {
+      if (reb_pending >= 0) mbar_wait(&bars[8], reb_pending);
     }
     if (have_s0)
       for (int i = 0; i < kChunks; ++i) mbar_wait(&bars[i], 0);
     if (issued) {
-      mbar_wait(&bars[4], 0);
+      if (s_kq_issued) mbar_wait(&bars[4], 0);
       if (s_mma_issued) {
         mbar_wait(&bars[5], 0);
         mbar_wait(&bars[7], 0);
