@@ -75,6 +75,18 @@ struct TcCfg {
   static_assert(3u * kListBytes <= kKQ, "A, M and T-scratch lists must fit the K/Q region");
 };
 
+// Dynamic shared memory of one kernel instance.  The fused fp32 instance for
+// 16-node trees adds a 16 KB tile for its commit's update operands after the
+// lists (its K/Q region, 8 KB, is too small to hold them; the larger buckets
+// use their K/Q region, and a bf16 state the free half of the state region).
+template <int NPM, bool FUSED, bool SB>
+struct TcSmem {
+  using C = TcCfg<NPM>;
+  static constexpr bool kExtraUpd = FUSED && !SB && NPM < 32;
+  static constexpr uint32_t kUpdOff = (C::kR2Off + C::kR2Bytes + 1023u) & ~1023u;
+  static constexpr uint32_t kBytes = kExtraUpd ? kUpdOff + 16384u + 1024u : C::kDynSmem;
+};
+
 // Per-CTA tree data for one (request, head), sized by the capacity bucket.
 template <int NPM>
 struct __align__(16) TreeTC {
@@ -267,7 +279,7 @@ __device__ __forceinline__ void build_path_row(const TreeTC<NPM>& ts, int n, int
 
 // Previous-round data for the fused commit (shared memory; empty when the
 // kernel is not fused).
-constexpr int kPrevSeg = 8;  // path nodes of the previous round staged per pass
+constexpr int kPrevSeg = 8;  // path entries a warpgroup stages per 16-entry update segment
 template <bool FUSED>
 struct PrevSmem {
   int a;
@@ -278,7 +290,6 @@ struct PrevSmem<true> {
   float alpha[kMaxNodes];
   float c[kMaxNodes];                // gamma_a / gamma_{path j} (alpha products)
   uint8_t path[kMaxNodes];           // accepted node, its parent, ... (root last)
-  __align__(16) __nv_bfloat16 k[kPrevSeg][kDim];  // staged k rows of up to kPrevSeg path nodes
   int tok0, N, a, len;
   float gamma_a;
 };
@@ -302,12 +313,11 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
   // The fused commit forms its rank-|path| update on the tensor cores into
   // TMEM columns 0..127 (before the first products need them), with its
   // operands in a 16 KB tile: the free upper half of the state region for a
-  // bf16 state, the K/Q region for an fp32 one (whose K/Q boxes are then
-  // requested once the update has read it; a 16-node tree's K/Q region is too
-  // small, so that instance updates on the CUDA cores).
-  constexpr bool kTcUpd = FUSED && (SB || NPM >= 32);
-  constexpr bool kDeferKQ = kTcUpd && !SB;
-  constexpr uint32_t kTmemCols = (kTcUpd && C::kCols < 128u) ? 128u : C::kCols;
+  // bf16 state; for an fp32 one the K/Q region (whose K/Q boxes are then
+  // requested once the update has read it), or for 16-node trees, whose K/Q
+  // region is too small, a tile of its own after the lists.
+  constexpr bool kDeferKQ = FUSED && !SB && NPM >= 32;
+  constexpr uint32_t kTmemCols = (FUSED && C::kCols < 128u) ? 128u : C::kCols;
   extern __shared__ unsigned char smem_raw[];
   __shared__ TreeTC<NPM> ts;
   __shared__ PrevSmem<FUSED> pv;
@@ -509,20 +519,20 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
 
 
   // Fused commit: validate the previous tree, walk the accepted node's path and
-  // stage its first segment (k rows in shared memory, c_j u_j[lane] in registers).
+  // stage its first segment (c_j u_j[lane] and k_j[lane] in registers).
   bool bad_prev = false;
   float cu[kPrevSeg];
-  uint32_t kb[kPrevSeg / 2];  // bf16 state: k_j[lane] of this thread's path entries, in pairs
+  uint32_t kb[kPrevSeg / 2];  // k_j[lane] of this thread's path entries, in pairs
 #pragma unroll
   for (int j = 0; j < kPrevSeg; ++j) cu[j] = 0.f;
 #pragma unroll
   for (int j = 0; j < kPrevSeg / 2; ++j) kb[j] = 0u;
-  // bf16 state: this thread's part of a 16-entry path segment starting at
+  // The fused commit: this thread's part of a 16-entry path segment starting at
   // seg, entries seg + 8wg .. seg + 8wg + 7: c_j u_j[lane] (row `lane` of the
   // update's left operand) and k_j[lane] (row `lane` of its right operand),
   // zero past the path's end; all loads issued before any result is used.
   auto stage_tc = [&](int seg) {
-    if constexpr (kTcUpd) {
+    if constexpr (FUSED) {
       const unsigned short* kg = reinterpret_cast<const unsigned short*>(prev.k);
       uint32_t kh[kPrevSeg];
       float uv[kPrevSeg];
@@ -544,44 +554,6 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
       }
 #pragma unroll
       for (int j = 0; j < kPrevSeg / 2; ++j) kb[j] = kh[2 * j] | (kh[2 * j + 1] << 16);
-    }
-  };
-  auto stage_prev = [&](int seg) {
-    if constexpr (FUSED) {
-      // every load of the pass is issued before any of its results is used
-      // (a shared-memory store of a loaded value would hold back the loads
-      // behind it by a full memory round trip)
-      constexpr int kPer = kPrevSeg * (kDim / 2) / kThreads;  // k words per thread
-      const int ns = min(kPrevSeg, pv.len - seg);
-      const uint32_t* kg = reinterpret_cast<const uint32_t*>(prev.k);
-      uint32_t kw[kPer];
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = t + i * kThreads;
-        const int j = e / (kDim / 2), w = e - j * (kDim / 2);
-        kw[i] = 0u;
-        if (j < ns) {
-          const int64_t row = (static_cast<int64_t>(pv.tok0) + pv.path[seg + j]) * H + h;
-          kw[i] = __ldg(kg + row * (kDim / 2) + w);
-        }
-      }
-      float uv[kPrevSeg];
-#pragma unroll
-      for (int j = 0; j < kPrevSeg; ++j) {
-        uv[j] = 0.f;
-        if (j < ns) {
-          const int64_t row = (static_cast<int64_t>(pv.tok0) + pv.path[seg + j]) * H + h;
-          uv[j] = __ldg(prev.U + row * kDim + lane);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = t + i * kThreads;
-        const int j = e / (kDim / 2), w = e - j * (kDim / 2);
-        if (j < ns) reinterpret_cast<uint32_t*>(&pv.k[j][0])[w] = kw[i];
-      }
-#pragma unroll
-      for (int j = 0; j < kPrevSeg; ++j) cu[j] = (j < ns) ? pv.c[seg + j] * uv[j] : 0.f;
     }
   };
   if constexpr (FUSED) {
@@ -606,10 +578,7 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
         pv.gamma_a = c;
       }
       __syncthreads();
-      if (!bad_prev) {
-        if constexpr (kTcUpd) stage_tc(0);
-        else stage_prev(0);
-      }
+      if (!bad_prev) stage_tc(0);
       __syncthreads();
     }
   }
@@ -651,13 +620,12 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
   if constexpr (FUSED) {
     // S_a = gamma_a S0 + sum_j c_j u_j k_j^T on this thread's own part of row
     // `lane` (columns 64wg .. 64wg+63: chunks 2wg, 2wg+1 of an fp32 tile,
-    // chunk wg of a bf16 one), 32 columns at a time held in f32 registers
-    // across every staged path segment and stored back once (rounded once
-    // for a bf16 state); the k rows are read as 16-byte broadcasts.
+    // chunk wg of a bf16 one), written back once (rounded once for a bf16
+    // state).
     if (commit_now && !__syncthreads_or(fail)) {
       const float ga = pv.gamma_a;
       const int len = pv.len;
-      if constexpr (kTcUpd) {
+      {
         // The update sum_j c_j u_j k_j^T on the tensor cores: per 16-entry
         // path segment, D += [c u]_hi K_p^T + [c u]_lo K_p^T (M = N = 128,
         // K = 16) into TMEM columns 0..127, both operands in one 128-row tile
@@ -665,7 +633,8 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
         // the _lo parts, slot 2 k_j[c]; thread (wg, lane) writes entries
         // 8wg..8wg+7 of row `lane` of each.  Then S_a = gamma_a S0 + D row by
         // row (rounded once for a bf16 state).
-        unsigned char* opt = SB ? s0 + 2 * kS0ChunkBytes : kq;
+        unsigned char* opt = SB ? s0 + 2 * kS0ChunkBytes
+                              : (NPM >= 32 ? kq : base + TcSmem<NPM, FUSED, SB>::kUpdOff);
         unsigned char* orow = opt + lane * 128;
         const int r7 = lane & 7;
         const int nseg = (len + 2 * kPrevSeg - 1) / (2 * kPrevSeg);
@@ -779,74 +748,6 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
           }
           stored = true;
         }
-      } else {
-        const int nseg = (len + kPrevSeg - 1) / kPrevSeg;
-        int staged = 0;
-        for (int hb = 0; hb < 2; ++hb) {
-          const int col0 = 64 * wg + 32 * hb;
-          float x[32];
-          {
-            const unsigned char* row = s0 + (2 * wg + hb) * kS0ChunkBytes + lane * 128;
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              const float4 v = *reinterpret_cast<const float4*>(row + ((g ^ (lane & 7)) << 4));
-              x[4 * g] = ga * v.x;
-              x[4 * g + 1] = ga * v.y;
-              x[4 * g + 2] = ga * v.z;
-              x[4 * g + 3] = ga * v.w;
-            }
-          }
-          for (int sg = 0; sg < nseg; ++sg) {
-            if (sg != staged) {
-              __syncthreads();
-              stage_prev(sg * kPrevSeg);
-              __syncthreads();
-              staged = sg;
-            }
-            const int ns = min(kPrevSeg, len - sg * kPrevSeg);
-#pragma unroll
-            for (int j = 0; j < kPrevSeg; ++j) {
-              if (j < ns) {
-                const float u = cu[j];
-                const uint4* kr = reinterpret_cast<const uint4*>(&pv.k[j][col0]);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const uint4 raw = kr[q];
-                  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    x[8 * q + 2 * i] = fmaf(u, __uint_as_float(w[i] << 16), x[8 * q + 2 * i]);
-                    x[8 * q + 2 * i + 1] = fmaf(u, __uint_as_float(w[i] & 0xFFFF0000u), x[8 * q + 2 * i + 1]);
-                  }
-                }
-              }
-            }
-          }
-          {
-            unsigned char* row = s0 + (2 * wg + hb) * kS0ChunkBytes + lane * 128;
-#pragma unroll
-            for (int g = 0; g < 8; ++g)
-              *reinterpret_cast<float4*>(row + ((g ^ (lane & 7)) << 4)) =
-                  make_float4(x[4 * g], x[4 * g + 1], x[4 * g + 2], x[4 * g + 3]);
-            // an fp32 chunk goes back to the pool by a bulk tensor store while
-            // the next one is computed (the tile layout in shared memory is
-            // the one the loads produced; per-thread stores straight from the
-            // registers, 32 rows per warp instruction, were measured slower)
-            fence_proxy_async_smem();
-            if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
-            if (lane == 0) {
-              tma_store_2d(&map_s0, s0 + (2 * wg + hb) * kS0ChunkBytes, 32 * (2 * wg + hb),
-                           (ts.slot * H + h) * kDim);
-              bulk_commit_group();
-            }
-          }
-        }
-        if (!issued) {
-          // nothing to convert: the stores still finish reading before the CTA ends
-          if (lane == 0) bulk_wait_group_read0();
-          if (wg) named_bar_sync<2, 128>(); else named_bar_sync<1, 128>();
-        }
-        stored = true;
       }
     }
   }
@@ -953,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || 
     finished = true;
     if (!waits) return;
     // No async copy or MMA may still target this CTA's memory at exit.
-    if constexpr (kTcUpd) {
+    if constexpr (FUSED) {
       if (reb_pending >= 0) mbar_wait(&bars[8], reb_pending);
     }
     if (have_s0)
@@ -1169,7 +1070,7 @@ cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, const PrevRou
   const cudaError_t attr = once_per_device(attr_done, [] {
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel<NPM, FUSED, SB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(TcCfg<NPM>::kDynSmem));
+                                         static_cast<int>(TcSmem<NPM, FUSED, SB>::kBytes));
     // the whole unified L1/shared array as shared memory, so that the
     // resident CTAs (two, three for 16-node trees) fit
     if (e == cudaSuccess)
@@ -1180,7 +1081,7 @@ cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, const PrevRou
   });
   if (attr != cudaSuccess) return attr;
   const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
-  verify_tc_kernel<NPM, FUSED, SB><<<grid, kThreads, TcCfg<NPM>::kDynSmem, stream>>>(
+  verify_tc_kernel<NPM, FUSED, SB><<<grid, kThreads, TcSmem<NPM, FUSED, SB>::kBytes, stream>>>(
       m.s0, m.k, m.q, m.k32, m.q32, b, prev);
   return cudaGetLastError();
 }

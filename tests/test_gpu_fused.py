@@ -14,15 +14,15 @@ from tests.gpu_helpers import np32
 pytestmark = pytest.mark.gpu
 
 
-def rounds(prev_trees, next_trees, accepted, H=4, dk=128, dv=128, qkv="bf16", seed=41):
+def rounds(prev_trees, next_trees, accepted, H=4, dk=128, dv=128, qkv="bf16", seed=41, max_nodes=64):
     """Two rounds over the same requests sharing one state pool."""
     R = len(prev_trees)
     assert len(next_trees) == R
     prev = wl.assemble([np.asarray(t, np.int32) for t in prev_trees], np.asarray(accepted, np.int32),
-                       H, dk, dv, qkv, 0.05, (0.9, 0.999), ("sigmoid",), seed=seed, max_nodes=64,
+                       H, dk, dv, qkv, 0.05, (0.9, 0.999), ("sigmoid",), seed=seed, max_nodes=max_nodes,
                        extra_slots=3).to("cuda")
     nxt = wl.assemble([np.asarray(t, np.int32) for t in next_trees], np.full(R, -1, np.int32),
-                      H, dk, dv, qkv, 0.05, (0.9, 0.999), ("sigmoid",), seed=seed + 1, max_nodes=64,
+                      H, dk, dv, qkv, 0.05, (0.9, 0.999), ("sigmoid",), seed=seed + 1, max_nodes=max_nodes,
                       extra_slots=3).to("cuda")
     nxt.state = prev.state
     nxt.state_slot = prev.state_slot
@@ -103,6 +103,23 @@ def test_fused_matches_oracle_mixed(cuda_lib):
     prev, nxt = rounds(prev_trees, next_trees, accepted)
     tp, tn, S0_pool = run_fused(prev, nxt)
     assert not tn.status.any(), tn.status.tolist()
+    check(prev, nxt, tn, S0_pool, range(len(prev_trees)))
+
+
+@pytest.mark.parametrize("max_nodes", [16, 32])
+def test_fused_small_buckets(cuda_lib, max_nodes):
+    """The 16- and 32-node capacity buckets (the update's operand tile after
+    the lists, and in the K/Q region whose boxes wait for it): accepted paths
+    of one and two 16-entry segments (a chain as long as the capacity), a
+    commit of the root only, a request without commit, an empty next tree."""
+    rng = np.random.default_rng(200 + max_nodes)
+    prev_trees = [random_tree(rng, n) for n in (max_nodes // 2, 3, max_nodes - 1, 1)]
+    prev_trees.append(wl.chain_parents(max_nodes))
+    next_trees = [random_tree(rng, n) for n in (max_nodes, 5, 0, max_nodes // 2, 2)]
+    accepted = [max_nodes // 2 - 1, -1, max_nodes - 2, 0, max_nodes - 1]
+    prev, nxt = rounds(prev_trees, next_trees, accepted, H=3, seed=31, max_nodes=max_nodes)
+    tp, tn, S0_pool = run_fused(prev, nxt)
+    assert not tn.status.any()
     check(prev, nxt, tn, S0_pool, range(len(prev_trees)))
 
 
