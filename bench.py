@@ -827,8 +827,16 @@ def study_configs(args, local, pool):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     peak, peak_kind = read_peaks()
-    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 2x the 129 MB L2
-    flush = flush_buf.zero_
+    # L2 flush before each timed launch: 256 MB written (twice the 129 MB L2),
+    # then another 256 MB buffer read, so that the launch starts from a cold
+    # L2 holding no dirty lines (otherwise the write-back of the flush's own
+    # writes, up to the whole L2, would fall inside the timed launch)
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        flush_r.sum()
     g = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
     specs = [("chain", wl.CONFIGS["chain"], 32),
              ("binary", wl.CONFIGS["binary"], 16),
@@ -876,7 +884,7 @@ def study_configs(args, local, pool):
                 "fused": {"ms": f_ms, "algorithmic_bytes": fb, "gbs": g(fb, f_ms),
                           "frac": g(fb, f_ms) / peak,
                           "vs_separate": (v_ms + c_ms) / f_ms},
-                "l2": "flushed (256 MB written) before every timed launch"}
+                "l2": "flushed before every timed launch: 256 MB written, then 256 MB of another buffer read (cold L2, no dirty lines)"}
         if not args.no_storeall:
             o = torch.empty_like(tv.o)
             sv, sc, sbytes, nch = storeall_chunked(w, o, stream)

@@ -184,9 +184,16 @@ treewy_status treewy_verify(const treewy_batch* batch, cudaStream_t stream) {
   treewy_status st = validate(batch, true, true, true);
   if (st != TREEWY_OK || batch->R == 0) return st;
   cudaError_t err;
-  // (a batch of empty trees, T = 0, goes to the CUDA-core kernel: there are
-  // no rows to map, and it still checks node_offset and the slots)
-  if (use_tensor_cores(batch) && batch->T > 0) {
+  // Trees of at most kSmallTreeNodes nodes are verified by warp-level MMAs
+  // straight from the state tile, larger ones by the tcgen05 kernel.  (A batch
+  // of empty trees, T = 0, goes to the portable kernel: there are no rows to
+  // map, and it still checks node_offset and the slots.)
+  if (use_tensor_cores(batch) && batch->T > 0 && batch->max_nodes <= treewy::kSmallTreeNodes) {
+    CUtensorMap map;
+    st = make_state_map(batch, &map);
+    if (st != TREEWY_OK) return st;
+    err = treewy::launch_verify_small(*batch, map, stream);
+  } else if (use_tensor_cores(batch) && batch->T > 0) {
     treewy::VerifyMaps maps;
     st = make_maps(batch, &maps);
     if (st != TREEWY_OK) return st;
@@ -224,7 +231,10 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
   if (!prev->U && prev->T > 0) return fail(TREEWY_ERR_INVALID_ARG, "prev->U is NULL");
   if (!prev_accepted) return fail(TREEWY_ERR_INVALID_ARG, "prev_accepted is NULL");
   cudaError_t err;
-  if (use_tensor_cores(next) && next->T > 0 && prev->qkv_dtype == TREEWY_DTYPE_BF16) {
+  // (trees of at most kSmallTreeNodes nodes take the two calls below: the
+  // small-tree verification has no fused form)
+  if (use_tensor_cores(next) && next->T > 0 && prev->qkv_dtype == TREEWY_DTYPE_BF16 &&
+      next->max_nodes > treewy::kSmallTreeNodes) {
     treewy::VerifyMaps maps;
     st = make_maps(next, &maps);
     if (st != TREEWY_OK) return st;

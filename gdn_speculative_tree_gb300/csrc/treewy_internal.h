@@ -56,6 +56,15 @@ struct PrevRound {
   int32_t active;  // 0: plain verification
 };
 
+// Batches whose trees have at most this many nodes (max_nodes) are verified
+// by the small-tree kernel (verify_small.cu: warp-level MMAs straight from
+// the state tile) when dk = dv = 128 and q/k/v are bf16; larger ones by the
+// tcgen05 kernel.
+constexpr int kSmallTreeNodes = 8;
+// state_map: the state pool as VerifyMaps::s0.
+cudaError_t launch_verify_small(const treewy_batch& b, const CUtensorMap& state_map,
+                                cudaStream_t stream);
+
 // npm: padded tree capacity (16, 32 or 64).
 size_t verify_tc_smem(int npm);
 cudaError_t launch_verify_tc(const treewy_batch& b, const VerifyMaps& maps, int npm,

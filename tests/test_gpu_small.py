@@ -1,0 +1,273 @@
+"""GPU parity of the small-tree verification (batches whose trees have at most
+8 nodes: the warp-MMA kernel for dk = dv = 128 with bf16 q/k/v; 4-node and
+8-node capacities) against the
+oracle on the same seeded inputs: every size from 1 to 8 in chain, star,
+forest and random shapes, ragged batches with empty trees, gates at the ends
+of their range, a bf16 state pool, the commit-into-verify call, device-side
+errors, CUDA-graph replay, and agreement with the tensor-core kernel on the
+same inputs.  Tolerances as in gpu_helpers (o, U: 2e-3 of the largest
+reference value; committed state 1e-3; gamma 1e-5 relative).
+"""
+import types
+
+import numpy as np
+import pytest
+import torch
+
+from gdn_speculative_tree_gb300 import binding
+from gdn_speculative_tree_gb300 import workloads as wl
+from oracle import gdn_tree_oracle as orc
+from tests.gpu_helpers import (CudaRun, FLT_MIN, G_TOL, O_TOL, U_TOL, assert_within, compare, np32,
+                               oracle_request)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = 8  # node capacity of the small-tree kernel
+
+
+def custom(trees, accepted, seed=101, H=3, alpha=(0.9, 0.999), beta=("sigmoid",), max_nodes=None,
+           extra_slots=2, state_dtype="f32"):
+    w = wl.assemble([np.asarray(t, np.int32) for t in trees], np.asarray(accepted, np.int32), H, 128,
+                    128, "bf16", 0.05, alpha, beta, seed=seed, max_nodes=max_nodes,
+                    extra_slots=extra_slots, state_dtype=state_dtype)
+    return w.to("cuda")
+
+
+def random_tree(rng, n):
+    return np.array([-1] + [int(rng.integers(-1, i)) for i in range(1, n)], np.int32) if n else \
+        np.zeros(0, np.int32)
+
+
+def shapes(cap=SMALL):
+    """Chains, stars (every node a child of the root), forests (every node a
+    root) and two random trees of every size 1..cap."""
+    rng = np.random.default_rng(8 + cap)
+    trees = []
+    for n in range(1, cap + 1):
+        trees.append(wl.chain_parents(n))
+        trees.append(np.array([-1] + [0] * (n - 1), np.int32))
+        trees.append(np.full(n, -1, np.int32))
+        trees.append(random_tree(rng, n))
+        trees.append(random_tree(rng, n))
+    acc = [int(rng.integers(-1, len(t))) for t in trees]
+    return trees, acc
+
+
+@pytest.mark.parametrize("cap", [4, SMALL])
+def test_small_every_size_and_shape(cuda_lib, cap):
+    """Both capacities: up to 4 nodes (keys and queries in one 8-wide tile) and
+    up to 8 (two tiles)."""
+    trees, acc = shapes(cap)
+    w = custom(trees, acc)
+    assert w.max_nodes == cap
+    run = CudaRun(w)
+    assert not run.status.any()
+    assert_within(compare(w, run, range(w.R)), f"small shapes, capacity {cap}")
+
+
+@pytest.mark.parametrize("sizes,H", [([0, 3, 0, 8, 1, 0, 5], 5), ([4] * 7 + [0], 1), ([1, 1, 2, 0], 7)])
+def test_small_ragged_with_empty_trees(cuda_lib, sizes, H):
+    rng = np.random.default_rng(sum(sizes) + H)
+    trees = [random_tree(rng, n) for n in sizes]
+    acc = [len(t) - 1 for t in trees]
+    w = custom(trees, acc, H=H, max_nodes=SMALL)
+    run = CudaRun(w)
+    assert not run.status.any()
+    assert_within(compare(w, run, range(w.R)), f"ragged {sizes}")
+
+
+@pytest.mark.parametrize("alpha,beta", [((1.0, 1.0), ("const", 1.0)),
+                                        ((0.9, 0.999), ("const", 0.0)),
+                                        ((0.01, 0.05), ("uniform", 0.05, 0.95)),
+                                        ((0.999999, 0.9999999), ("uniform", 0.9999, 0.99999))])
+@pytest.mark.parametrize("cap", [4, SMALL])
+def test_small_gate_edges(cuda_lib, alpha, beta, cap):
+    trees, acc = shapes(cap)
+    w = custom(trees, acc, alpha=alpha, beta=beta, seed=37)
+    run = CudaRun(w)
+    assert not run.status.any()
+    assert_within(compare(w, run, range(w.R)), f"gates {alpha} {beta}")
+
+
+def test_small_agrees_with_tensor_cores(cuda_lib):
+    """The same batch through the small-tree kernel (max_nodes 8) and the
+    tcgen05 kernel (max_nodes 16): both within tolerance of the oracle, and of
+    each other."""
+    trees, acc = shapes()
+    w_small = custom(trees, acc, seed=5)
+    w_tc = custom(trees, acc, seed=5)
+    small = CudaRun(w_small)
+    tc = CudaRun(w_tc, max_nodes=16)
+    assert not small.status.any() and not tc.status.any()
+    assert_within(compare(w_small, small, range(w_small.R)), "small kernel")
+    assert_within(compare(w_tc, tc, range(w_tc.R)), "tensor-core kernel")
+    scale = float(np.abs(tc.o).max())
+    assert float(np.abs(small.o - tc.o).max()) <= 2 * O_TOL * scale
+    assert float(np.abs(small.U - tc.U).max()) <= 2 * U_TOL * float(np.abs(tc.U).max())
+    assert np.array_equal(small.gamma, tc.gamma)  # the same products of alpha in the same order
+
+
+def test_small_deterministic(cuda_lib):
+    trees, acc = shapes()
+    w = custom(trees, acc)
+    tv = binding.TreeVerifier(w)
+    tv.verify()
+    o1, u1 = tv.o.clone(), tv.U.clone()
+    tv.verify()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, tv.o) and torch.equal(u1, tv.U)
+
+
+@pytest.mark.parametrize("cap", [4, SMALL])
+def test_small_bf16_state(cuda_lib, cap):
+    """A bf16 state pool: verification reads the bf16 S0 exactly (o and U to
+    the fp32 tolerances), the commit rounds S_a once to bf16:
+    |S_gpu - S_ref| <= 2^-8 |S_ref| + 1e-3 max|S_ref| (8 significant bits,
+    round to nearest, plus the fp32 bound before the rounding)."""
+    trees, acc = shapes(cap)
+    w = custom(trees, acc, seed=71, state_dtype="bf16")
+    run = CudaRun(w, flags=binding.FLAG_STATE_BF16)
+    assert not run.status.any()
+    slot = w.state_slot.cpu().numpy()
+    o_err = o_max = u_err = u_max = g_err = 0.0
+    for r in range(w.R):
+        lo, hi, S0, ref = oracle_request(w, r, run.S0_pool)
+        o_err = max(o_err, float(np.abs(run.o[lo:hi] - ref.o).max()))
+        o_max = max(o_max, float(np.abs(ref.o).max()))
+        u_err = max(u_err, float(np.abs(run.U[lo:hi] - ref.U).max()))
+        u_max = max(u_max, float(np.abs(ref.U).max()))
+        g_err = max(g_err, float((np.abs(run.gamma[lo:hi] - ref.gamma) /
+                                  np.maximum(ref.gamma, FLT_MIN)).max()))
+        S_ref = orc.commit_request(S0, ref, int(acc[r]))
+        S_gpu = np32(w.state[int(slot[r])]).astype(np.float64)
+        bound = 2.0 ** -8 * np.abs(S_ref) + 1e-3 * np.abs(S_ref).max()
+        assert np.all(np.abs(S_gpu - S_ref) <= bound), r
+    assert o_err <= O_TOL * o_max, (o_err, o_max)
+    assert u_err <= U_TOL * u_max, (u_err, u_max)
+    assert g_err <= G_TOL, g_err
+
+
+def test_small_bad_inputs_set_status_and_spare_others(cuda_lib):
+    rng = np.random.default_rng(13)
+    trees = [random_tree(rng, n) for n in (6, 7, 8, 5, 4, 7)]
+    trees[1][4] = 5                        # parent after child
+    trees[5][6] = 6                        # parent is the node itself
+    acc = [3, 2, 1, 5, 0, 1]               # request 3: accepted outside its 5-node tree
+    w = custom(trees, acc, max_nodes=SMALL, extra_slots=2)
+    slots = w.state_slot.clone()
+    slots[4] = -1                          # outside the pool
+    w.state_slot.copy_(slots)
+    tv = binding.TreeVerifier(w, max_nodes=7)  # request 2 (8 nodes) exceeds it
+    tv.o.fill_(float("nan"))
+    tv.U.fill_(float("nan"))
+    S_before = w.state.clone()
+    tv.verify()
+    tv.commit()
+    torch.cuda.synchronize()
+    st = tv.status.cpu().tolist()
+    assert st[0] == 0
+    assert st[1] & binding.STATUS_BAD_TREE
+    assert st[2] & binding.STATUS_TOO_MANY_NODES
+    assert st[3] == binding.STATUS_BAD_ACCEPTED
+    assert st[4] & binding.STATUS_BAD_SLOT
+    assert st[5] & binding.STATUS_BAD_TREE
+    node = w.node_offset.cpu().tolist()
+    for r in (1, 2, 4, 5):
+        assert torch.isnan(tv.o[node[r]:node[r + 1]]).all()
+        assert torch.isnan(tv.U[node[r]:node[r + 1]]).all()
+    for r in (1, 2, 3, 5):  # state untouched where the commit was refused
+        s = int(w.state_slot[r])
+        assert torch.equal(w.state[s], S_before[s])
+    for r in (0, 3):        # verified normally
+        lo, hi, S0, ref = oracle_request(w, r, S_before.cpu())
+        assert np.abs(np32(tv.o[lo:hi]) - ref.o).max() <= O_TOL * np.abs(ref.o).max()
+
+
+def two_rounds(prev_trees, next_trees, accepted, H=3, seed=43):
+    """Two rounds over the same requests sharing one state pool; the previous
+    round's trees may be larger than 8 nodes, the next round's are not."""
+    R = len(prev_trees)
+    prev = wl.assemble([np.asarray(t, np.int32) for t in prev_trees], np.asarray(accepted, np.int32),
+                       H, 128, 128, "bf16", 0.05, (0.9, 0.999), ("sigmoid",), seed=seed,
+                       extra_slots=3).to("cuda")
+    nxt = wl.assemble([np.asarray(t, np.int32) for t in next_trees], np.full(R, -1, np.int32),
+                      H, 128, 128, "bf16", 0.05, (0.9, 0.999), ("sigmoid",), seed=seed + 1,
+                      max_nodes=SMALL, extra_slots=3).to("cuda")
+    nxt.state = prev.state
+    nxt.state_slot = prev.state_slot
+    return prev, nxt
+
+
+def test_small_commit_verify_matches_oracle(cuda_lib):
+    """treewy_commit_verify whose next trees have at most 8 nodes (the commit
+    then the small-tree verification): the committed S_a and the next round's
+    o and U against the oracle run as commit-then-verify."""
+    rng = np.random.default_rng(17)
+    prev_trees = [random_tree(rng, n) for n in (40, 4, 64, 8, 1, 12)]
+    prev_trees[2] = wl.chain_parents(64)
+    next_trees = [random_tree(rng, n) for n in (4, 8, 0, 1, 6, 3)]
+    accepted = [39, -1, 63, 5, 0, 11]
+    prev, nxt = two_rounds(prev_trees, next_trees, accepted)
+    tp = binding.TreeVerifier(prev)
+    tp.verify()
+    torch.cuda.synchronize()
+    S0_pool = prev.state.cpu()
+    tn = binding.TreeVerifier(nxt)
+    binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
+    torch.cuda.synchronize()
+    assert not tn.status.any(), tn.status.tolist()
+    o, U = np32(tn.o), np32(tn.U)
+    pn, nn = prev.node_offset.cpu().numpy(), nxt.node_offset.cpu().numpy()
+    for r in range(len(prev_trees)):
+        slot = int(prev.state_slot[r])
+        S0 = np32(S0_pool[slot])
+        lo, hi = int(pn[r]), int(pn[r + 1])
+        ref_prev = orc.verify_request(S0, prev.parent[lo:hi].cpu().numpy(), np32(prev.q[lo:hi]),
+                                      np32(prev.k[lo:hi]), np32(prev.v[lo:hi]),
+                                      np32(prev.alpha[lo:hi]), np32(prev.beta[lo:hi]))
+        Sa = orc.commit_request(S0, ref_prev, int(accepted[r]))
+        assert np.abs(np32(prev.state[slot]) - Sa).max() <= 1e-3 * np.abs(Sa).max(), r
+        lo2, hi2 = int(nn[r]), int(nn[r + 1])
+        if hi2 == lo2:
+            continue
+        ref = orc.verify_request(Sa, nxt.parent[lo2:hi2].cpu().numpy(), np32(nxt.q[lo2:hi2]),
+                                 np32(nxt.k[lo2:hi2]), np32(nxt.v[lo2:hi2]), np32(nxt.alpha[lo2:hi2]),
+                                 np32(nxt.beta[lo2:hi2]))
+        assert np.abs(o[lo2:hi2] - ref.o).max() <= O_TOL * np.abs(ref.o).max(), r
+        assert np.abs(U[lo2:hi2] - ref.U).max() <= U_TOL * np.abs(ref.U).max(), r
+
+
+def test_small_graph_replay_matches_eager(cuda_lib):
+    """The chain workload's verify + commit captured in a CUDA graph and
+    replayed: the oracle's results within the tolerances, and the eager
+    launches' bit for bit."""
+    cfg = wl.CONFIGS["chain"]
+    w_eager = wl.generate(cfg, R=24).to("cuda")
+    run = CudaRun(w_eager)
+    w = wl.generate(cfg, R=24).to("cuda")
+    assert w.max_nodes <= SMALL
+    S0 = w.state.clone()
+    tv = binding.TreeVerifier(w)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        tv.verify(s)
+        w.state.copy_(S0)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tv.verify()
+        tv.commit()
+    w.state.copy_(S0)
+    tv.o.fill_(float("nan"))
+    tv.U.fill_(float("nan"))
+    tv.gamma.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert not tv.status.any()
+    replay = types.SimpleNamespace(o=np32(tv.o), U=np32(tv.U), gamma=np32(tv.gamma),
+                                   S0_pool=S0.cpu(), S_after=w.state)
+    assert_within(compare(w, replay, range(w.R)), "chain graph replay")
+    assert torch.equal(tv.o.cpu(), torch.from_numpy(run.o))
+    assert torch.equal(w.state.cpu(), run.S_after.cpu())
