@@ -192,7 +192,7 @@ treewy_status treewy_verify(const treewy_batch* batch, cudaStream_t stream) {
     CUtensorMap map;
     st = make_state_map(batch, &map);
     if (st != TREEWY_OK) return st;
-    err = treewy::launch_verify_small(*batch, map, stream);
+    err = treewy::launch_verify_small(*batch, map, nullptr, stream);
   } else if (use_tensor_cores(batch) && batch->T > 0) {
     treewy::VerifyMaps maps;
     st = make_maps(batch, &maps);
@@ -231,13 +231,15 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
   if (!prev->U && prev->T > 0) return fail(TREEWY_ERR_INVALID_ARG, "prev->U is NULL");
   if (!prev_accepted) return fail(TREEWY_ERR_INVALID_ARG, "prev_accepted is NULL");
   cudaError_t err;
-  // (trees of at most kSmallTreeNodes nodes take the two calls below: the
-  // small-tree verification has no fused form)
+  // The small-tree kernel applies an accepted path 8 entries per pass over
+  // the state tile; a bf16 pool is rounded at the end of each pass, so it
+  // takes the fused form only while every path fits one pass (S_a rounded
+  // once, as the separate commit does).
+  const bool small = next->max_nodes <= treewy::kSmallTreeNodes;
+  const bool small_fused_ok =
+      !(next->flags & TREEWY_FLAG_STATE_BF16) || prev->max_nodes <= treewy::kSmallTreeNodes;
   if (use_tensor_cores(next) && next->T > 0 && prev->qkv_dtype == TREEWY_DTYPE_BF16 &&
-      next->max_nodes > treewy::kSmallTreeNodes) {
-    treewy::VerifyMaps maps;
-    st = make_maps(next, &maps);
-    if (st != TREEWY_OK) return st;
+      (!small || small_fused_ok)) {
     treewy::PrevRound pr;
     pr.node_offset = prev->node_offset;
     pr.parent = prev->parent;
@@ -248,7 +250,17 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
     pr.T = prev->T;
     pr.max_nodes = prev->max_nodes;
     pr.active = 1;
-    err = treewy::launch_commit_verify_tc(*next, pr, maps, next->max_nodes, stream);
+    if (small) {
+      CUtensorMap map;
+      st = make_state_map(next, &map);
+      if (st != TREEWY_OK) return st;
+      err = treewy::launch_verify_small(*next, map, &pr, stream);
+    } else {
+      treewy::VerifyMaps maps;
+      st = make_maps(next, &maps);
+      if (st != TREEWY_OK) return st;
+      err = treewy::launch_commit_verify_tc(*next, pr, maps, next->max_nodes, stream);
+    }
     return err == cudaSuccess ? TREEWY_OK : cuda_fail(err, "treewy_commit_verify launch");
   }
   // other shapes: the two kernels back to back on the same stream, the

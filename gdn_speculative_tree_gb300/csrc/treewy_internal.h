@@ -61,9 +61,11 @@ struct PrevRound {
 // the state tile) when dk = dv = 128 and q/k/v are bf16; larger ones by the
 // tcgen05 kernel.
 constexpr int kSmallTreeNodes = 8;
-// state_map: the state pool as VerifyMaps::s0.
+// state_map: the state pool as VerifyMaps::s0; prev != nullptr fuses the
+// previous round's commit in front (PrevRound below).
+struct PrevRound;
 cudaError_t launch_verify_small(const treewy_batch& b, const CUtensorMap& state_map,
-                                cudaStream_t stream);
+                                const PrevRound* prev, cudaStream_t stream);
 
 // npm: padded tree capacity (16, 32 or 64).
 size_t verify_tc_smem(int npm);

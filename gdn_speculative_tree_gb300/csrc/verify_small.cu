@@ -51,20 +51,42 @@ struct SmallTree {
   float M[8][8];        // M[n][i], zero unless i is n or an ancestor of n
 };
 
+// The previous round's tree and the accepted node's root path, for the
+// commit fused in front of the verification.
+struct SmallPrev {
+  int parent[kMaxNodes];
+  float alpha[kMaxNodes];
+  float c[kMaxNodes];        // gamma_a / gamma_{path j} as products of alpha
+  uint8_t path[kMaxNodes];   // accepted node, its parent, ... (root last)
+  float w[8];                // previous trees of at most 8 nodes: c_j by node
+  int onpath;                // ... and the nodes on the accepted path (bit j)
+  int len;
+  float gamma_a;
+};
+constexpr int kSeg = 8;      // path entries applied per pass over the tile
+static_assert(kSeg == kSmallTreeNodes, "a bf16 pool's fused commit needs one pass per path");
+
 // NT n8-tiles of vectors: NT = 1 holds keys 0..3 in slots 0..3 and queries
 // 0..3 in slots 4..7 (trees of up to 4 nodes); NT = 2 holds keys 0..7 in
 // slots 0..7 and queries in 8..15.  The K/Q region always has 16 rows (the
 // Gram's M = 16 operand), unused ones zero.  Dynamic shared memory: alignment
 // slack, the state tile (4 boxes of 32 fp32 or 2 of 64 bf16 columns, 128B
-// swizzle), the 16 K/Q rows, the per-tree data.
-template <bool SB, int NT>
+// swizzle), the 16 K/Q rows, the per-tree data; with the commit fused in,
+// the previous tree and kSeg bf16 key rows of the accepted path.
+template <bool SB, int NT, bool FUSED>
 struct SmallCfg {
   static constexpr int kMaxN = 4 * NT;  // node capacity
   static constexpr int kQ0 = kMaxN;     // slot of query 0
   static constexpr uint32_t kS0Bytes = SB ? 2u * kSChunk : 4u * kSChunk;
   static constexpr uint32_t kKQOff = kS0Bytes;
   static constexpr uint32_t kTreeOff = kKQOff + 16u * kKQStride;
-  static constexpr uint32_t kDynSmem = 1024u + kTreeOff + static_cast<uint32_t>(sizeof(SmallTree));
+  static constexpr uint32_t kPrevOff = (kTreeOff + static_cast<uint32_t>(sizeof(SmallTree)) + 15u) & ~15u;
+  static constexpr uint32_t kPathKOff = (kPrevOff + static_cast<uint32_t>(sizeof(SmallPrev)) + 15u) & ~15u;
+  static constexpr uint32_t kEnd = FUSED ? kPathKOff + kSeg * kKQStride
+                                         : kTreeOff + static_cast<uint32_t>(sizeof(SmallTree));
+  static constexpr uint32_t kDynSmem = 1024u + kEnd;
+  // three CTAs per SM: 228 KB of shared memory, 1 KB of it reserved per CTA
+  static_assert(3u * (kDynSmem + 1024u) <= 228u * 1024u, "three CTAs per SM");
 };
 
 // D += A B for one m16n8k16 bf16 tile with fp32 accumulation.  Fragments
@@ -89,16 +111,26 @@ __device__ __forceinline__ uint32_t lds32(const unsigned char* p) {
 // 16w..16w+15; lane (g, q) = (lane / 4, lane % 4) holds rows 16w+g and
 // 16w+g+8 of the MMA tiles, and for the solve takes row 16w+g (q < 2) or
 // 16w+g+8 (q >= 2), writing U (q even) or o (q odd).
-template <bool SB, int NT>
+//
+// FUSED: the previous round's commit first, S_a = gamma_a S0 +
+// sum_{j in path(a)} c_j u_j k_j^T with c_j = gamma_a / gamma_j (TreeWY
+// paper §3 "Reconstruct on commit"), applied to the tile rows as the first
+// products read them and written back to the pool once; the verification
+// then runs from S_a.  Each half runs exactly when its separate call would:
+// a refused commit leaves the state alone, a bad next tree still commits.
+template <bool SB, int NT, bool FUSED>
 __global__ void __launch_bounds__(kSThreads, 3)
-    verify_small_kernel(const __grid_constant__ CUtensorMap map_s0, const treewy_batch b) {
-  using C = SmallCfg<SB, NT>;
+    verify_small_kernel(const __grid_constant__ CUtensorMap map_s0, const treewy_batch b,
+                        const PrevRound prev) {
+  using C = SmallCfg<SB, NT, FUSED>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
   unsigned char* s0 = base;
   unsigned char* kqs = base + C::kKQOff;
   SmallTree& ts = *reinterpret_cast<SmallTree*>(base + C::kTreeOff);
+  SmallPrev& pv = *reinterpret_cast<SmallPrev*>(base + C::kPrevOff);  // FUSED only
+  unsigned char* pathk = base + C::kPathKOff;                          // FUSED only
 
   const int H = b.H;
   const int r = blockIdx.x / H;
@@ -116,9 +148,26 @@ __global__ void __launch_bounds__(kSThreads, 3)
   int flags = 0;
   if (hi - lo < 0 || hi - lo > b.max_nodes) flags |= TREEWY_STATUS_TOO_MANY_NODES;
   else if (lo < 0 || static_cast<int64_t>(hi) > b.T) flags |= TREEWY_STATUS_BAD_TREE;
-  if (slot < 0 || static_cast<int64_t>(slot) >= b.num_slots) flags |= TREEWY_STATUS_BAD_SLOT;
+  const bool bad_slot = slot < 0 || static_cast<int64_t>(slot) >= b.num_slots;
+  if (bad_slot) flags |= TREEWY_STATUS_BAD_SLOT;
   const int N = flags ? 0 : hi - lo;  // at most C::kMaxN (the launcher's max_nodes bound)
   const bool issued = N > 0;
+  // the previous round's request: its errors refuse the commit only
+  int cflags = 0, commit_a = -1, plo = 0, pn = 0;
+  if constexpr (FUSED) {
+    const int pa = __ldg(prev.accepted + r);
+    plo = __ldg(prev.node_offset + r);
+    const int phi = __ldg(prev.node_offset + r + 1);
+    pn = phi - plo;
+    if (pa != -1) {
+      if (pn < 0 || pn > prev.max_nodes) cflags |= TREEWY_STATUS_TOO_MANY_NODES;
+      else if (plo < 0 || static_cast<int64_t>(phi) > prev.T) cflags |= TREEWY_STATUS_BAD_TREE;
+      if (pa < -1 || pa >= pn) cflags |= TREEWY_STATUS_BAD_ACCEPTED;
+      if (cflags || bad_slot) cflags |= TREEWY_STATUS_COMMIT_REFUSED;
+    }
+    commit_a = cflags ? -1 : pa;
+  }
+  const bool have_s0 = issued || commit_a >= 0;
 
   // this thread's 16 bytes of the K/Q rows: slot v = t / 16 (keys from slot
   // 0, queries from slot kQ0), zero where the slot holds no node
@@ -139,6 +188,39 @@ __global__ void __launch_bounds__(kSThreads, 3)
     al = __ldg(b.alpha + rw * H + h);
     be = __ldg(b.beta + rw * H + h);
   }
+  // node t of the previous tree
+  int pp = -1;
+  float pal = 0.f;
+  if (FUSED && commit_a >= 0 && t < pn) {
+    const int64_t rw = static_cast<int64_t>(plo) + t;
+    pp = __ldg(prev.parent + rw);
+    pal = __ldg(prev.alpha + rw * H + h);
+  }
+  // A previous tree of at most kSeg nodes: every node's U values in this
+  // lane's two state rows and (threads < 128) its key row are requested in
+  // the same round trip as the tree; the path walk then only weights them
+  // (c_j on the accepted path, 0 elsewhere), so S_a waits for no further
+  // memory round trip.
+  const int r0 = 16 * warp + g;  // this lane's state rows r0 and r0 + 8
+  const bool spec = FUSED && commit_a >= 0 && prev.max_nodes <= kSeg;
+  float cu0[kSeg], cu1[kSeg];    // c_j u_j of rows r0, r0 + 8
+#pragma unroll
+  for (int j = 0; j < kSeg; ++j) cu0[j] = cu1[j] = 0.f;
+  uint4 pkr = make_uint4(0u, 0u, 0u, 0u);
+  if (spec) {
+#pragma unroll
+    for (int j = 0; j < kSeg; ++j) {
+      if (j < pn) {
+        const float* ur = prev.U + ((static_cast<int64_t>(plo) + j) * H + h) * kSDim;
+        cu0[j] = __ldg(ur + r0);
+        cu1[j] = __ldg(ur + r0 + 8);
+      }
+    }
+    if (t < kSeg * 16 && (t >> 4) < pn) {
+      const uint4* kg4 = reinterpret_cast<const uint4*>(prev.k);
+      pkr = __ldg(kg4 + ((static_cast<int64_t>(plo) + (t >> 4)) * H + h) * (kSDim / 8) + (t & 15));
+    }
+  }
   // column `row` of every node's v, as bf16 pairs until the solve
   uint32_t vpk[C::kMaxN / 2];
   const unsigned short* vg = reinterpret_cast<const unsigned short*>(b.v);
@@ -153,7 +235,7 @@ __global__ void __launch_bounds__(kSThreads, 3)
   if (t == 0) {
     mbar_init(&ts.bar, 1);
     fence_mbarrier_init();
-    if (issued) {
+    if (have_s0) {
       const int y = (slot * H + h) * kSDim;
       mbar_arrive_expect_tx(&ts.bar, C::kS0Bytes);
 #pragma unroll
@@ -163,6 +245,7 @@ __global__ void __launch_bounds__(kSThreads, 3)
   }
 
   *reinterpret_cast<uint4*>(kqs + kv * kKQStride + (t & 15) * 16) = kraw;
+  if (spec && t < kSeg * 16) *reinterpret_cast<uint4*>(pathk + (t >> 4) * kKQStride + (t & 15) * 16) = pkr;
   if (t < 128) (t < 64 ? &ts.A[0][0] : &ts.M[0][0])[t & 63] = 0.f;
   bool bad = false;
   if (t < N) {
@@ -172,6 +255,41 @@ __global__ void __launch_bounds__(kSThreads, 3)
   }
   const bool bad_tree = __syncthreads_or(bad);
   const bool work = issued && !bad_tree;
+
+  // ---- the previous tree: parents checked, then (thread 0) the accepted
+  //      node's root path with the decay ratios c_j = gamma_a / gamma_j as
+  //      products of alpha (no division), published by the barrier after the
+  //      state tile's wait
+  bool bad_prev = false;
+  if constexpr (FUSED) {
+    if (commit_a >= 0) {
+      bool badp = false;
+      if (t < pn) {
+        badp = !(pp >= -1 && pp < t);
+        pv.parent[t] = pp;
+        pv.alpha[t] = pal;
+      }
+      bad_prev = __syncthreads_or(badp);
+      if (!bad_prev && t == 0) {
+        int len = 0, onpath = 0;
+        float c = 1.f;
+        for (int cur = commit_a; cur >= 0; cur = pv.parent[cur]) {
+          pv.path[len] = static_cast<uint8_t>(cur);
+          pv.c[len] = c;
+          if (spec) {
+            pv.w[cur] = c;
+            onpath |= 1 << cur;
+          }
+          c *= pv.alpha[cur];
+          ++len;
+        }
+        pv.len = len;
+        pv.onpath = onpath;
+        pv.gamma_a = c;
+      }
+    }
+  }
+  const bool commit_now = commit_a >= 0 && !bad_prev;
 
   if (work && warp == 0) {
     // ---- Gram: slot_m . slot_n for the 16 slots m and the 8 slots n of the
@@ -212,50 +330,146 @@ __global__ void __launch_bounds__(kSThreads, 3)
     }
   }
   int fail = 0;
-  if (issued && t == 0 && !mbar_wait(&ts.bar, 0)) fail = 1;
+  if (have_s0 && t == 0 && !mbar_wait(&ts.bar, 0)) fail = 1;
   fail = __syncthreads_or(fail);
   const bool go = work && !fail;
+  const bool commit_go = commit_now && !fail;
 
-  // ---- S0 [K;Q]^T, rows 16w..16w+15: per k-step of 16 state columns the A
-  //      fragment is read from the swizzled tile and split into hi + lo (fp32
-  //      state) or read as it is (bf16 state); one MMA per part and tile
+  // ---- passes over this warp's 16 tile rows, per k-step of 16 state
+  //      columns: the fused commit's update applied to the A fragment's
+  //      elements and written back to the tile, then the first products
+  //      S0 [K;Q]^T with the fragment split into hi + lo (fp32 state) or used
+  //      as it is (bf16 state), one MMA per part and tile.  A path longer
+  //      than kSeg entries takes one update-only pass per further kSeg.
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-  if (go) {
-    const int r0 = 16 * warp + g;  // and r0 + 8: the same swizzle phase
-    const int sw = r0 & 7;
-#pragma unroll 2
+  const int len = (FUSED && commit_go) ? pv.len : 0;
+  const int nseg = spec ? (commit_go ? 1 : 0) : (len + kSeg - 1) / kSeg;
+  const int npass = nseg > 0 ? nseg : (go ? 1 : 0);
+  const int sw = r0 & 7;  // rows r0 and r0 + 8: the same swizzle phase
+  for (int ps = 0; ps < npass; ++ps) {
+    const bool upd = ps < nseg;
+    const bool mma_pass = go && ps == npass - 1;
+    const int j0 = kSeg * ps;
+    int ne = 0;          // update entries of this pass
+    int use = ~0;        // ... of which those with bit j set apply
+    float ga = 1.f;
+    if constexpr (FUSED) {
+      if (upd && spec) {
+        // entries = the previous tree's nodes; those on the accepted path
+        // weighted by c_j, the others skipped (their rows never read)
+        use = pv.onpath;
+#pragma unroll
+        for (int j = 0; j < kSeg; ++j) {
+          cu0[j] = ((use >> j) & 1) ? cu0[j] * pv.w[j] : 0.f;
+          cu1[j] = ((use >> j) & 1) ? cu1[j] * pv.w[j] : 0.f;
+        }
+        ne = pn;
+        ga = pv.gamma_a;
+      } else if (upd) {
+        // c_j u_j of this lane's two rows, and (shared) the key rows k_j,
+        // for the path entries j0 .. j0 + kSeg - 1 (zero past the path)
+        ne = len - j0 < kSeg ? len - j0 : kSeg;
+        if (ps > 0) __syncthreads();  // the previous pass has read the key rows
+        if (t < kSeg * 16) {
+          const int j = t >> 4;
+          uint4 kr = make_uint4(0u, 0u, 0u, 0u);
+          if (j0 + j < len) {
+            const uint4* kg4 = reinterpret_cast<const uint4*>(prev.k);
+            kr = __ldg(kg4 + ((static_cast<int64_t>(plo) + pv.path[j0 + j]) * H + h) * (kSDim / 8) +
+                       (t & 15));
+          }
+          *reinterpret_cast<uint4*>(pathk + j * kKQStride + (t & 15) * 16) = kr;
+        }
+#pragma unroll
+        for (int j = 0; j < kSeg; ++j) {
+          cu0[j] = cu1[j] = 0.f;
+          if (j0 + j < len) {
+            const float* ur = prev.U + ((static_cast<int64_t>(plo) + pv.path[j0 + j]) * H + h) * kSDim;
+            cu0[j] = pv.c[j0 + j] * __ldg(ur + r0);
+            cu1[j] = pv.c[j0 + j] * __ldg(ur + r0 + 8);
+          }
+        }
+        if (ps == 0) ga = pv.gamma_a;
+        __syncthreads();
+      }
+    }
+#pragma unroll(FUSED ? 1 : 2)
     for (int ks = 0; ks < 8; ++ks) {
       uint32_t ah[4], al4[4];
-      if constexpr (!SB) {
-        // box ks / 2 holds columns 32 (ks / 2) .. + 31, four per 16-byte granule
-        const unsigned char* box = s0 + (ks >> 1) * kSChunk;
 #pragma unroll
-        for (int f = 0; f < 4; ++f) {
-          const int col = 16 * (ks & 1) + 2 * q + ((f & 2) ? 8 : 0);
-          const int rr = r0 + ((f & 1) ? 8 : 0);
-          const float2 x = *reinterpret_cast<const float2*>(box + rr * 128 + (((col >> 2) ^ sw) << 4) +
-                                                            (col & 3) * 4);
-          split_pair(x.x, x.y, ah[f], al4[f]);
+      for (int f = 0; f < 4; ++f) {
+        const int colg = 16 * ks + 2 * q + ((f & 2) ? 8 : 0);  // state column
+        const int rr = r0 + ((f & 1) ? 8 : 0);
+        // the element pair (rr, colg), (rr, colg + 1) in the swizzled tile:
+        // box colg / 32 (fp32) or colg / 64 (bf16), 16-byte granule in the row
+        unsigned char* ep = SB ? s0 + (colg >> 6) * kSChunk + rr * 128 +
+                                     ((((colg & 63) >> 3) ^ sw) << 4) + (colg & 7) * 2
+                               : s0 + (colg >> 5) * kSChunk + rr * 128 +
+                                     ((((colg & 31) >> 2) ^ sw) << 4) + (colg & 3) * 4;
+        float x0, x1;
+        uint32_t raw = 0u;
+        if constexpr (SB) {
+          raw = lds32(ep);
+          x0 = __uint_as_float(raw << 16);
+          x1 = __uint_as_float(raw & 0xFFFF0000u);
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(ep);
+          x0 = x.x;
+          x1 = x.y;
         }
-      } else {
-        // box ks / 4 holds columns 64 (ks / 4) .. + 63, eight per granule
-        const unsigned char* box = s0 + (ks >> 2) * kSChunk;
+        if constexpr (FUSED) {
+          if (upd) {
+            // S_a = gamma_a S0 + sum_j c_j u_j k_j^T on this pair
+            float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-        for (int f = 0; f < 4; ++f) {
-          const int col = 16 * (ks & 3) + 2 * q + ((f & 2) ? 8 : 0);
-          const int rr = r0 + ((f & 1) ? 8 : 0);
-          ah[f] = lds32(box + rr * 128 + (((col >> 3) ^ sw) << 4) + (col & 7) * 2);
+            for (int j = 0; j < kSeg; ++j) {
+              if (j < ne && ((use >> j) & 1)) {
+                const uint32_t kp = lds32(pathk + j * kKQStride + colg * 2);  // entry j < ne
+                const float cu = (f & 1) ? cu1[j] : cu0[j];
+                d0 = fmaf(cu, __uint_as_float(kp << 16), d0);
+                d1 = fmaf(cu, __uint_as_float(kp & 0xFFFF0000u), d1);
+              }
+            }
+            x0 = fmaf(ga, x0, d0);
+            x1 = fmaf(ga, x1, d1);
+            if constexpr (SB) {
+              const __nv_bfloat162 pr = __floats2bfloat162_rn(x0, x1);  // rounded once
+              raw = *reinterpret_cast<const uint32_t*>(&pr);
+              *reinterpret_cast<uint32_t*>(ep) = raw;
+            } else {
+              *reinterpret_cast<float2*>(ep) = make_float2(x0, x1);
+            }
+          }
+        }
+        if constexpr (SB) ah[f] = raw;
+        else split_pair(x0, x1, ah[f], al4[f]);
+      }
+      if (mma_pass) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const unsigned char* bp = kqs + (8 * nt + g) * kKQStride + (16 * ks + 2 * q) * 2;
+          const uint32_t b0 = lds32(bp), b1 = lds32(bp + 16);
+          mma16816(acc[nt], ah[0], ah[1], ah[2], ah[3], b0, b1);
+          if constexpr (!SB) mma16816(acc[nt], al4[0], al4[1], al4[2], al4[3], b0, b1);
         }
       }
+    }
+  }
+  // the committed state goes back to the pool once every row is updated
+  bool stored = false;
+  if constexpr (FUSED) {
+    if (commit_go) {
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (t == 0) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const unsigned char* bp = kqs + (8 * nt + g) * kKQStride + (16 * ks + 2 * q) * 2;
-        const uint32_t b0 = lds32(bp), b1 = lds32(bp + 16);
-        mma16816(acc[nt], ah[0], ah[1], ah[2], ah[3], b0, b1);
-        if constexpr (!SB) mma16816(acc[nt], al4[0], al4[1], al4[2], al4[3], b0, b1);
+        for (int c = 0; c < (SB ? 2 : 4); ++c)
+          tma_store_2d(&map_s0, s0 + c * kSChunk, (SB ? 64 : 32) * c, (slot * H + h) * kSDim);
+        bulk_commit_group();
       }
+      stored = true;
     }
   }
 
@@ -301,40 +515,57 @@ __global__ void __launch_bounds__(kSThreads, 3)
 
   if (t == 0) {
     int bits = fail ? kStatusTimeout : 0;
-    if (h == 0) bits |= flags | (issued && bad_tree ? TREEWY_STATUS_BAD_TREE : 0);
+    if (h == 0) bits |= flags | cflags | (issued && bad_tree ? TREEWY_STATUS_BAD_TREE : 0);
+    // the previous tree failed its checks, or a wait gave up before S_a was
+    // stored: that request's commit did not happen
+    if (bad_prev && h == 0) bits |= TREEWY_STATUS_BAD_TREE | TREEWY_STATUS_COMMIT_REFUSED;
+    if (fail && commit_now && !stored) bits |= TREEWY_STATUS_COMMIT_REFUSED;
     if (bits) atomicOr(b.status + r, bits);
     // no copy may still target this CTA's memory at exit
     if (fail) mbar_wait(&ts.bar, 0);
+    if (stored) bulk_wait_group_read0();
   }
 }
 
-template <bool SB, int NT>
-cudaError_t launch_small(const treewy_batch& b, const CUtensorMap& map_s0, cudaStream_t stream) {
+template <bool SB, int NT, bool FUSED>
+cudaError_t launch_small(const treewy_batch& b, const CUtensorMap& map_s0, const PrevRound& prev,
+                         cudaStream_t stream) {
+  using C = SmallCfg<SB, NT, FUSED>;
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t attr = once_per_device(attr_done, [] {
-    cudaError_t e = cudaFuncSetAttribute(verify_small_kernel<SB, NT>,
+    cudaError_t e = cudaFuncSetAttribute(verify_small_kernel<SB, NT, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SmallCfg<SB, NT>::kDynSmem));
+                                         static_cast<int>(C::kDynSmem));
     // the whole unified L1/shared array as shared memory: three CTAs per SM
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(verify_small_kernel<SB, NT>,
+      e = cudaFuncSetAttribute(verify_small_kernel<SB, NT, FUSED>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
     return e;
   });
   if (attr != cudaSuccess) return attr;
   const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
-  verify_small_kernel<SB, NT><<<grid, kSThreads, SmallCfg<SB, NT>::kDynSmem, stream>>>(map_s0, b);
+  verify_small_kernel<SB, NT, FUSED><<<grid, kSThreads, C::kDynSmem, stream>>>(map_s0, b, prev);
   return cudaGetLastError();
+}
+
+template <bool FUSED>
+cudaError_t launch_small_any(const treewy_batch& b, const CUtensorMap& map_s0, const PrevRound& prev,
+                             cudaStream_t stream) {
+  const bool sb = (b.flags & TREEWY_FLAG_STATE_BF16) != 0;
+  if (b.max_nodes <= 4)
+    return sb ? launch_small<true, 1, FUSED>(b, map_s0, prev, stream)
+              : launch_small<false, 1, FUSED>(b, map_s0, prev, stream);
+  return sb ? launch_small<true, 2, FUSED>(b, map_s0, prev, stream)
+            : launch_small<false, 2, FUSED>(b, map_s0, prev, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_verify_small(const treewy_batch& b, const CUtensorMap& map_s0, cudaStream_t stream) {
-  const bool sb = (b.flags & TREEWY_FLAG_STATE_BF16) != 0;
-  if (b.max_nodes <= 4) return sb ? launch_small<true, 1>(b, map_s0, stream)
-                                  : launch_small<false, 1>(b, map_s0, stream);
-  return sb ? launch_small<true, 2>(b, map_s0, stream) : launch_small<false, 2>(b, map_s0, stream);
+cudaError_t launch_verify_small(const treewy_batch& b, const CUtensorMap& map_s0, const PrevRound* prev,
+                                cudaStream_t stream) {
+  if (prev == nullptr) return launch_small_any<false>(b, map_s0, PrevRound{}, stream);
+  return launch_small_any<true>(b, map_s0, *prev, stream);
 }
 
 }  // namespace treewy

@@ -183,58 +183,176 @@ def test_small_bad_inputs_set_status_and_spare_others(cuda_lib):
         assert np.abs(np32(tv.o[lo:hi]) - ref.o).max() <= O_TOL * np.abs(ref.o).max()
 
 
-def two_rounds(prev_trees, next_trees, accepted, H=3, seed=43):
+def two_rounds(prev_trees, next_trees, accepted, H=3, seed=43, cap=SMALL, state_dtype="f32"):
     """Two rounds over the same requests sharing one state pool; the previous
     round's trees may be larger than 8 nodes, the next round's are not."""
     R = len(prev_trees)
     prev = wl.assemble([np.asarray(t, np.int32) for t in prev_trees], np.asarray(accepted, np.int32),
                        H, 128, 128, "bf16", 0.05, (0.9, 0.999), ("sigmoid",), seed=seed,
-                       extra_slots=3).to("cuda")
+                       extra_slots=3, state_dtype=state_dtype).to("cuda")
     nxt = wl.assemble([np.asarray(t, np.int32) for t in next_trees], np.full(R, -1, np.int32),
                       H, 128, 128, "bf16", 0.05, (0.9, 0.999), ("sigmoid",), seed=seed + 1,
-                      max_nodes=SMALL, extra_slots=3).to("cuda")
+                      max_nodes=cap, extra_slots=3, state_dtype=state_dtype).to("cuda")
     nxt.state = prev.state
     nxt.state_slot = prev.state_slot
     return prev, nxt
 
 
-def test_small_commit_verify_matches_oracle(cuda_lib):
-    """treewy_commit_verify whose next trees have at most 8 nodes (the commit
-    then the small-tree verification): the committed S_a and the next round's
-    o and U against the oracle run as commit-then-verify."""
-    rng = np.random.default_rng(17)
-    prev_trees = [random_tree(rng, n) for n in (40, 4, 64, 8, 1, 12)]
-    prev_trees[2] = wl.chain_parents(64)
-    next_trees = [random_tree(rng, n) for n in (4, 8, 0, 1, 6, 3)]
-    accepted = [39, -1, 63, 5, 0, 11]
-    prev, nxt = two_rounds(prev_trees, next_trees, accepted)
+def run_commit_verify(prev, nxt):
     tp = binding.TreeVerifier(prev)
     tp.verify()
     torch.cuda.synchronize()
+    assert not tp.status.any()
     S0_pool = prev.state.cpu()
     tn = binding.TreeVerifier(nxt)
     binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
     torch.cuda.synchronize()
-    assert not tn.status.any(), tn.status.tolist()
+    return tn, S0_pool
+
+
+def check_two_rounds(prev, nxt, tn, S0_pool, requests, bf16=False, refused=(), verified=True):
+    """The oracle commits the previous round (unless refused) and verifies the
+    next one from the state the pool then holds: S_a (rounded to bf16 for a
+    bf16 pool, |S_gpu - S_ref| <= 2^-8 |S_ref| + 1e-3 max|S_ref|; fp32: 1e-3
+    max|S_ref|)."""
     o, U = np32(tn.o), np32(tn.U)
     pn, nn = prev.node_offset.cpu().numpy(), nxt.node_offset.cpu().numpy()
-    for r in range(len(prev_trees)):
+    acc = prev.accepted.cpu().numpy()
+    for r in requests:
         slot = int(prev.state_slot[r])
-        S0 = np32(S0_pool[slot])
-        lo, hi = int(pn[r]), int(pn[r + 1])
-        ref_prev = orc.verify_request(S0, prev.parent[lo:hi].cpu().numpy(), np32(prev.q[lo:hi]),
-                                      np32(prev.k[lo:hi]), np32(prev.v[lo:hi]),
-                                      np32(prev.alpha[lo:hi]), np32(prev.beta[lo:hi]))
-        Sa = orc.commit_request(S0, ref_prev, int(accepted[r]))
-        assert np.abs(np32(prev.state[slot]) - Sa).max() <= 1e-3 * np.abs(Sa).max(), r
+        S0 = np32(S0_pool[slot]).astype(np.float64)
+        S_gpu = np32(prev.state[slot]).astype(np.float64)
+        if r in refused or int(acc[r]) < 0:
+            assert np.array_equal(S_gpu, S0), r
+            S_next = S0
+        else:
+            lo, hi = int(pn[r]), int(pn[r + 1])
+            ref_prev = orc.verify_request(S0, prev.parent[lo:hi].cpu().numpy(), np32(prev.q[lo:hi]),
+                                          np32(prev.k[lo:hi]), np32(prev.v[lo:hi]),
+                                          np32(prev.alpha[lo:hi]), np32(prev.beta[lo:hi]))
+            Sa = orc.commit_request(S0, ref_prev, int(acc[r]))
+            if bf16:
+                bound = 2.0 ** -8 * np.abs(Sa) + 1e-3 * np.abs(Sa).max()
+                assert np.all(np.abs(S_gpu - Sa) <= bound), r
+                S_next = orc.commit_request(S0, ref_prev, int(acc[r]), state_dtype="bf16")
+            else:
+                assert np.abs(S_gpu - Sa).max() <= 1e-3 * np.abs(Sa).max(), r
+                S_next = Sa
         lo2, hi2 = int(nn[r]), int(nn[r + 1])
-        if hi2 == lo2:
+        if hi2 == lo2 or not verified:
             continue
-        ref = orc.verify_request(Sa, nxt.parent[lo2:hi2].cpu().numpy(), np32(nxt.q[lo2:hi2]),
+        ref = orc.verify_request(S_next, nxt.parent[lo2:hi2].cpu().numpy(), np32(nxt.q[lo2:hi2]),
                                  np32(nxt.k[lo2:hi2]), np32(nxt.v[lo2:hi2]), np32(nxt.alpha[lo2:hi2]),
                                  np32(nxt.beta[lo2:hi2]))
         assert np.abs(o[lo2:hi2] - ref.o).max() <= O_TOL * np.abs(ref.o).max(), r
         assert np.abs(U[lo2:hi2] - ref.U).max() <= U_TOL * np.abs(ref.U).max(), r
+
+
+@pytest.mark.parametrize("cap", [4, SMALL])
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_small_commit_verify_matches_oracle(cuda_lib, cap, state_dtype):
+    """treewy_commit_verify whose next trees have at most 4 or 8 nodes: accepted
+    paths from the root only to 64 entries (eight update passes of the fused
+    kernel for an fp32 pool; a bf16 pool with previous trees above 8 nodes
+    takes the commit and the verification as two calls), no commit, empty
+    next trees; S_a and the next round's o and U against the oracle run as
+    commit-then-verify."""
+    rng = np.random.default_rng(17 + cap)
+    prev_trees = [random_tree(rng, n) for n in (40, 4, 64, 8, 1, 12, 9)]
+    prev_trees[2] = wl.chain_parents(64)
+    prev_trees[6] = wl.chain_parents(9)     # a path of kSeg + 1 entries
+    next_trees = [random_tree(rng, n) for n in (cap, 2, 0, 1, cap - 1, 3, cap)]
+    accepted = [39, -1, 63, 5, 0, 11, 8]
+    prev, nxt = two_rounds(prev_trees, next_trees, accepted, cap=cap, state_dtype=state_dtype)
+    tn, S0_pool = run_commit_verify(prev, nxt)
+    assert not tn.status.any(), tn.status.tolist()
+    check_two_rounds(prev, nxt, tn, S0_pool, range(len(prev_trees)), bf16=state_dtype == "bf16")
+
+
+@pytest.mark.parametrize("cap", [4, SMALL])
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_small_commit_verify_short_paths(cuda_lib, cap, state_dtype):
+    """Both rounds with trees of at most 8 nodes (the fused kernel for either
+    pool; a bf16 pool's S_a rounded once): chains, stars and random trees,
+    accepted nodes from the root to the deepest node."""
+    rng = np.random.default_rng(41 + cap)
+    prev_trees = [wl.chain_parents(8), np.array([-1] + [0] * 7, np.int32), random_tree(rng, 5),
+                  random_tree(rng, 8), wl.chain_parents(3), random_tree(rng, 1)]
+    next_trees = [random_tree(rng, n) for n in (cap, 1, cap, 2, 0, cap - 1)]
+    accepted = [7, 6, 4, 5, -1, 0]
+    prev, nxt = two_rounds(prev_trees, next_trees, accepted, cap=cap, state_dtype=state_dtype, seed=9)
+    assert prev.max_nodes <= SMALL
+    tn, S0_pool = run_commit_verify(prev, nxt)
+    assert not tn.status.any(), tn.status.tolist()
+    check_two_rounds(prev, nxt, tn, S0_pool, range(len(prev_trees)), bf16=state_dtype == "bf16")
+
+
+def test_small_commit_verify_refusals(cuda_lib):
+    """Each half runs exactly when its separate call would: an accepted index
+    outside the previous tree, a previous parent after its node and a state
+    slot outside the pool refuse the commit (state unchanged, COMMIT_REFUSED
+    beside the reason; the bad slot skips the verification too), while a bad
+    next tree (parent after its node, more nodes than the capacity) skips
+    only the verification and still commits."""
+    rng = np.random.default_rng(29)
+    prev_trees = [random_tree(rng, n) for n in (6, 7, 5, 8, 6, 4)]
+    prev_trees[2] = prev_trees[2].copy()
+    prev_trees[2][3] = 4                    # previous tree: parent after its node
+    next_trees = [random_tree(rng, n) for n in (4, 3, 4, 4, 6, 2)]
+    next_trees[3] = next_trees[3].copy()
+    next_trees[3][2] = 3                    # next tree: parent after its node
+    accepted = [5, 7, 2, 6, 3, 1]           # request 1: outside its 7-node tree
+    prev, nxt = two_rounds(prev_trees, next_trees, accepted, cap=SMALL)
+    slots = prev.state_slot.clone()
+    slots[5] = prev.num_slots               # outside the pool
+    tp = binding.TreeVerifier(prev)
+    tp.verify()
+    torch.cuda.synchronize()
+    S0_pool = prev.state.cpu()
+    prev.state_slot.copy_(slots)
+    nxt.state_slot = prev.state_slot
+    tn = binding.TreeVerifier(nxt, max_nodes=4)   # request 4 (6 nodes) exceeds it
+    tn.o.fill_(float("nan"))
+    binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
+    torch.cuda.synchronize()
+    st = tn.status.cpu().tolist()
+    R_ = binding.STATUS_COMMIT_REFUSED
+    assert st[0] == 0, st
+    assert st[1] == binding.STATUS_BAD_ACCEPTED | R_, st
+    assert st[2] == binding.STATUS_BAD_TREE | R_, st
+    assert st[3] == binding.STATUS_BAD_TREE, st
+    assert st[4] == binding.STATUS_TOO_MANY_NODES, st
+    assert st[5] == binding.STATUS_BAD_SLOT | R_, st
+    nn = nxt.node_offset.cpu().tolist()
+    for r in (3, 4, 5):
+        assert torch.isnan(tn.o[nn[r]:nn[r + 1]]).all(), r
+    check_two_rounds(prev, nxt, tn, S0_pool, [0, 1, 2], refused=(1, 2))
+    # committed although not verified
+    check_two_rounds(prev, nxt, tn, S0_pool, [3, 4], verified=False)
+
+
+def test_small_commit_verify_equals_separate_calls(cuda_lib):
+    """The chain workload, two layers on one state pool: the fused call
+    against verify(prev), commit(prev), verify(next)."""
+    cfg = wl.CONFIGS["chain"]
+    pa = wl.generate(cfg, R=48).to("cuda")
+    na = wl.generate(cfg, R=48, layer=1).to("cuda")
+    pb = wl.generate(cfg, R=48).to("cuda")
+    nb = wl.generate(cfg, R=48, layer=1).to("cuda")
+    na.state, na.state_slot = pa.state, pa.state_slot
+    nb.state, nb.state_slot = pb.state, pb.state_slot
+    tn, _ = run_commit_verify(pa, na)
+    tpb = binding.TreeVerifier(pb)
+    tpb.verify()
+    tpb.commit()
+    tnb = binding.TreeVerifier(nb)
+    tnb.verify()
+    torch.cuda.synchronize()
+    assert not tn.status.any() and not tnb.status.any()
+    ds = (pa.state - pb.state).abs().max().item()
+    assert ds <= 1e-4 * pb.state.abs().max().item(), ds
+    do = (tn.o - tnb.o).abs().max().item()
+    assert do <= 1e-3 * tnb.o.abs().max().item(), do
 
 
 def test_small_graph_replay_matches_eager(cuda_lib):
