@@ -37,7 +37,7 @@ namespace {
 constexpr int kSThreads = 256;
 constexpr int kSDim = 128;
 constexpr uint32_t kSChunk = 128u * 128u;  // one 16 KB box: 128 rows x 128 bytes
-constexpr uint32_t kKQStride = 272u;       // bf16 K/Q row: 256 bytes + 16 (bank offset)
+constexpr uint32_t kKQStride = 288u;       // bf16 K/Q row: 256 bytes + 32 (bank offset)
 
 // Per-tree data after the K/Q rows in dynamic shared memory.
 struct SmallTree {
@@ -90,10 +90,18 @@ struct SmallCfg {
 };
 
 // D += A B for one m16n8k16 bf16 tile with fp32 accumulation.  Fragments
-// (g = lane / 4, q = lane % 4): a0 row g, columns 2q, 2q+1; a1 row g+8;
-// a2 row g, columns 2q+8, 2q+9; a3 row g+8, those columns; b0 column g,
-// rows 2q, 2q+1; b1 rows 2q+8, 2q+9; d[0..1] row g, columns 2q, 2q+1;
-// d[2..3] row g+8.
+// (g = lane / 4, q = lane % 4): a0 row g, k 2q, 2q+1; a1 row g+8; a2 row g,
+// k 2q+8, 2q+9; a3 row g+8, those k; b0 column g, k 2q, 2q+1; b1 k 2q+8,
+// 2q+9; d[0..1] row g, columns 2q, 2q+1; d[2..3] row g+8.
+//
+// The products only need A and B to agree on which state column each k
+// stands for, so within a k-step of 16 columns k = 2q, 2q+1, 2q+8, 2q+9
+// stand for columns 4q .. 4q+3: a lane reads one 16-byte granule of a state
+// row (8 bytes of a bf16 one, or of a key row) per fragment row.  And the
+// fragment rows g stand for state rows perm(g) (below), so that the lanes
+// of each shared-memory load phase meet rows of different 128B-swizzle
+// phases: every load of the state tile and of the key rows is free of bank
+// conflicts.
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -103,8 +111,19 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t lds32(const unsigned char* p) {
-  return *reinterpret_cast<const uint32_t*>(p);
+__device__ __forceinline__ uint2 lds64(const unsigned char* p) {
+  return *reinterpret_cast<const uint2*>(p);
+}
+
+// State row of fragment row g (0..7) of a warp's 16 rows.  fp32 tile: 16-byte
+// loads run in phases of 8 lanes (fragment rows 2i, 2i+1), which take rows i
+// and i+4, whose swizzles place the row's four granules in opposite halves
+// of the 128-byte line.  bf16 tile: 8-byte loads run in phases of 16 lanes
+// (rows 4i .. 4i+3), which take rows of distinct swizzle pairs 0, 2, 4, 6
+// (or 1, 3, 5, 7).
+template <bool SB>
+__device__ __forceinline__ int frag_row(int g) {
+  return SB ? ((g & 3) << 1) | (g >> 2) : (g >> 1) | ((g & 1) << 2);
 }
 
 // One CTA per (request, head), 256 threads.  Warp w owns state rows
@@ -138,7 +157,8 @@ __global__ void __launch_bounds__(kSThreads, 3)
   const int t = threadIdx.x;
   const int warp = t >> 5, lane = t & 31;
   const int g = lane >> 2, q = lane & 3;
-  const int row = 16 * warp + g + ((q & 2) ? 8 : 0);  // this lane's row in the solve
+  const int r0 = 16 * warp + frag_row<SB>(g);  // this lane's state rows r0 and r0 + 8
+  const int row = r0 + ((q & 2) ? 8 : 0);       // and its row in the solve
   const bool is_o = (q & 1) != 0;
 
   // Every thread reads the request's metadata and checks it (the same
@@ -201,7 +221,6 @@ __global__ void __launch_bounds__(kSThreads, 3)
   // the same round trip as the tree; the path walk then only weights them
   // (c_j on the accepted path, 0 elsewhere), so S_a waits for no further
   // memory round trip.
-  const int r0 = 16 * warp + g;  // this lane's state rows r0 and r0 + 8
   const bool spec = FUSED && commit_a >= 0 && prev.max_nodes <= kSeg;
   float cu0[kSeg], cu1[kSeg];    // c_j u_j of rows r0, r0 + 8
 #pragma unroll
@@ -297,10 +316,9 @@ __global__ void __launch_bounds__(kSThreads, 3)
     float gd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const unsigned char* r0 = kqs + g * kKQStride + (16 * ks + 2 * q) * 2;
-      const unsigned char* r1 = r0 + 8 * kKQStride;
-      const uint32_t a0 = lds32(r0), a1 = lds32(r1), a2 = lds32(r0 + 16), a3 = lds32(r1 + 16);
-      mma16816(gd, a0, a1, a2, a3, a0, a2);
+      const uint2 x0 = lds64(kqs + g * kKQStride + (16 * ks + 4 * q) * 2);
+      const uint2 x1 = lds64(kqs + (g + 8) * kKQStride + (16 * ks + 4 * q) * 2);
+      mma16816(gd, x0.x, x1.x, x0.y, x1.y, x0.x, x0.y);
     }
     ts.gram[g][2 * q] = gd[0];
     ts.gram[g][2 * q + 1] = gd[1];
@@ -397,62 +415,73 @@ __global__ void __launch_bounds__(kSThreads, 3)
     }
 #pragma unroll(FUSED ? 1 : 2)
     for (int ks = 0; ks < 8; ++ks) {
+      // a[hr], a[2 + hr]: row r0 + 8hr, state columns c0, c0+1 and c0+2, c0+3
       uint32_t ah[4], al4[4];
+      const int c0 = 16 * ks + 4 * q;
 #pragma unroll
-      for (int f = 0; f < 4; ++f) {
-        const int colg = 16 * ks + 2 * q + ((f & 2) ? 8 : 0);  // state column
-        const int rr = r0 + ((f & 1) ? 8 : 0);
-        // the element pair (rr, colg), (rr, colg + 1) in the swizzled tile:
-        // box colg / 32 (fp32) or colg / 64 (bf16), 16-byte granule in the row
-        unsigned char* ep = SB ? s0 + (colg >> 6) * kSChunk + rr * 128 +
-                                     ((((colg & 63) >> 3) ^ sw) << 4) + (colg & 7) * 2
-                               : s0 + (colg >> 5) * kSChunk + rr * 128 +
-                                     ((((colg & 31) >> 2) ^ sw) << 4) + (colg & 3) * 4;
-        float x0, x1;
-        uint32_t raw = 0u;
+      for (int hr = 0; hr < 2; ++hr) {
+        const int rr = r0 + 8 * hr;
+        // box c0 / 32 (fp32) or c0 / 64 (bf16), 16-byte granule in the row
+        unsigned char* ep = SB ? s0 + (c0 >> 6) * kSChunk + rr * 128 +
+                                     ((((c0 & 63) >> 3) ^ sw) << 4) + (c0 & 7) * 2
+                               : s0 + (c0 >> 5) * kSChunk + rr * 128 + ((((c0 & 31) >> 2) ^ sw) << 4);
+        float x[4];
+        uint2 raw = make_uint2(0u, 0u);
         if constexpr (SB) {
-          raw = lds32(ep);
-          x0 = __uint_as_float(raw << 16);
-          x1 = __uint_as_float(raw & 0xFFFF0000u);
+          raw = lds64(ep);
+          x[0] = __uint_as_float(raw.x << 16);
+          x[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+          x[2] = __uint_as_float(raw.y << 16);
+          x[3] = __uint_as_float(raw.y & 0xFFFF0000u);
         } else {
-          const float2 x = *reinterpret_cast<const float2*>(ep);
-          x0 = x.x;
-          x1 = x.y;
+          const float4 v = *reinterpret_cast<const float4*>(ep);
+          x[0] = v.x;
+          x[1] = v.y;
+          x[2] = v.z;
+          x[3] = v.w;
         }
         if constexpr (FUSED) {
           if (upd) {
-            // S_a = gamma_a S0 + sum_j c_j u_j k_j^T on this pair
-            float d0 = 0.f, d1 = 0.f;
+            // S_a = gamma_a S0 + sum_j c_j u_j k_j^T on these four elements
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < kSeg; ++j) {
               if (j < ne && ((use >> j) & 1)) {
-                const uint32_t kp = lds32(pathk + j * kKQStride + colg * 2);  // entry j < ne
-                const float cu = (f & 1) ? cu1[j] : cu0[j];
-                d0 = fmaf(cu, __uint_as_float(kp << 16), d0);
-                d1 = fmaf(cu, __uint_as_float(kp & 0xFFFF0000u), d1);
+                const uint2 kp = lds64(pathk + j * kKQStride + c0 * 2);
+                const float cu = hr ? cu1[j] : cu0[j];
+                d[0] = fmaf(cu, __uint_as_float(kp.x << 16), d[0]);
+                d[1] = fmaf(cu, __uint_as_float(kp.x & 0xFFFF0000u), d[1]);
+                d[2] = fmaf(cu, __uint_as_float(kp.y << 16), d[2]);
+                d[3] = fmaf(cu, __uint_as_float(kp.y & 0xFFFF0000u), d[3]);
               }
             }
-            x0 = fmaf(ga, x0, d0);
-            x1 = fmaf(ga, x1, d1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[i] = fmaf(ga, x[i], d[i]);
             if constexpr (SB) {
-              const __nv_bfloat162 pr = __floats2bfloat162_rn(x0, x1);  // rounded once
-              raw = *reinterpret_cast<const uint32_t*>(&pr);
-              *reinterpret_cast<uint32_t*>(ep) = raw;
+              const __nv_bfloat162 p0 = __floats2bfloat162_rn(x[0], x[1]);  // rounded once
+              const __nv_bfloat162 p1 = __floats2bfloat162_rn(x[2], x[3]);
+              raw = make_uint2(*reinterpret_cast<const uint32_t*>(&p0),
+                               *reinterpret_cast<const uint32_t*>(&p1));
+              *reinterpret_cast<uint2*>(ep) = raw;
             } else {
-              *reinterpret_cast<float2*>(ep) = make_float2(x0, x1);
+              *reinterpret_cast<float4*>(ep) = make_float4(x[0], x[1], x[2], x[3]);
             }
           }
         }
-        if constexpr (SB) ah[f] = raw;
-        else split_pair(x0, x1, ah[f], al4[f]);
+        if constexpr (SB) {
+          ah[hr] = raw.x;
+          ah[2 + hr] = raw.y;
+        } else {
+          split_pair(x[0], x[1], ah[hr], al4[hr]);
+          split_pair(x[2], x[3], ah[2 + hr], al4[2 + hr]);
+        }
       }
       if (mma_pass) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const unsigned char* bp = kqs + (8 * nt + g) * kKQStride + (16 * ks + 2 * q) * 2;
-          const uint32_t b0 = lds32(bp), b1 = lds32(bp + 16);
-          mma16816(acc[nt], ah[0], ah[1], ah[2], ah[3], b0, b1);
-          if constexpr (!SB) mma16816(acc[nt], al4[0], al4[1], al4[2], al4[3], b0, b1);
+          const uint2 bk = lds64(kqs + (8 * nt + g) * kKQStride + c0 * 2);
+          mma16816(acc[nt], ah[0], ah[1], ah[2], ah[3], bk.x, bk.y);
+          if constexpr (!SB) mma16816(acc[nt], al4[0], al4[1], al4[2], al4[3], bk.x, bk.y);
         }
       }
     }
