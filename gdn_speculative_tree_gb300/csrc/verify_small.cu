@@ -127,9 +127,10 @@ __device__ __forceinline__ int frag_row(int g) {
 }
 
 // One CTA per (request, head), 256 threads.  Warp w owns state rows
-// 16w..16w+15; lane (g, q) = (lane / 4, lane % 4) holds rows 16w+g and
-// 16w+g+8 of the MMA tiles, and for the solve takes row 16w+g (q < 2) or
-// 16w+g+8 (q >= 2), writing U (q even) or o (q odd).
+// 16w..16w+15; lane (g, q) = (lane / 4, lane % 4) holds fragment rows g and
+// g+8 of the MMA tiles, which stand for state rows r0 = 16w + frag_row(g) and
+// r0 + 8, and for the solve takes row r0 (q < 2) or r0 + 8 (q >= 2), writing
+// U (q even) or o (q odd).
 //
 // FUSED: the previous round's commit first, S_a = gamma_a S0 +
 // sum_{j in path(a)} c_j u_j k_j^T with c_j = gamma_a / gamma_j (TreeWY
@@ -219,8 +220,8 @@ __global__ void __launch_bounds__(kSThreads, 3)
   // A previous tree of at most kSeg nodes: every node's U values in this
   // lane's two state rows and (threads < 128) its key row are requested in
   // the same round trip as the tree; the path walk then only weights them
-  // (c_j on the accepted path, 0 elsewhere), so S_a waits for no further
-  // memory round trip.
+  // (c_j on the accepted path; nodes off it are skipped), so S_a waits for
+  // no further memory round trip.
   const bool spec = FUSED && commit_a >= 0 && prev.max_nodes <= kSeg;
   float cu0[kSeg], cu1[kSeg];    // c_j u_j of rows r0, r0 + 8
 #pragma unroll
