@@ -35,11 +35,11 @@ def draw_tree(rng, cap):
     return np.array([-1] + [int(rng.integers(-1, i)) for i in range(1, n)], np.int32)
 
 
-def draw_batch(seed):
+def draw_batch(seed, caps=(16, 32, 64)):
     rng = np.random.default_rng(1000 + seed)
     dk, dv, qkv = SHAPES[int(rng.integers(0, len(SHAPES)))]
     sd = "bf16" if rng.integers(0, 2) else "f32"
-    cap = int(rng.choice([16, 32, 64]))
+    cap = int(rng.choice(list(caps)))
     R = int(rng.integers(1, 9))
     H = int(rng.integers(1, 4))
     trees = [draw_tree(rng, cap) for _ in range(R)]
@@ -62,9 +62,16 @@ def check_state(S_gpu, S_ref, sd):
     assert np.all(np.abs(S_gpu - S_ref) <= bound + 1e-30)
 
 
-@pytest.mark.parametrize("seed", range(48))
+SMALL_CAPS = (4, 8)  # the small-tree kernel's capacities (dk = dv = 128, bf16 q/k/v)
+
+
+@pytest.mark.parametrize("seed", list(range(48)) + [f"small{i}" for i in range(24)])
 def test_fuzz_verify_commit(cuda_lib, seed):
-    _, p = draw_batch(seed)
+    if isinstance(seed, str):
+        _, p = draw_batch(3000 + int(seed[5:]), caps=SMALL_CAPS)
+        seed = 3000 + int(seed[5:])
+    else:
+        _, p = draw_batch(seed)
     w = assemble(p, p["trees"], p["acc"], seed)
     S0_pool = w.state.cpu()
     tv = binding.TreeVerifier(w)
@@ -92,9 +99,13 @@ def test_fuzz_verify_commit(cuda_lib, seed):
     assert u_err <= 2e-3 * max(u_max, 1e-30), (u_err, u_max)
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", list(range(24)) + [f"small{i}" for i in range(16)])
 def test_fuzz_fused_two_rounds(cuda_lib, seed):
-    rng, p = draw_batch(100 + seed)
+    if isinstance(seed, str):
+        rng, p = draw_batch(4000 + int(seed[5:]), caps=SMALL_CAPS)
+        seed = 4000 + int(seed[5:])
+    else:
+        rng, p = draw_batch(100 + seed)
     R = len(p["trees"])
     nxt_trees = [draw_tree(rng, p["cap"]) for _ in range(R)]
     prev = assemble(p, p["trees"], p["acc"], 2 * seed)
@@ -147,7 +158,7 @@ def test_fuzz_error_reporting(cuda_lib, seed, flags):
     index outside the tree) get exactly their status bits and keep their
     outputs and state; every other request matches the oracle."""
     rng = np.random.default_rng(5000 + seed)
-    cap = int(rng.choice([16, 32]))
+    cap = int(rng.choice([4, 8, 16, 32]))
     R = int(rng.integers(4, 10))
     kinds = [int(rng.integers(0, 5)) for _ in range(R)]   # 0 clean, 1 parent, 2 size, 3 slot, 4 accepted
     trees, acc = [], []
