@@ -38,6 +38,7 @@ constexpr int kSThreads = 256;
 constexpr int kSDim = 128;
 constexpr uint32_t kSChunk = 128u * 128u;  // one 16 KB box: 128 rows x 128 bytes
 constexpr uint32_t kKQStride = 288u;       // bf16 K/Q row: 256 bytes + 32 (bank offset)
+constexpr uint32_t kPathStride = 272u;     // bf16 key row of the accepted path: 256 + 16
 
 // Per-tree data after the K/Q rows in dynamic shared memory.
 struct SmallTree {
@@ -82,7 +83,7 @@ struct SmallCfg {
   static constexpr uint32_t kTreeOff = kKQOff + 16u * kKQStride;
   static constexpr uint32_t kPrevOff = (kTreeOff + static_cast<uint32_t>(sizeof(SmallTree)) + 15u) & ~15u;
   static constexpr uint32_t kPathKOff = (kPrevOff + static_cast<uint32_t>(sizeof(SmallPrev)) + 15u) & ~15u;
-  static constexpr uint32_t kEnd = FUSED ? kPathKOff + kSeg * kKQStride
+  static constexpr uint32_t kEnd = FUSED ? kPathKOff + kSeg * kPathStride
                                          : kTreeOff + static_cast<uint32_t>(sizeof(SmallTree));
   static constexpr uint32_t kDynSmem = 1024u + kEnd;
   // three CTAs per SM: 228 KB of shared memory, 1 KB of it reserved per CTA
@@ -223,17 +224,18 @@ __global__ void __launch_bounds__(kSThreads, 3)
   // (c_j on the accepted path; nodes off it are skipped), so S_a waits for
   // no further memory round trip.
   const bool spec = FUSED && commit_a >= 0 && prev.max_nodes <= kSeg;
-  float cu0[kSeg], cu1[kSeg];    // c_j u_j of rows r0, r0 + 8
-#pragma unroll
-  for (int j = 0; j < kSeg; ++j) cu0[j] = cu1[j] = 0.f;
+  // The update's left operand for this lane: u_j of entries j = 2q, 2q+1 in
+  // rows r0 (cu[0], cu[1]) and r0 + 8 (cu[2], cu[3]), later times c_j.
+  float cu[4] = {0.f, 0.f, 0.f, 0.f};
   uint4 pkr = make_uint4(0u, 0u, 0u, 0u);
   if (spec) {
 #pragma unroll
-    for (int j = 0; j < kSeg; ++j) {
+    for (int e = 0; e < 2; ++e) {
+      const int j = 2 * q + e;
       if (j < pn) {
         const float* ur = prev.U + ((static_cast<int64_t>(plo) + j) * H + h) * kSDim;
-        cu0[j] = __ldg(ur + r0);
-        cu1[j] = __ldg(ur + r0 + 8);
+        cu[e] = __ldg(ur + r0);
+        cu[2 + e] = __ldg(ur + r0 + 8);
       }
     }
     if (t < kSeg * 16 && (t >> 4) < pn) {
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(kSThreads, 3)
   }
 
   *reinterpret_cast<uint4*>(kqs + kv * kKQStride + (t & 15) * 16) = kraw;
-  if (spec && t < kSeg * 16) *reinterpret_cast<uint4*>(pathk + (t >> 4) * kKQStride + (t & 15) * 16) = pkr;
+  if (spec && t < kSeg * 16) *reinterpret_cast<uint4*>(pathk + (t >> 4) * kPathStride + (t & 15) * 16) = pkr;
   if (t < 128) (t < 64 ? &ts.A[0][0] : &ts.M[0][0])[t & 63] = 0.f;
   bool bad = false;
   if (t < N) {
@@ -371,25 +373,30 @@ __global__ void __launch_bounds__(kSThreads, 3)
     const bool upd = ps < nseg;
     const bool mma_pass = go && ps == npass - 1;
     const int j0 = kSeg * ps;
-    int ne = 0;          // update entries of this pass
-    int use = ~0;        // ... of which those with bit j set apply
     float ga = 1.f;
+    // the update's A fragment (rows r0, r0 + 8; entries 2q, 2q+1 as k), split
+    // into hi + lo bf16 halves
+    uint32_t uh0 = 0u, uh1 = 0u, ul0 = 0u, ul1 = 0u;
     if constexpr (FUSED) {
       if (upd && spec) {
-        // entries = the previous tree's nodes; those on the accepted path
-        // weighted by c_j, the others skipped (their rows never read)
-        use = pv.onpath;
+        // entries = the previous tree's nodes: those on the accepted path
+        // weighted by c_j, the others zero (their key rows cleared as well)
+        const int use = pv.onpath;
+        if (t < kSeg * 16 && !((use >> (t >> 4)) & 1))
+          *reinterpret_cast<uint4*>(pathk + (t >> 4) * kPathStride + (t & 15) * 16) = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int j = 0; j < kSeg; ++j) {
-          cu0[j] = ((use >> j) & 1) ? cu0[j] * pv.w[j] : 0.f;
-          cu1[j] = ((use >> j) & 1) ? cu1[j] * pv.w[j] : 0.f;
+        for (int e = 0; e < 2; ++e) {
+          const int j = 2 * q + e;
+          const float w = ((use >> j) & 1) ? pv.w[j] : 0.f;
+          cu[e] = ((use >> j) & 1) ? cu[e] * w : 0.f;
+          cu[2 + e] = ((use >> j) & 1) ? cu[2 + e] * w : 0.f;
         }
-        ne = pn;
         ga = pv.gamma_a;
+        __syncthreads();  // the cleared key rows
       } else if (upd) {
-        // c_j u_j of this lane's two rows, and (shared) the key rows k_j,
-        // for the path entries j0 .. j0 + kSeg - 1 (zero past the path)
-        ne = len - j0 < kSeg ? len - j0 : kSeg;
+        // c_j u_j of this lane's two rows for path entries j0 + 2q, j0 + 2q + 1,
+        // and (shared) the key rows k_j of entries j0 .. j0 + kSeg - 1 (zero
+        // past the path)
         if (ps > 0) __syncthreads();  // the previous pass has read the key rows
         if (t < kSeg * 16) {
           const int j = t >> 4;
@@ -399,19 +406,24 @@ __global__ void __launch_bounds__(kSThreads, 3)
             kr = __ldg(kg4 + ((static_cast<int64_t>(plo) + pv.path[j0 + j]) * H + h) * (kSDim / 8) +
                        (t & 15));
           }
-          *reinterpret_cast<uint4*>(pathk + j * kKQStride + (t & 15) * 16) = kr;
+          *reinterpret_cast<uint4*>(pathk + j * kPathStride + (t & 15) * 16) = kr;
         }
 #pragma unroll
-        for (int j = 0; j < kSeg; ++j) {
-          cu0[j] = cu1[j] = 0.f;
-          if (j0 + j < len) {
-            const float* ur = prev.U + ((static_cast<int64_t>(plo) + pv.path[j0 + j]) * H + h) * kSDim;
-            cu0[j] = pv.c[j0 + j] * __ldg(ur + r0);
-            cu1[j] = pv.c[j0 + j] * __ldg(ur + r0 + 8);
+        for (int e = 0; e < 2; ++e) {
+          const int j = j0 + 2 * q + e;
+          cu[e] = cu[2 + e] = 0.f;
+          if (j < len) {
+            const float* ur = prev.U + ((static_cast<int64_t>(plo) + pv.path[j]) * H + h) * kSDim;
+            cu[e] = pv.c[j] * __ldg(ur + r0);
+            cu[2 + e] = pv.c[j] * __ldg(ur + r0 + 8);
           }
         }
         if (ps == 0) ga = pv.gamma_a;
         __syncthreads();
+      }
+      if (upd) {
+        split_pair(cu[0], cu[1], uh0, ul0);
+        split_pair(cu[2], cu[3], uh1, ul1);
       }
     }
 #pragma unroll(FUSED ? 1 : 2)
@@ -419,6 +431,25 @@ __global__ void __launch_bounds__(kSThreads, 3)
       // a[hr], a[2 + hr]: row r0 + 8hr, state columns c0, c0+1 and c0+2, c0+3
       uint32_t ah[4], al4[4];
       const int c0 = 16 * ks + 4 * q;
+      // the fused commit's update sum_j c_j u_j k_j^T on these elements, as
+      // two tiles of warp MMAs: A = [c u] (rows; path entries as k), B = the
+      // path's key rows, with D column n of tile tt standing for state column
+      // 16 ks + 4 (n / 2) + 2 tt + n % 2, so that du[tt] lands on this lane's
+      // columns c0 + 2 tt, c0 + 2 tt + 1 (rows r0: du[tt][0..1], r0 + 8: [2..3])
+      float du[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      if constexpr (FUSED) {
+        if (upd) {
+#pragma unroll
+          for (int tt = 0; tt < 2; ++tt) {
+            const int pc = 16 * ks + 4 * (g >> 1) + 2 * tt + (g & 1);
+            const uint32_t k0 = *reinterpret_cast<const unsigned short*>(pathk + (2 * q) * kPathStride + pc * 2);
+            const uint32_t k1 = *reinterpret_cast<const unsigned short*>(pathk + (2 * q + 1) * kPathStride + pc * 2);
+            const uint32_t bk = k0 | (k1 << 16);
+            mma16816(du[tt], uh0, uh1, 0u, 0u, bk, 0u);
+            mma16816(du[tt], ul0, ul1, 0u, 0u, bk, 0u);
+          }
+        }
+      }
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int rr = r0 + 8 * hr;
@@ -444,20 +475,8 @@ __global__ void __launch_bounds__(kSThreads, 3)
         if constexpr (FUSED) {
           if (upd) {
             // S_a = gamma_a S0 + sum_j c_j u_j k_j^T on these four elements
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < kSeg; ++j) {
-              if (j < ne && ((use >> j) & 1)) {
-                const uint2 kp = lds64(pathk + j * kKQStride + c0 * 2);
-                const float cu = hr ? cu1[j] : cu0[j];
-                d[0] = fmaf(cu, __uint_as_float(kp.x << 16), d[0]);
-                d[1] = fmaf(cu, __uint_as_float(kp.x & 0xFFFF0000u), d[1]);
-                d[2] = fmaf(cu, __uint_as_float(kp.y << 16), d[2]);
-                d[3] = fmaf(cu, __uint_as_float(kp.y & 0xFFFF0000u), d[3]);
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) x[i] = fmaf(ga, x[i], d[i]);
+            for (int i = 0; i < 4; ++i) x[i] = fmaf(ga, x[i], du[i >> 1][2 * hr + (i & 1)]);
             if constexpr (SB) {
               const __nv_bfloat162 p0 = __floats2bfloat162_rn(x[0], x[1]);  // rounded once
               const __nv_bfloat162 p1 = __floats2bfloat162_rn(x[2], x[3]);
