@@ -389,3 +389,19 @@ def test_small_graph_replay_matches_eager(cuda_lib):
     assert_within(compare(w, replay, range(w.R)), "chain graph replay")
     assert torch.equal(tv.o.cpu(), torch.from_numpy(run.o))
     assert torch.equal(w.state.cpu(), run.S_after.cpu())
+
+
+def test_small_commit_verify_chain_full_size(cuda_lib):
+    """The chain workload at full size (64 requests x 32 heads, the launch
+    configuration of the per-workload study): two layers on one state pool,
+    the fused call against the oracle run as commit-then-verify on every
+    request."""
+    cfg = wl.CONFIGS["chain"]
+    prev = wl.generate(cfg).to("cuda")
+    nxt = wl.generate(cfg, layer=1).to("cuda")
+    nxt.state, nxt.state_slot = prev.state, prev.state_slot
+    assert prev.max_nodes <= SMALL and nxt.max_nodes <= SMALL
+    assert (prev.accepted.cpu() == -1).any()   # the no-op commit is exercised
+    tn, S0_pool = run_commit_verify(prev, nxt)
+    assert not tn.status.any(), tn.status.tolist()
+    check_two_rounds(prev, nxt, tn, S0_pool, range(prev.R))
