@@ -79,7 +79,8 @@ enum {
 /* Flags. */
 enum {
   /* Use the portable kernels (CUDA cores, no bulk tensor copies) even where
-     the tensor-core verification (dk = dv = 128, bf16 q/k/v) or the
+     the tensor-core verification (dk = dv = 128, bf16 q/k/v: tcgen05, or
+     warp-level MMAs for batches of trees of at most 8 nodes) or the
      bulk-copy commit (dk = dv = 128) applies.  Same results within rounding. */
   TREEWY_FLAG_FORCE_GENERIC = 1u,
   /* The state pool holds bf16 instead of f32: the dtype in which the GDN
@@ -188,8 +189,11 @@ treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted,
  * S_a = gamma_a S0 + sum_{i on path(a)} (gamma_a/gamma_i) u_i k_i^T on chip,
  * writes it back to the state block once, and verifies `next` from it: the
  * results equal treewy_commit(prev, prev_accepted) followed by
- * treewy_verify(next), with one state read per head instead of two.  A request
- * with no node in `next` still gets its commit.  prev and next must have the
+ * treewy_verify(next), with one state read per head instead of two.  (Shapes
+ * other than dk = dv = 128 with bf16 q/k/v in both rounds, and a bf16 pool
+ * whose next trees have at most 8 nodes while the previous ones have more,
+ * run as those two calls back to back on `stream`.)  A request with no node
+ * in `next` still gets its commit.  prev and next must have the
  * same R, H, dk, dv, state pool pointer, num_slots, state_slot pointer and
  * TREEWY_FLAG_STATE_BF16.
  * Errors, as for the two calls made one after the other, with every status
