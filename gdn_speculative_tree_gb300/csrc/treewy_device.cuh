@@ -231,6 +231,21 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// D += A B for one m16n8k16 warp-level tile, bf16 x bf16 -> fp32: the
+// register-operand tensor path, for products too small to pay for tcgen05's
+// TMEM round trip.  Fragments (g = lane / 4, q = lane % 4): a0 row g, k 2q,
+// 2q+1; a1 row g+8; a2 row g, k 2q+8, 2q+9; a3 row g+8, those k; b0 column g,
+// k 2q, 2q+1; b1 k 2q+8, 2q+9; d[0..1] row g, columns 2q, 2q+1; d[2..3] row
+// g+8.
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // 16 consecutive 32-bit TMEM columns of this thread's lane.  The hardware
 // writes the target registers asynchronously, until tcgen05.wait::ld; the
 // compiler sees them as written here, so the matching wait (tmem_wait16 /

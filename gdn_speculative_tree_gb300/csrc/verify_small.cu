@@ -90,10 +90,7 @@ struct SmallCfg {
   static_assert(3u * (kDynSmem + 1024u) <= 228u * 1024u, "three CTAs per SM");
 };
 
-// D += A B for one m16n8k16 bf16 tile with fp32 accumulation.  Fragments
-// (g = lane / 4, q = lane % 4): a0 row g, k 2q, 2q+1; a1 row g+8; a2 row g,
-// k 2q+8, 2q+9; a3 row g+8, those k; b0 column g, k 2q, 2q+1; b1 k 2q+8,
-// 2q+9; d[0..1] row g, columns 2q, 2q+1; d[2..3] row g+8.
+// Warp-level MMAs: mma16816_bf16 (treewy_device.cuh).
 //
 // The products only need A and B to agree on which state column each k
 // stands for, so within a k-step of 16 columns k = 2q, 2q+1, 2q+8, 2q+9
@@ -103,15 +100,6 @@ struct SmallCfg {
 // of each shared-memory load phase meet rows of different 128B-swizzle
 // phases: every load of the state tile and of the key rows is free of bank
 // conflicts.
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ uint2 lds64(const unsigned char* p) {
   return *reinterpret_cast<const uint2*>(p);
 }
@@ -321,7 +309,7 @@ __global__ void __launch_bounds__(kSThreads, 3)
     for (int ks = 0; ks < 8; ++ks) {
       const uint2 x0 = lds64(kqs + g * kKQStride + (16 * ks + 4 * q) * 2);
       const uint2 x1 = lds64(kqs + (g + 8) * kKQStride + (16 * ks + 4 * q) * 2);
-      mma16816(gd, x0.x, x1.x, x0.y, x1.y, x0.x, x0.y);
+      mma16816_bf16(gd, x0.x, x1.x, x0.y, x1.y, x0.x, x0.y);
     }
     ts.gram[g][2 * q] = gd[0];
     ts.gram[g][2 * q + 1] = gd[1];
@@ -445,8 +433,8 @@ __global__ void __launch_bounds__(kSThreads, 3)
             const uint32_t k0 = *reinterpret_cast<const unsigned short*>(pathk + (2 * q) * kPathStride + pc * 2);
             const uint32_t k1 = *reinterpret_cast<const unsigned short*>(pathk + (2 * q + 1) * kPathStride + pc * 2);
             const uint32_t bk = k0 | (k1 << 16);
-            mma16816(du[tt], uh0, uh1, 0u, 0u, bk, 0u);
-            mma16816(du[tt], ul0, ul1, 0u, 0u, bk, 0u);
+            mma16816_bf16(du[tt], uh0, uh1, 0u, 0u, bk, 0u);
+            mma16816_bf16(du[tt], ul0, ul1, 0u, 0u, bk, 0u);
           }
         }
       }
@@ -500,8 +488,8 @@ __global__ void __launch_bounds__(kSThreads, 3)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const uint2 bk = lds64(kqs + (8 * nt + g) * kKQStride + c0 * 2);
-          mma16816(acc[nt], ah[0], ah[1], ah[2], ah[3], bk.x, bk.y);
-          if constexpr (!SB) mma16816(acc[nt], al4[0], al4[1], al4[2], al4[3], bk.x, bk.y);
+          mma16816_bf16(acc[nt], ah[0], ah[1], ah[2], ah[3], bk.x, bk.y);
+          if constexpr (!SB) mma16816_bf16(acc[nt], al4[0], al4[1], al4[2], al4[3], bk.x, bk.y);
         }
       }
     }
