@@ -709,63 +709,71 @@ def study_graph(args, local):
 
 
 def study_bf16state(args, local):
-    """The benchmark step with a bf16 state pool (32 KiB per head instead of
-    64 KiB): 30 layers of verify + commit, and the fused commit-into-verify
-    step, on the same wide ragged workload."""
+    """A bf16 state pool (32 KiB per head instead of 64 KiB), the serving
+    dtype: 30 layers of verify + commit, and the fused commit-into-verify
+    step, on the wide ragged workload (the benchmark) and on the chain
+    workload (multi-token-prediction chains, the pages' serving shape); one
+    JSON line each.  Each step cycles through 30 layers of distinct inputs,
+    more than the 129 MB L2 holds."""
     from gdn_speculative_tree_gb300 import binding
     dev = torch.device("cuda", local)
-    cfg = wl.CONFIGS[CONFIG_NAME]
-    layers = args.layers
-    work = [binding.TreeVerifier(wl.generate(cfg, layer=l, device=dev, state_dtype="bf16"))
-            for l in range(layers)]
     stream = torch.cuda.current_stream()
     peak, peak_kind = read_peaks()
-    Ns, plen = tree_stats(work[0].wl.trees, work[0].wl.accepted.cpu().numpy())
-    H = cfg.H
-    vb, cb = verify_bytes(Ns, H, 32768), commit_bytes(plen, H, 32768)
-    fb = vb + cb - int(H * 32768 * int((plen > 0).sum()))
-    nodes = int(Ns.sum())
-
-    def timed(fn_layer):
-        for _ in range(args.warmup):
-            for tv in work:
-                fn_layer(tv)
-        torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps * layers)]
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        i = 0
-        for _ in range(args.steps):
-            for tv in work:
-                ev[i][0].record(stream)
-                fn_layer(tv)
-                ev[i][1].record(stream)
-                i += 1
-        end.record(stream)
-        torch.cuda.synchronize()
-        per = [a.elapsed_time(b) for a, b in ev]
-        return start.elapsed_time(end) / args.steps, sum(per) / len(per)
-
-    v_step, v_ms = timed(lambda tv: tv.verify(stream))
-    c_step, c_ms = timed(lambda tv: tv.commit(None, stream))
-    f_step, f_ms = timed(lambda tv: binding.treewy_commit_verify(tv.batch, tv.wl.accepted, tv.batch,
-                                                                 stream))
-    for tv in work:
-        if tv.status.any().item():
-            raise SystemExit("device status bits set in the bf16 state study")
+    layers = args.layers
     g = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
-    print(json.dumps({
-        "study": "bf16 state pool", "workload": "wide ragged trees, 256 req x 32 heads, "
-        f"{layers} layers, bf16 state", "peak_gbs": peak, "peak_kind": f"{peak_kind} hbm_gbs",
-        "ms_per_step": v_step + c_step, "value": nodes / ((v_step + c_step) * 1e-3), "unit": UNIT,
-        "verify": {"avg_launch_ms": v_ms, "algorithmic_bytes": vb, "gbs": g(vb, v_ms),
-                   "frac": g(vb, v_ms) / peak},
-        "commit": {"avg_launch_ms": c_ms, "algorithmic_bytes": cb, "gbs": g(cb, c_ms),
-                   "frac": g(cb, c_ms) / peak},
-        "fused": {"ms_per_step": f_step, "value": nodes / (f_step * 1e-3), "avg_launch_ms": f_ms,
-                  "algorithmic_bytes": fb, "gbs": g(fb, f_ms), "frac": g(fb, f_ms) / peak}}),
-        flush=True)
+    for name, label in ((CONFIG_NAME, "wide ragged trees, 256 req x 32 heads"),
+                        ("chain", "MTP chains of 4, 64 req x 32 heads")):
+        cfg = wl.CONFIGS[name]
+        work = [binding.TreeVerifier(wl.generate(cfg, layer=l, device=dev, state_dtype="bf16"))
+                for l in range(layers)]
+        Ns, plen = tree_stats(work[0].wl.trees, work[0].wl.accepted.cpu().numpy())
+        H = cfg.H
+        vb, cb = verify_bytes(Ns, H, 32768), commit_bytes(plen, H, 32768)
+        fb = vb + cb - int(H * 32768 * int((plen > 0).sum()))
+        nodes = int(Ns.sum())
+
+        def timed(fn_layer):
+            for _ in range(args.warmup):
+                for tv in work:
+                    fn_layer(tv)
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps * layers)]
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            i = 0
+            for _ in range(args.steps):
+                for tv in work:
+                    ev[i][0].record(stream)
+                    fn_layer(tv)
+                    ev[i][1].record(stream)
+                    i += 1
+            end.record(stream)
+            torch.cuda.synchronize()
+            per = [a.elapsed_time(b) for a, b in ev]
+            return start.elapsed_time(end) / args.steps, sum(per) / len(per)
+
+        v_step, v_ms = timed(lambda tv: tv.verify(stream))
+        c_step, c_ms = timed(lambda tv: tv.commit(None, stream))
+        f_step, f_ms = timed(lambda tv: binding.treewy_commit_verify(tv.batch, tv.wl.accepted,
+                                                                     tv.batch, stream))
+        for tv in work:
+            if tv.status.any().item():
+                raise SystemExit(f"device status bits set in the bf16 state study ({name})")
+        print(json.dumps({
+            "study": "bf16 state pool", "config": name,
+            "workload": f"{label}, {layers} layers, bf16 state", "peak_gbs": peak,
+            "peak_kind": f"{peak_kind} hbm_gbs",
+            "ms_per_step": v_step + c_step, "value": nodes / ((v_step + c_step) * 1e-3), "unit": UNIT,
+            "verify": {"avg_launch_ms": v_ms, "algorithmic_bytes": vb, "gbs": g(vb, v_ms),
+                       "frac": g(vb, v_ms) / peak},
+            "commit": {"avg_launch_ms": c_ms, "algorithmic_bytes": cb, "gbs": g(cb, c_ms),
+                       "frac": g(cb, c_ms) / peak},
+            "fused": {"ms_per_step": f_step, "value": nodes / (f_step * 1e-3), "avg_launch_ms": f_ms,
+                      "algorithmic_bytes": fb, "gbs": g(fb, f_ms), "frac": g(fb, f_ms) / peak}}),
+            flush=True)
+        del work
+        torch.cuda.empty_cache()
 
 
 def storeall_chunked(w, o, stream, reps=3, max_bytes=34e9):
