@@ -127,8 +127,12 @@ __device__ __forceinline__ int frag_row(int g) {
 // products read them and written back to the pool once; the verification
 // then runs from S_a.  Each half runs exactly when its separate call would:
 // a refused commit leaves the state alone, a bad next tree still commits.
+//
+// Residency: three CTAs per SM for an fp32 pool (shared memory); a bf16 pool's
+// 4-node instances fit more (40-43 KB), and are held to the registers of five
+// (plain: 48) or four (fused: 64) CTAs per SM.
 template <bool SB, int NT, bool FUSED>
-__global__ void __launch_bounds__(kSThreads, 3)
+__global__ void __launch_bounds__(kSThreads, (SB && NT == 1) ? (FUSED ? 4 : 5) : 3)
     verify_small_kernel(const __grid_constant__ CUtensorMap map_s0, const treewy_batch b,
                         const PrevRound prev) {
   using C = SmallCfg<SB, NT, FUSED>;
@@ -573,7 +577,7 @@ cudaError_t launch_small(const treewy_batch& b, const CUtensorMap& map_s0, const
     cudaError_t e = cudaFuncSetAttribute(verify_small_kernel<SB, NT, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kDynSmem));
-    // the whole unified L1/shared array as shared memory: three CTAs per SM
+    // the whole unified L1/shared array as shared memory: three or more CTAs per SM
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(verify_small_kernel<SB, NT, FUSED>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
