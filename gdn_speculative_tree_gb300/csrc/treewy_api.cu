@@ -184,15 +184,18 @@ treewy_status treewy_verify(const treewy_batch* batch, cudaStream_t stream) {
   treewy_status st = validate(batch, true, true, true);
   if (st != TREEWY_OK || batch->R == 0) return st;
   cudaError_t err;
-  // Trees of at most kSmallTreeNodes nodes are verified by warp-level MMAs
-  // straight from the state tile, larger ones by the tcgen05 kernel.  (A batch
-  // of empty trees, T = 0, goes to the portable kernel: there are no rows to
-  // map, and it still checks node_offset and the slots.)
-  if (use_tensor_cores(batch) && batch->T > 0 && batch->max_nodes <= treewy::kSmallTreeNodes) {
+  // Trees of at most kSmallTreeNodes nodes are verified by the small-tree
+  // kernel, of at most kWarpTreeNodes by the warp-MMA kernel (both multiply
+  // straight from the state tile), larger ones by the tcgen05 kernel.  (A
+  // batch of empty trees, T = 0, goes to the portable kernel: there are no
+  // rows to map, and it still checks node_offset and the slots.)
+  if (use_tensor_cores(batch) && batch->T > 0 && batch->max_nodes <= treewy::kWarpTreeNodes) {
     CUtensorMap map;
     st = make_state_map(batch, &map);
     if (st != TREEWY_OK) return st;
-    err = treewy::launch_verify_small(*batch, map, nullptr, stream);
+    err = batch->max_nodes <= treewy::kSmallTreeNodes
+              ? treewy::launch_verify_small(*batch, map, nullptr, stream)
+              : treewy::launch_verify_warp(*batch, map, stream);
   } else if (use_tensor_cores(batch) && batch->T > 0) {
     treewy::VerifyMaps maps;
     st = make_maps(batch, &maps);

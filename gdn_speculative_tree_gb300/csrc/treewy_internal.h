@@ -67,6 +67,14 @@ struct PrevRound;
 cudaError_t launch_verify_small(const treewy_batch& b, const CUtensorMap& state_map,
                                 const PrevRound* prev, cudaStream_t stream);
 
+// Batches of at most this many nodes per tree (and more than
+// kSmallTreeNodes) are verified by warp-level MMAs over the whole method
+// (verify_warp.cu); larger trees by the tcgen05 kernel, whose state products
+// run at several times the rate of warp-level MMAs.
+constexpr int kWarpTreeNodes = 16;
+cudaError_t launch_verify_warp(const treewy_batch& b, const CUtensorMap& state_map,
+                               cudaStream_t stream);
+
 // npm: padded tree capacity (16, 32 or 64).
 size_t verify_tc_smem(int npm);
 cudaError_t launch_verify_tc(const treewy_batch& b, const VerifyMaps& maps, int npm,

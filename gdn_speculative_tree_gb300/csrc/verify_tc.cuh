@@ -64,7 +64,8 @@ struct TcCfg {
   // 16-node tree uses 32 rows, so its chunks are 32 rows and the region sits
   // before the S0 tile: the Gram's reads of rows 32..127 stay inside the
   // CTA's shared memory (their products land in TMEM lanes that are never
-  // read), and the smaller footprint fits three CTAs per SM.
+  // read).  (16-node trees reach this kernel only with the commit fused in;
+  // plain verification of trees of up to 16 nodes has its own kernels.)
   static constexpr uint32_t kKQRows = NPM == 16 ? 32u : 128u;
   static constexpr uint32_t kKQChunk = kKQRows * 128u;
   static constexpr uint32_t kKQ = 2u * kKQChunk;
@@ -300,7 +301,7 @@ struct PrevSmem<true> {
 // state it so the register allocation avoids spills, that one (0: no
 // minimum) was measured faster with the default allocation.
 template <int NPM, bool FUSED, bool SB>
-__global__ void __launch_bounds__(kThreads, (NPM == 16 && !FUSED) ? 3 : ((SB || FUSED || NPM < 64) ? 2 : 0))
+__global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
     verify_tc_kernel(const __grid_constant__ CUtensorMap map_s0,
                      const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_q,
@@ -1071,8 +1072,8 @@ cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, const PrevRou
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel<NPM, FUSED, SB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(TcSmem<NPM, FUSED, SB>::kBytes));
-    // the whole unified L1/shared array as shared memory, so that the
-    // resident CTAs (two, three for 16-node trees) fit
+    // the whole unified L1/shared array as shared memory, so that two
+    // resident CTAs fit
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(verify_tc_kernel<NPM, FUSED, SB>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -1092,8 +1093,9 @@ template <bool SB>
 cudaError_t launch_tc(const treewy_batch& b, const VerifyMaps& m, const PrevRound* prev, int npm,
                       cudaStream_t stream) {
   if (prev == nullptr) {
+    // plain verification: trees of more than 16 nodes (smaller ones go to
+    // the small-tree and warp-MMA kernels)
     const PrevRound none{};
-    if (npm <= 16) return launch_npm<16, false, SB>(b, m, none, stream);
     if (npm <= 32) return launch_npm<32, false, SB>(b, m, none, stream);
     return launch_npm<64, false, SB>(b, m, none, stream);
   }

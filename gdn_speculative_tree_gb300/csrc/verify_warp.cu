@@ -1,0 +1,542 @@
+// verify_warp.cu -- TreeWY verification of trees of 9 to 16 nodes with
+// warp-level MMAs, dk = dv = 128, bf16 q/k/v, fp32 or bf16 committed state.
+//
+// One CTA of 256 threads per (request, head).  The state tile lands in
+// shared memory by bulk tensor copies; warp w owns 16 of its rows (value
+// dimensions) and carries them through every product of the method (TreeWY
+// paper §3 Eq. (2); review §3.2) with m16n8k16 bf16 MMAs (fp32 accumulation)
+// whose operands come straight from registers or shared memory:
+//
+//  MMA 1    S0 [K;Q]^T for the warp's rows: each state element is read once
+//           and split into hi + lo bf16 halves on the way (fp32 state: two
+//           MMAs per tile, 16 significant bits; a bf16 state needs one).
+//  W        in the accumulator registers: W[d][n] = beta_n v_n[d] -
+//           beta_n gamma_n (S0 k_n)[d], and the read-out's first term
+//           gamma_n (S0 q_n)[d]; the accumulator layout of MMA 1 is already
+//           the A-operand layout of MMA 2.
+//  Gram     warp w: slots 16w..16w+15 of [K;Q] times K^T, written over the
+//           warp's own (already read) rows of the state tile.
+//  rows     thread t builds operand row t of [T;B], T = (I + A)^-1 and
+//           B = M T restricted to node n's root path (both non-zero only
+//           there), by the recurrence x_q = r_q - sum_{a<q} x_a A[p_a, p_q]
+//           with A[m, j] = beta_m (gamma_m / gamma_j) k_j.k_m and
+//           r = e_0 (T) or M[n, p_q] = (gamma_n / gamma_{p_q}) k_{p_q}.q_n (B);
+//           the decay ratios are products of alpha along the path.
+//  MMA 2    [U | O] = W [T;B]^T (W and [T;B] in hi + lo bf16, three terms),
+//           O accumulated onto gamma_n S0 q_n; only the blocks of input nodes
+//           that can be ancestors of a tile's nodes (parents precede their
+//           children) are multiplied.
+//  store    each lane writes its two adjacent value rows of U[n] and o_n.
+//
+// The kernel is written for a capacity NPM of up to 64 nodes, but launched
+// for NPM = 16 only: three CTAs per SM fit (76 KB of shared memory, 80
+// registers), and the tile count is small.  At 32 nodes it measured level
+// with the tcgen05 kernel, at 64 nodes ~35 % slower: the first products take
+// two warp MMAs per 8-node tile and state element pair (hi and lo), and warp
+// MMAs run at ~0.47 m16n8k16 per cycle per SM, about a quarter of the tcgen05
+// rate, so two resident 64-node CTAs keep the MMA pipe saturated.
+#include "treewy_device.cuh"
+#include "treewy_internal.h"
+
+namespace treewy {
+namespace {
+
+constexpr int kWThreads = 256;
+constexpr int kWDim = 128;
+constexpr uint32_t kWBox = 128u * 128u;  // one 16 KB box: 128 rows x 128 bytes
+constexpr uint32_t kWKQStride = 288u;    // bf16 K/Q row: 256 bytes + 32 (bank offset)
+constexpr int kWRegPath = 8;             // root paths up to this long stay in registers
+
+template <int NPM>
+struct WarpTree {
+  uint64_t bar;  // state tile landed
+  int par[NPM];
+  float alpha[NPM];
+  float beta[NPM];
+  float4 coef[NPM];  // (beta_n, beta_n gamma_n, gamma_n, 0)
+};
+
+// Dynamic shared memory: alignment slack, a 64 KB region that first holds
+// the state tile (4 boxes of 32 fp32 or 2 of 64 bf16 columns, 128B swizzle)
+// and later the Gram rows (boxes 0-1: each warp over its own state rows) and
+// the hi and lo halves of the [T;B] operand (boxes 2 and 3), the 2 NPM K/Q
+// slot rows (later the x scratch of root paths longer than kWRegPath), the
+// tree.
+template <int NPM, bool SB>
+struct WarpCfg {
+  static constexpr int kSlots = 2 * NPM;  // keys 0..NPM-1, queries NPM..2NPM-1
+  static constexpr int kKT = NPM / 8;     // n8-tiles of keys (and of queries)
+  static constexpr uint32_t kKQOff = 4u * kWBox;
+  static constexpr uint32_t kKQBytes = kSlots * kWKQStride;
+  static constexpr uint32_t kTreeOff = kKQOff + kKQBytes;
+  static constexpr uint32_t kEnd = kTreeOff + static_cast<uint32_t>(sizeof(WarpTree<NPM>));
+  static constexpr uint32_t kDynSmem = 1024u + kEnd;
+  static constexpr int kBlocks = NPM == 16 ? 3 : 2;  // CTAs per SM
+  static_assert(kBlocks * (kDynSmem + 1024u) <= 228u * 1024u, "CTAs per SM");
+  static_assert(8u * NPM * NPM <= kKQBytes, "x scratch of 2 NPM long paths");
+  static_assert(2 * NPM <= kWThreads && NPM <= 64, "one operand row per thread");
+};
+
+// Fragment row g of a warp's tiles stands for state rows 16 w + 2 f(g) (row
+// g) and 16 w + 2 f(g) + 1 (row g + 8): a lane's two rows are adjacent, so
+// its v loads and U / o stores take both at once.  f pairs the fragment rows
+// that share a shared-memory load phase (2i and 2i + 1 for 16-byte loads of
+// an fp32 tile, 4i .. 4i + 3 for 8-byte loads of a bf16 tile) with rows of
+// distinct 128B-swizzle phases, so no tile load has a bank conflict.
+__device__ __forceinline__ int wfrag(int g) { return (g & 4) | ((g & 1) << 1) | ((g >> 1) & 1); }
+
+__device__ __forceinline__ uint2 wlds64(const unsigned char* p) {
+  return *reinterpret_cast<const uint2*>(p);
+}
+
+// m16n8k16 bf16 MMA (fragments as mma16816_bf16) without `volatile`: the
+// compiler may interleave independent products with the loads around them.
+__device__ __forceinline__ void wmma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const unsigned char* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+
+// Gram entry slot_m . key_i (fp32), row m of the Gram region: key columns
+// 0-31 in box 0, 32-63 in box 1 of the state region, at state row m (warp
+// m / 16 writes it over its own rows), words XOR-ed by (m mod 4) * 8 so that
+// the dump's 8-byte stores meet distinct banks.
+__device__ __forceinline__ uint32_t gram_off(int m, int i) {
+  return static_cast<uint32_t>((i >> 5) * kWBox + m * 128 + (((i & 31) ^ ((m & 3) << 3)) << 2));
+}
+
+// Byte of entry (o, i) of a [T;B] operand half: row o = output column (T rows
+// 0..NPM-1, B rows NPM..2NPM-1), i = input node; 16-byte chunks XOR-ed by
+// o mod 8 (ldmatrix reads 8 rows of one chunk column without conflicts).
+__device__ __forceinline__ uint32_t op_off(int o, int i) {
+  return static_cast<uint32_t>(o * 128 + ((((i >> 3) ^ (o & 7))) << 4) + ((i & 7) << 1));
+}
+
+__device__ __forceinline__ void put_op(unsigned char* oph, unsigned char* opl, int o, int i, float x) {
+  const __nv_bfloat16 xh = __float2bfloat16_rn(x);
+  const __nv_bfloat16 xl = __float2bfloat16_rn(x - __bfloat162float(xh));
+  const uint32_t off = op_off(o, i);
+  *reinterpret_cast<__nv_bfloat16*>(oph + off) = xh;
+  *reinterpret_cast<__nv_bfloat16*>(opl + off) = xl;
+}
+
+template <int NPM, bool SB>
+__global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
+    verify_warp_kernel(const __grid_constant__ CUtensorMap map_s0, const treewy_batch b) {
+  using C = WarpCfg<NPM, SB>;
+  constexpr int KT = C::kKT;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023u) & ~uintptr_t(1023));
+  unsigned char* s0 = base;
+  unsigned char* kqs = base + C::kKQOff;
+  WarpTree<NPM>& ts = *reinterpret_cast<WarpTree<NPM>*>(base + C::kTreeOff);
+
+  const int H = b.H;
+  const int r = blockIdx.x / H;
+  const int h = blockIdx.x - r * H;
+  const int t = threadIdx.x;
+  const int warp = t >> 5, lane = t & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const int sr0 = 16 * warp + 2 * wfrag(g);  // this lane's state rows sr0, sr0 + 1
+
+  // Every thread reads the request's metadata and checks it (the same
+  // outcome everywhere), so that its own loads follow one round trip later.
+  const int lo = __ldg(b.node_offset + r), hi = __ldg(b.node_offset + r + 1);
+  const int slot = __ldg(b.state_slot + r);
+  int flags = 0;
+  if (hi - lo < 0 || hi - lo > b.max_nodes) flags |= TREEWY_STATUS_TOO_MANY_NODES;
+  else if (lo < 0 || static_cast<int64_t>(hi) > b.T) flags |= TREEWY_STATUS_BAD_TREE;
+  if (slot < 0 || static_cast<int64_t>(slot) >= b.num_slots) flags |= TREEWY_STATUS_BAD_SLOT;
+  const int N = flags ? 0 : hi - lo;  // at most NPM (the launcher's max_nodes bound)
+  const bool issued = N > 0;
+  const int64_t rowstride = static_cast<int64_t>(H) * kWDim;
+  const int64_t node0 = static_cast<int64_t>(lo) * H + h;  // (node 0, head h) row
+
+  // the K/Q slot rows this thread copies: 16 bytes of slot 16 p + t / 16 per
+  // group p of 16 slots (two n8-tiles); groups of dead tiles are skipped
+  constexpr int kGroups = C::kSlots / 16;
+  uint4 kraw[kGroups];
+#pragma unroll
+  for (int p = 0; p < kGroups; ++p) {
+    kraw[p] = make_uint4(0u, 0u, 0u, 0u);
+    const int s = 16 * p + (t >> 4);
+    const int n = s < NPM ? s : s - NPM;
+    if (issued && n < N) {
+      const uint4* src = reinterpret_cast<const uint4*>(s < NPM ? b.k : b.q);
+      kraw[p] = __ldg(src + (node0 + static_cast<int64_t>(n) * H) * (kWDim / 8) + (t & 15));
+    }
+  }
+  // node t of the tree
+  int p_t = -1;
+  float al_t = 0.f, be_t = 0.f;
+  if (t < N) {
+    const int64_t rw = static_cast<int64_t>(lo) + t;
+    p_t = __ldg(b.parent + rw);
+    al_t = __ldg(b.alpha + rw * H + h);
+    be_t = __ldg(b.beta + rw * H + h);
+  }
+  // v_n at this lane's rows sr0, sr0 + 1 for the nodes n = 8 j + 2 q + e of
+  // its accumulator columns, as bf16 pairs
+  uint32_t vv[KT][2];
+  const unsigned short* vg = reinterpret_cast<const unsigned short*>(b.v);
+#pragma unroll
+  for (int j = 0; j < KT; ++j) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int n = 8 * j + 2 * q + e;
+      vv[j][e] = 0u;
+      if (n < N)
+        vv[j][e] = __ldg(reinterpret_cast<const uint32_t*>(vg + (node0 + static_cast<int64_t>(n) * H) * kWDim + sr0));
+    }
+  }
+  // the state tile, requested once this thread's own loads are on their way
+  if (t == 0) {
+    mbar_init(&ts.bar, 1);
+    fence_mbarrier_init();
+    if (issued) {
+      const int y = (slot * H + h) * kWDim;
+      mbar_arrive_expect_tx(&ts.bar, SB ? 2u * kWBox : 4u * kWBox);
+#pragma unroll
+      for (int c = 0; c < (SB ? 2 : 4); ++c)
+        tma_load_2d(s0 + c * kWBox, &map_s0, &ts.bar, (SB ? 64 : 32) * c, y);
+    }
+  }
+  const int live_tiles = (N + 7) >> 3;  // n8-tiles of keys holding a node
+#pragma unroll
+  for (int p = 0; p < kGroups; ++p) {
+    const int tile0 = 2 * p < KT ? 2 * p : 2 * p - KT;
+    if (tile0 < live_tiles)
+      *reinterpret_cast<uint4*>(kqs + (16 * p + (t >> 4)) * kWKQStride + (t & 15) * 16) = kraw[p];
+  }
+  bool bad = false;
+  if (t < N) {
+    bad = !(p_t >= -1 && p_t < t);
+    ts.par[t] = bad ? -1 : p_t;
+    ts.alpha[t] = al_t;
+    ts.beta[t] = be_t;
+  }
+  const bool bad_tree = __syncthreads_or(bad);
+  const bool work = issued && !bad_tree;
+
+  // gamma_n: the product of alpha over node n's root path
+  if (work && t < N) {
+    float c = 1.f;
+    for (int cur = t; cur >= 0; cur = ts.par[cur]) c *= ts.alpha[cur];
+    ts.coef[t] = make_float4(be_t, be_t * c, c, 0.f);
+  }
+  int fail = 0;
+  if (issued && t == 0 && !mbar_wait(&ts.bar, 0)) fail = 1;
+  fail = __syncthreads_or(fail);
+  const bool go = work && !fail;
+
+  if (go) {
+    // ---- MMA 1: acc[nt] = S0 [K;Q]^T, tile nt of slots 8 nt .. 8 nt + 7
+    //      (keys: nt < KT; queries: nt >= KT).  Within a k-step of 16 state
+    //      columns, k = 2q, 2q+1, 2q+8, 2q+9 stand for columns 4q .. 4q+3: a
+    //      lane reads one 16-byte granule (8 bytes of a bf16 state) per row.
+    float acc[2 * KT][4];
+#pragma unroll
+    for (int nt = 0; nt < 2 * KT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const int sw = sr0 & 7;  // sr0 + 1: sw ^ 1
+#pragma unroll 2
+    for (int ks = 0; ks < 8; ++ks) {
+      const int c0 = 16 * ks + 4 * q;
+      uint32_t ah[4], al4[4];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int rr = sr0 + hr;
+        const int sr = sw ^ hr;
+        if constexpr (SB) {
+          const uint2 raw = wlds64(s0 + (c0 >> 6) * kWBox + rr * 128 + ((((c0 & 63) >> 3) ^ sr) << 4) +
+                                   (c0 & 7) * 2);
+          ah[hr] = raw.x;
+          ah[2 + hr] = raw.y;
+        } else {
+          const float4 x = *reinterpret_cast<const float4*>(s0 + (c0 >> 5) * kWBox + rr * 128 +
+                                                            ((((c0 & 31) >> 2) ^ sr) << 4));
+          split_pair(x.x, x.y, ah[hr], al4[hr]);
+          split_pair(x.z, x.w, ah[2 + hr], al4[2 + hr]);
+        }
+      }
+      // groups of 4 tiles: their hi products, then their lo products, so
+      // that no MMA waits for the one before it
+#pragma unroll
+      for (int nt0 = 0; nt0 < 2 * KT; nt0 += 4) {
+        uint2 bk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int nt = nt0 + i;
+          bk[i] = make_uint2(0u, 0u);
+          if ((nt < KT ? nt : nt - KT) < live_tiles) bk[i] = wlds64(kqs + (8 * nt + g) * kWKQStride + c0 * 2);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int nt = nt0 + i;
+          if ((nt < KT ? nt : nt - KT) < live_tiles)
+            wmma16816(acc[nt], ah[0], ah[1], ah[2], ah[3], bk[i].x, bk[i].y);
+        }
+        if constexpr (!SB) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int nt = nt0 + i;
+            if ((nt < KT ? nt : nt - KT) < live_tiles)
+              wmma16816(acc[nt], al4[0], al4[1], al4[2], al4[3], bk[i].x, bk[i].y);
+          }
+        }
+      }
+    }
+
+    // ---- W in the key tiles, gamma_n S0 q_n in the query tiles (zero for
+    //      nodes past N), then W as MMA 2's A fragments in hi + lo bf16:
+    //      k-step s of input nodes 16 s .. 16 s + 15 is key tiles 2s, 2s+1
+#pragma unroll
+    for (int j = 0; j < KT; ++j) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int n = 8 * j + 2 * q + e;
+        float be = 0.f, bg = 0.f, gm = 0.f;
+        if (n < N) {
+          const float4 cf = ts.coef[n];
+          be = cf.x;
+          bg = cf.y;
+          gm = cf.z;
+        }
+        const float v0 = __uint_as_float(vv[j][e] << 16), v1 = __uint_as_float(vv[j][e] & 0xFFFF0000u);
+        acc[j][e] = fmaf(-bg, acc[j][e], be * v0);
+        acc[j][2 + e] = fmaf(-bg, acc[j][2 + e], be * v1);
+        acc[KT + j][e] *= gm;
+        acc[KT + j][2 + e] *= gm;
+      }
+    }
+    uint32_t wh[KT / 2][4], wl[KT / 2][4];
+#pragma unroll
+    for (int s = 0; s < KT / 2; ++s) {
+      split_pair(acc[2 * s][0], acc[2 * s][1], wh[s][0], wl[s][0]);
+      split_pair(acc[2 * s][2], acc[2 * s][3], wh[s][1], wl[s][1]);
+      split_pair(acc[2 * s + 1][0], acc[2 * s + 1][1], wh[s][2], wl[s][2]);
+      split_pair(acc[2 * s + 1][2], acc[2 * s + 1][3], wh[s][3], wl[s][3]);
+    }
+    float oi[KT][4];
+#pragma unroll
+    for (int j = 0; j < KT; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) oi[j][i] = acc[KT + j][i];
+
+    // ---- Gram: slots 16 warp .. 16 warp + 15 (fragment rows g, g + 8) times
+    //      the live key tiles, in passes of at most 4 tiles, written over the
+    //      warp's own rows of the state tile (all read above)
+    __syncwarp();
+    const int mt = warp < KT / 2 ? warp : warp - KT / 2;  // key tile pair of these slots
+    if (warp < KT && 2 * mt < live_tiles) {
+      constexpr int kGP = KT < 4 ? KT : 4;
+#pragma unroll
+      for (int gp = 0; gp < KT / kGP; ++gp) {
+        if (kGP * gp < live_tiles) {
+          float gd[kGP][4];
+#pragma unroll
+          for (int i = 0; i < kGP; ++i) gd[i][0] = gd[i][1] = gd[i][2] = gd[i][3] = 0.f;
+#pragma unroll 2
+          for (int ks = 0; ks < 8; ++ks) {
+            const int cb = (16 * ks + 4 * q) * 2;
+            const uint2 x0 = wlds64(kqs + (16 * warp + g) * kWKQStride + cb);
+            const uint2 x1 = wlds64(kqs + (16 * warp + g + 8) * kWKQStride + cb);
+#pragma unroll
+            for (int i = 0; i < kGP; ++i) {
+              if (kGP * gp + i < live_tiles) {
+                const uint2 bk = wlds64(kqs + (8 * (kGP * gp + i) + g) * kWKQStride + cb);
+                wmma16816(gd[i], x0.x, x1.x, x0.y, x1.y, bk.x, bk.y);
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kGP; ++i) {
+            const int col = 8 * (kGP * gp + i) + 2 * q;
+            const int m0 = 16 * warp + g;
+            *reinterpret_cast<float2*>(s0 + gram_off(m0, col)) = make_float2(gd[i][0], gd[i][1]);
+            *reinterpret_cast<float2*>(s0 + gram_off(m0 + 8, col)) = make_float2(gd[i][2], gd[i][3]);
+          }
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- operand rows of [T;B]: thread t < NPM the T row of node t, thread
+    //      NPM + n the B row of node n, over boxes 2 (hi) and 3 (lo)
+    unsigned char* oph = s0 + 2 * kWBox;
+    unsigned char* opl = s0 + 3 * kWBox;
+    if (t < 2 * NPM) {
+      const bool isB = t >= NPM;
+      const int n = isB ? t - NPM : t;
+      if (n < N) {
+#pragma unroll
+        for (int c = 0; c < NPM / 8; ++c) {
+          const uint32_t off = static_cast<uint32_t>(t * 128 + ((c ^ (t & 7)) << 4));
+          *reinterpret_cast<uint4*>(oph + off) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(opl + off) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        const unsigned char* gq = s0;  // Gram rows: key slot m = node m, query slot NPM + n
+        auto G = [&](int m, int i) { return *reinterpret_cast<const float*>(gq + gram_off(m, i)); };
+        int pn[kWRegPath];
+        float al[kWRegPath], be[kWRegPath], x[kWRegPath];
+        int L = 0, cur = n;
+#pragma unroll
+        for (int s = 0; s < kWRegPath; ++s) {
+          pn[s] = 0;
+          al[s] = 0.f;
+          be[s] = 0.f;
+          if (cur >= 0) {
+            pn[s] = cur;
+            al[s] = ts.alpha[cur];
+            be[s] = ts.beta[cur];
+            cur = ts.par[cur];
+            ++L;
+          }
+        }
+        if (cur < 0) {
+          // root path of at most kWRegPath nodes: x in registers
+          float c = 1.f;
+#pragma unroll
+          for (int s = 0; s < kWRegPath; ++s) {
+            x[s] = isB ? ((s < L) ? c * G(NPM + n, pn[s]) : 0.f) : (s == 0 ? 1.f : 0.f);
+            c *= al[s];
+          }
+#pragma unroll
+          for (int qq = 1; qq < kWRegPath; ++qq) {
+            if (qq < L) {
+              float rt = 1.f;  // gamma_{p_a} / gamma_{p_qq}
+#pragma unroll
+              for (int a = qq - 1; a >= 0; --a) {
+                rt *= al[a];
+                x[qq] = fmaf(-x[a] * be[a] * rt, G(pn[a], pn[qq]), x[qq]);
+              }
+            }
+          }
+#pragma unroll
+          for (int s = 0; s < kWRegPath; ++s)
+            if (s < L) put_op(oph, opl, t, pn[s], x[s]);
+        } else {
+          // longer root path: x in this thread's scratch row (the K/Q region
+          // is free: every product that reads it is complete), each settled
+          // x_a pushed into the later entries
+          float* xs = reinterpret_cast<float*>(kqs) + t * NPM;
+          float c = 1.f;
+          L = 0;
+          for (int cu = n; cu >= 0; cu = ts.par[cu]) {
+            xs[L] = isB ? c * G(NPM + n, cu) : (L == 0 ? 1.f : 0.f);
+            c *= ts.alpha[cu];
+            ++L;
+          }
+          int pa = n;
+          for (int a = 0; a + 1 < L; ++a) {
+            const float ba = ts.beta[pa] * xs[a];
+            float rt = 1.f;
+            int node = pa;
+            for (int qq = a + 1; qq < L; ++qq) {
+              rt *= ts.alpha[node];
+              node = ts.par[node];
+              xs[qq] = fmaf(-ba * rt, G(pa, node), xs[qq]);
+            }
+            pa = ts.par[pa];
+          }
+          int node = n;
+          for (int s = 0; s < L; ++s, node = ts.par[node]) put_op(oph, opl, t, node, xs[s]);
+        }
+      }
+    }
+    if (b.gamma != nullptr && t < N) b.gamma[node0 + static_cast<int64_t>(t) * H] = ts.coef[t].z;
+    __syncthreads();
+
+    // ---- MMA 2 and the stores, per pair of output tiles (16 nodes): O onto
+    //      gamma S0 q, then U; input k-steps up to the pair's own (a node's
+    //      ancestors have smaller indices)
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const bool isO = part == 0;
+      float* dstb = (isO ? b.o : b.U) + node0 * kWDim + sr0;
+#pragma unroll
+      for (int jp = 0; jp < KT / 2; ++jp) {
+        if (16 * jp < N) {
+          float d[2][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            d[0][i] = isO ? oi[2 * jp][i] : 0.f;
+            d[1][i] = isO ? oi[2 * jp + 1][i] : 0.f;
+          }
+          const int orow = (isO ? NPM : 0) + 16 * jp + ((lane >> 4) << 3) + (lane & 7);
+#pragma unroll
+          for (int s = 0; s <= jp; ++s) {
+            uint32_t bh[4], bl[4];
+            const uint32_t off = op_off(orow, 16 * s + ((lane >> 3) & 1) * 8);
+            ldsm_x4(bh, oph + off);
+            ldsm_x4(bl, opl + off);
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt)
+              wmma16816(d[tt], wh[s][0], wh[s][1], wh[s][2], wh[s][3], bh[2 * tt], bh[2 * tt + 1]);
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt)
+              wmma16816(d[tt], wl[s][0], wl[s][1], wl[s][2], wl[s][3], bh[2 * tt], bh[2 * tt + 1]);
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt)
+              wmma16816(d[tt], wh[s][0], wh[s][1], wh[s][2], wh[s][3], bl[2 * tt], bl[2 * tt + 1]);
+          }
+#pragma unroll
+          for (int tt = 0; tt < 2; ++tt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int n = 16 * jp + 8 * tt + 2 * q + e;
+              if (n < N)
+                *reinterpret_cast<float2*>(dstb + static_cast<int64_t>(n) * rowstride) =
+                    make_float2(d[tt][e], d[tt][2 + e]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  if (t == 0) {
+    int bits = fail ? kStatusTimeout : 0;
+    if (h == 0) bits |= flags | (issued && bad_tree ? TREEWY_STATUS_BAD_TREE : 0);
+    if (bits) atomicOr(b.status + r, bits);
+    // no copy may still target this CTA's memory at exit
+    if (fail) mbar_wait(&ts.bar, 0);
+  }
+}
+
+template <int NPM, bool SB>
+cudaError_t launch_warp(const treewy_batch& b, const CUtensorMap& map_s0, cudaStream_t stream) {
+  using C = WarpCfg<NPM, SB>;
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t attr = once_per_device(attr_done, [] {
+    cudaError_t e = cudaFuncSetAttribute(verify_warp_kernel<NPM, SB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kDynSmem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(verify_warp_kernel<NPM, SB>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    return e;
+  });
+  if (attr != cudaSuccess) return attr;
+  const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
+  verify_warp_kernel<NPM, SB><<<grid, kWThreads, C::kDynSmem, stream>>>(map_s0, b);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_verify_warp(const treewy_batch& b, const CUtensorMap& map_s0, cudaStream_t stream) {
+  static_assert(kWarpTreeNodes == 16, "launched for the 16-node capacity");
+  const bool sb = (b.flags & TREEWY_FLAG_STATE_BF16) != 0;
+  return sb ? launch_warp<16, true>(b, map_s0, stream) : launch_warp<16, false>(b, map_s0, stream);
+}
+
+}  // namespace treewy

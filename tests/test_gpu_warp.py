@@ -1,0 +1,212 @@
+"""GPU parity of the warp-MMA verification (batches whose trees have at most
+16 nodes and more than 8: dk = dv = 128 with bf16 q/k/v) against the oracle
+on the same seeded inputs: every size from 1 to 16 in chain, star, forest and
+random shapes (chains longer than 8 take the kernel's general root-path
+recurrence, shorter paths its register form), the smallest capacity routed
+to it (9), ragged batches with empty trees, gates at the ends of their range,
+a bf16 state pool, device-side errors, CUDA-graph replay, and agreement with
+the small-tree and tcgen05 kernels on the same inputs.  Tolerances as in
+gpu_helpers (o, U: 2e-3 of the largest reference value; committed state
+1e-3; gamma 1e-5 relative).
+"""
+import types
+
+import numpy as np
+import pytest
+import torch
+
+from gdn_speculative_tree_gb300 import binding
+from gdn_speculative_tree_gb300 import workloads as wl
+from oracle import gdn_tree_oracle as orc
+from tests.gpu_helpers import (CudaRun, FLT_MIN, G_TOL, O_TOL, U_TOL, assert_within, compare, np32,
+                               oracle_request)
+from tests.test_gpu_small import custom, random_tree, shapes
+
+pytestmark = pytest.mark.gpu
+
+CAP = 16  # node capacity of the warp-MMA kernel
+
+
+def test_warp_every_size_and_shape(cuda_lib):
+    trees, acc = shapes(CAP)
+    w = custom(trees, acc)
+    assert w.max_nodes == CAP
+    run = CudaRun(w)
+    assert not run.status.any()
+    assert_within(compare(w, run, range(w.R)), "warp kernel shapes")
+
+
+@pytest.mark.parametrize("max_nodes,sizes", [(9, [9, 1, 9, 0, 4]), (16, [16]), (12, [12, 11, 3])])
+def test_warp_capacities(cuda_lib, max_nodes, sizes):
+    """The smallest capacity routed to the kernel (9) and full trees at it."""
+    rng = np.random.default_rng(max_nodes + len(sizes))
+    trees = [random_tree(rng, n) for n in sizes]
+    if sizes[0] == 16:
+        trees = [wl.chain_parents(16)]  # the longest root path
+    acc = [len(t) - 1 for t in trees]
+    w = custom(trees, acc, H=2, max_nodes=max_nodes)
+    run = CudaRun(w)
+    assert not run.status.any()
+    assert_within(compare(w, run, range(w.R)), f"capacity {max_nodes}, sizes {sizes}")
+
+
+@pytest.mark.parametrize("sizes,H", [([0, 13, 0, 16, 1, 0, 9], 5), ([15] * 7 + [0], 1), ([10, 2, 14, 0], 7)])
+def test_warp_ragged_with_empty_trees(cuda_lib, sizes, H):
+    rng = np.random.default_rng(sum(sizes) + H)
+    trees = [random_tree(rng, n) for n in sizes]
+    acc = [len(t) - 1 for t in trees]
+    w = custom(trees, acc, H=H, max_nodes=CAP)
+    run = CudaRun(w)
+    assert not run.status.any()
+    assert_within(compare(w, run, range(w.R)), f"ragged {sizes}")
+
+
+@pytest.mark.parametrize("alpha,beta", [((1.0, 1.0), ("const", 1.0)),
+                                        ((0.9, 0.999), ("const", 0.0)),
+                                        ((0.01, 0.05), ("uniform", 0.05, 0.95)),
+                                        ((0.999999, 0.9999999), ("uniform", 0.9999, 0.99999))])
+def test_warp_gate_edges(cuda_lib, alpha, beta):
+    trees, acc = shapes(CAP)
+    w = custom(trees, acc, alpha=alpha, beta=beta, seed=41)
+    run = CudaRun(w)
+    assert not run.status.any()
+    assert_within(compare(w, run, range(w.R)), f"gates {alpha} {beta}")
+
+
+def test_warp_agrees_with_other_kernels(cuda_lib):
+    """The same batch through the warp-MMA kernel (max_nodes 16) and the
+    tcgen05 kernel (max_nodes 32), and its trees of at most 8 nodes through
+    the small-tree kernel as well: all within tolerance of the oracle and of
+    each other, with identical decays (the same products of alpha in the same
+    order)."""
+    trees, acc = shapes(CAP)
+    runs = {}
+    for name, mn in (("warp", 16), ("tcgen05", 32)):
+        w = custom(trees, acc, seed=5)
+        runs[name] = (w, CudaRun(w, max_nodes=mn))
+    for name, (w, run) in runs.items():
+        assert not run.status.any(), name
+        assert_within(compare(w, run, range(w.R)), name)
+    warp, tc = runs["warp"][1], runs["tcgen05"][1]
+    assert float(np.abs(warp.o - tc.o).max()) <= 2 * O_TOL * float(np.abs(tc.o).max())
+    assert float(np.abs(warp.U - tc.U).max()) <= 2 * U_TOL * float(np.abs(tc.U).max())
+    assert np.array_equal(warp.gamma, tc.gamma)
+    small_trees = [t for t in trees if len(t) <= 8]
+    small_acc = [a for t, a in zip(trees, acc) if len(t) <= 8]
+    ws, ww = custom(small_trees, small_acc, seed=9), custom(small_trees, small_acc, seed=9)
+    small, warp8 = CudaRun(ws), CudaRun(ww, max_nodes=16)
+    assert not small.status.any() and not warp8.status.any()
+    assert_within(compare(ww, warp8, range(ww.R)), "warp kernel, trees of at most 8 nodes")
+    assert float(np.abs(warp8.o - small.o).max()) <= 2 * O_TOL * float(np.abs(small.o).max())
+    assert np.array_equal(warp8.gamma, small.gamma)
+
+
+def test_warp_deterministic(cuda_lib):
+    trees, acc = shapes(CAP)
+    w = custom(trees, acc)
+    tv = binding.TreeVerifier(w)
+    tv.verify()
+    o1, u1 = tv.o.clone(), tv.U.clone()
+    tv.verify()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, tv.o) and torch.equal(u1, tv.U)
+
+
+def test_warp_bf16_state(cuda_lib):
+    """A bf16 state pool: verification reads the bf16 S0 exactly (o and U to
+    the fp32 tolerances), the commit rounds S_a once to bf16:
+    |S_gpu - S_ref| <= 2^-8 |S_ref| + 1e-3 max|S_ref|."""
+    trees, acc = shapes(CAP)
+    w = custom(trees, acc, seed=73, state_dtype="bf16")
+    run = CudaRun(w, flags=binding.FLAG_STATE_BF16)
+    assert not run.status.any()
+    slot = w.state_slot.cpu().numpy()
+    o_err = o_max = u_err = u_max = g_err = 0.0
+    for r in range(w.R):
+        lo, hi, S0, ref = oracle_request(w, r, run.S0_pool)
+        o_err = max(o_err, float(np.abs(run.o[lo:hi] - ref.o).max()))
+        o_max = max(o_max, float(np.abs(ref.o).max()))
+        u_err = max(u_err, float(np.abs(run.U[lo:hi] - ref.U).max()))
+        u_max = max(u_max, float(np.abs(ref.U).max()))
+        g_err = max(g_err, float((np.abs(run.gamma[lo:hi] - ref.gamma) /
+                                  np.maximum(ref.gamma, FLT_MIN)).max()))
+        S_ref = orc.commit_request(S0, ref, int(acc[r]))
+        S_gpu = np32(w.state[int(slot[r])]).astype(np.float64)
+        bound = 2.0 ** -8 * np.abs(S_ref) + 1e-3 * np.abs(S_ref).max()
+        assert np.all(np.abs(S_gpu - S_ref) <= bound), r
+    assert o_err <= O_TOL * o_max, (o_err, o_max)
+    assert u_err <= U_TOL * u_max, (u_err, u_max)
+    assert g_err <= G_TOL, g_err
+
+
+def test_warp_bad_inputs_set_status_and_spare_others(cuda_lib):
+    rng = np.random.default_rng(29)
+    trees = [random_tree(rng, n) for n in (12, 15, 16, 10, 9, 14)]
+    trees[1][11] = 13                      # parent after child
+    trees[5][13] = 13                      # parent is the node itself
+    acc = [3, 2, 1, 10, 0, 1]              # request 3: accepted outside its 10-node tree
+    w = custom(trees, acc, max_nodes=CAP, extra_slots=2)
+    slots = w.state_slot.clone()
+    slots[4] = -1                          # outside the pool
+    w.state_slot.copy_(slots)
+    tv = binding.TreeVerifier(w, max_nodes=15)  # request 2 (16 nodes) exceeds it
+    tv.o.fill_(float("nan"))
+    tv.U.fill_(float("nan"))
+    S_before = w.state.clone()
+    tv.verify()
+    tv.commit()
+    torch.cuda.synchronize()
+    st = tv.status.cpu().tolist()
+    assert st[0] == 0
+    assert st[1] & binding.STATUS_BAD_TREE
+    assert st[2] & binding.STATUS_TOO_MANY_NODES
+    assert st[3] == binding.STATUS_BAD_ACCEPTED
+    assert st[4] & binding.STATUS_BAD_SLOT
+    assert st[5] & binding.STATUS_BAD_TREE
+    node = w.node_offset.cpu().tolist()
+    for r in (1, 2, 4, 5):
+        assert torch.isnan(tv.o[node[r]:node[r + 1]]).all()
+        assert torch.isnan(tv.U[node[r]:node[r + 1]]).all()
+    for r in (1, 2, 3, 5):  # state untouched where the commit was refused
+        s = int(w.state_slot[r])
+        assert torch.equal(w.state[s], S_before[s])
+    for r in (0, 3):        # verified normally
+        lo, hi, S0, ref = oracle_request(w, r, S_before.cpu())
+        assert np.abs(np32(tv.o[lo:hi]) - ref.o).max() <= O_TOL * np.abs(ref.o).max()
+        assert np.abs(np32(tv.U[lo:hi]) - ref.U).max() <= U_TOL * np.abs(ref.U).max()
+
+
+def test_warp_graph_replay_matches_eager(cuda_lib):
+    """The binary-tree workload's verify + commit captured in a CUDA graph and
+    replayed: the oracle's results within the tolerances, and the eager
+    launches' bit for bit."""
+    cfg = wl.CONFIGS["binary"]
+    w_eager = wl.generate(cfg, R=12).to("cuda")
+    run = CudaRun(w_eager)
+    w = wl.generate(cfg, R=12).to("cuda")
+    assert 8 < w.max_nodes <= CAP
+    S0 = w.state.clone()
+    tv = binding.TreeVerifier(w)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        tv.verify(s)
+        w.state.copy_(S0)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tv.verify()
+        tv.commit()
+    w.state.copy_(S0)
+    tv.o.fill_(float("nan"))
+    tv.U.fill_(float("nan"))
+    tv.gamma.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert not tv.status.any()
+    replay = types.SimpleNamespace(o=np32(tv.o), U=np32(tv.U), gamma=np32(tv.gamma),
+                                   S0_pool=S0.cpu(), S_after=w.state)
+    assert_within(compare(w, replay, range(w.R)), "binary graph replay")
+    assert torch.equal(tv.o.cpu(), torch.from_numpy(run.o))
+    assert torch.equal(w.state.cpu(), run.S_after.cpu())
