@@ -246,6 +246,35 @@ __device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The same MMA without `volatile`: the compiler may interleave independent
+// products with the loads around them.
+__device__ __forceinline__ void mma16816_bf16_nv(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                 uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four 8 x 8 b16 matrices from shared memory (ldmatrix): lanes 8i .. 8i+7
+// give the row addresses of matrix i (16-byte aligned), and lane (g, q) =
+// (lane / 4, lane % 4) receives elements 2q, 2q+1 of row g of matrix i in
+// r[i]: the B fragments of a warp MMA for two n8-tiles when the matrices are
+// (tile 0, k 0-7), (tile 0, k 8-15), (tile 1, k 0-7), (tile 1, k 8-15).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+
+// Byte of entry (row o, column i) of a K-major bf16 operand with 128-byte
+// rows and 128-byte swizzle (16-byte chunk i / 8 of row o at position
+// (i / 8) XOR (o mod 8)), which ldmatrix reads without bank conflicts (eight
+// rows of one chunk column).
+__device__ __forceinline__ uint32_t sw128_off(int o, int i) {
+  return static_cast<uint32_t>(o * 128 + ((((i >> 3) ^ (o & 7))) << 4) + ((i & 7) << 1));
+}
+
 // 16 consecutive 32-bit TMEM columns of this thread's lane.  The hardware
 // writes the target registers asynchronously, until tcgen05.wait::ld; the
 // compiler sees them as written here, so the matching wait (tmem_wait16 /

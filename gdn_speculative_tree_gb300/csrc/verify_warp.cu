@@ -89,22 +89,6 @@ __device__ __forceinline__ uint2 wlds64(const unsigned char* p) {
   return *reinterpret_cast<const uint2*>(p);
 }
 
-// m16n8k16 bf16 MMA (fragments as mma16816_bf16) without `volatile`: the
-// compiler may interleave independent products with the loads around them.
-__device__ __forceinline__ void wmma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const unsigned char* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p)));
-}
-
 // Gram entry slot_m . key_i (fp32), row m of the Gram region: key columns
 // 0-31 in box 0, 32-63 in box 1 of the state region, at state row m (warp
 // m / 16 writes it over its own rows), words XOR-ed by (m mod 4) * 8 so that
@@ -113,17 +97,13 @@ __device__ __forceinline__ uint32_t gram_off(int m, int i) {
   return static_cast<uint32_t>((i >> 5) * kWBox + m * 128 + (((i & 31) ^ ((m & 3) << 3)) << 2));
 }
 
-// Byte of entry (o, i) of a [T;B] operand half: row o = output column (T rows
-// 0..NPM-1, B rows NPM..2NPM-1), i = input node; 16-byte chunks XOR-ed by
-// o mod 8 (ldmatrix reads 8 rows of one chunk column without conflicts).
-__device__ __forceinline__ uint32_t op_off(int o, int i) {
-  return static_cast<uint32_t>(o * 128 + ((((i >> 3) ^ (o & 7))) << 4) + ((i & 7) << 1));
-}
-
+// [T;B] operand halves: row o = output column (T rows 0..NPM-1, B rows
+// NPM..2NPM-1), column i = input node, in the 128-byte swizzled layout
+// (sw128_off).
 __device__ __forceinline__ void put_op(unsigned char* oph, unsigned char* opl, int o, int i, float x) {
   const __nv_bfloat16 xh = __float2bfloat16_rn(x);
   const __nv_bfloat16 xl = __float2bfloat16_rn(x - __bfloat162float(xh));
-  const uint32_t off = op_off(o, i);
+  const uint32_t off = sw128_off(o, i);
   *reinterpret_cast<__nv_bfloat16*>(oph + off) = xh;
   *reinterpret_cast<__nv_bfloat16*>(opl + off) = xl;
 }
@@ -282,14 +262,14 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
         for (int i = 0; i < 4; ++i) {
           const int nt = nt0 + i;
           if ((nt < KT ? nt : nt - KT) < live_tiles)
-            wmma16816(acc[nt], ah[0], ah[1], ah[2], ah[3], bk[i].x, bk[i].y);
+            mma16816_bf16_nv(acc[nt], ah[0], ah[1], ah[2], ah[3], bk[i].x, bk[i].y);
         }
         if constexpr (!SB) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int nt = nt0 + i;
             if ((nt < KT ? nt : nt - KT) < live_tiles)
-              wmma16816(acc[nt], al4[0], al4[1], al4[2], al4[3], bk[i].x, bk[i].y);
+              mma16816_bf16_nv(acc[nt], al4[0], al4[1], al4[2], al4[3], bk[i].x, bk[i].y);
           }
         }
       }
@@ -353,7 +333,7 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
             for (int i = 0; i < kGP; ++i) {
               if (kGP * gp + i < live_tiles) {
                 const uint2 bk = wlds64(kqs + (8 * (kGP * gp + i) + g) * kWKQStride + cb);
-                wmma16816(gd[i], x0.x, x1.x, x0.y, x1.y, bk.x, bk.y);
+                mma16816_bf16_nv(gd[i], x0.x, x1.x, x0.y, x1.y, bk.x, bk.y);
               }
             }
           }
@@ -475,18 +455,18 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
 #pragma unroll
           for (int s = 0; s <= jp; ++s) {
             uint32_t bh[4], bl[4];
-            const uint32_t off = op_off(orow, 16 * s + ((lane >> 3) & 1) * 8);
+            const uint32_t off = sw128_off(orow, 16 * s + ((lane >> 3) & 1) * 8);
             ldsm_x4(bh, oph + off);
             ldsm_x4(bl, opl + off);
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
-              wmma16816(d[tt], wh[s][0], wh[s][1], wh[s][2], wh[s][3], bh[2 * tt], bh[2 * tt + 1]);
+              mma16816_bf16_nv(d[tt], wh[s][0], wh[s][1], wh[s][2], wh[s][3], bh[2 * tt], bh[2 * tt + 1]);
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
-              wmma16816(d[tt], wl[s][0], wl[s][1], wl[s][2], wl[s][3], bh[2 * tt], bh[2 * tt + 1]);
+              mma16816_bf16_nv(d[tt], wl[s][0], wl[s][1], wl[s][2], wl[s][3], bh[2 * tt], bh[2 * tt + 1]);
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
-              wmma16816(d[tt], wh[s][0], wh[s][1], wh[s][2], wh[s][3], bl[2 * tt], bl[2 * tt + 1]);
+              mma16816_bf16_nv(d[tt], wh[s][0], wh[s][1], wh[s][2], wh[s][3], bl[2 * tt], bl[2 * tt + 1]);
           }
 #pragma unroll
           for (int tt = 0; tt < 2; ++tt) {
