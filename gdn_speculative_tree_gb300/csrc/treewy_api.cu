@@ -195,7 +195,7 @@ treewy_status treewy_verify(const treewy_batch* batch, cudaStream_t stream) {
     if (st != TREEWY_OK) return st;
     err = batch->max_nodes <= treewy::kSmallTreeNodes
               ? treewy::launch_verify_small(*batch, map, nullptr, stream)
-              : treewy::launch_verify_warp(*batch, map, stream);
+              : treewy::launch_verify_warp(*batch, map, nullptr, stream);
   } else if (use_tensor_cores(batch) && batch->T > 0) {
     treewy::VerifyMaps maps;
     st = make_maps(batch, &maps);
@@ -234,11 +234,11 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
   if (!prev->U && prev->T > 0) return fail(TREEWY_ERR_INVALID_ARG, "prev->U is NULL");
   if (!prev_accepted) return fail(TREEWY_ERR_INVALID_ARG, "prev_accepted is NULL");
   cudaError_t err;
-  // The small-tree kernel applies an accepted path 8 entries per pass over
-  // the state tile; a bf16 pool is rounded at the end of each pass, so it
-  // takes the fused form only while every path fits one pass (S_a rounded
-  // once, as the separate commit does).
-  const bool small = next->max_nodes <= treewy::kSmallTreeNodes;
+  // The small-tree and warp-MMA kernels apply an accepted path 8 entries per
+  // pass over the state tile; a bf16 pool is rounded at the end of each pass,
+  // so it takes their fused form only while every path fits one pass (S_a
+  // rounded once, as the separate commit does).
+  const bool small = next->max_nodes <= treewy::kWarpTreeNodes;
   const bool small_fused_ok =
       !(next->flags & TREEWY_FLAG_STATE_BF16) || prev->max_nodes <= treewy::kSmallTreeNodes;
   if (use_tensor_cores(next) && next->T > 0 && prev->qkv_dtype == TREEWY_DTYPE_BF16 &&
@@ -257,7 +257,9 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
       CUtensorMap map;
       st = make_state_map(next, &map);
       if (st != TREEWY_OK) return st;
-      err = treewy::launch_verify_small(*next, map, &pr, stream);
+      err = next->max_nodes <= treewy::kSmallTreeNodes
+                ? treewy::launch_verify_small(*next, map, &pr, stream)
+                : treewy::launch_verify_warp(*next, map, &pr, stream);
     } else {
       treewy::VerifyMaps maps;
       st = make_maps(next, &maps);

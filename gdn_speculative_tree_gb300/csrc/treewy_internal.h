@@ -73,7 +73,7 @@ cudaError_t launch_verify_small(const treewy_batch& b, const CUtensorMap& state_
 // run at several times the rate of warp-level MMAs.
 constexpr int kWarpTreeNodes = 16;
 cudaError_t launch_verify_warp(const treewy_batch& b, const CUtensorMap& state_map,
-                               cudaStream_t stream);
+                               const PrevRound* prev, cudaStream_t stream);
 
 // npm: padded tree capacity (16, 32 or 64).
 size_t verify_tc_smem(int npm);

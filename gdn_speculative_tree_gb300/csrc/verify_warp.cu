@@ -56,6 +56,25 @@ struct WarpTree {
   float4 coef[NPM];  // (beta_n, beta_n gamma_n, gamma_n, 0)
 };
 
+// The previous round's tree and the accepted node's root path, for the
+// commit fused in front of the verification; with kWSeg bf16 key rows of the
+// path, they sit in the K/Q region until the update is applied (the K/Q rows
+// wait in registers meanwhile).
+struct WarpPrev {
+  int parent[kMaxNodes];
+  float alpha[kMaxNodes];
+  float c[kMaxNodes];        // gamma_a / gamma_{path j} as products of alpha
+  uint8_t path[kMaxNodes];   // accepted node, its parent, ... (root last)
+  float w[8];                // previous trees of at most 8 nodes: c_j by node
+  int onpath;                // ... and the nodes on the accepted path (bit j)
+  int len;
+  float gamma_a;
+};
+constexpr int kWSeg = 8;              // path entries applied per pass over the tile
+constexpr uint32_t kWPathStride = 272u;  // bf16 key row of the path: 256 + 16
+constexpr uint32_t kWPathOff = 1024u;    // key rows after WarpPrev in the K/Q region
+static_assert(sizeof(WarpPrev) <= kWPathOff, "previous tree before the key rows");
+
 // Dynamic shared memory: alignment slack, a 64 KB region that first holds
 // the state tile (4 boxes of 32 fp32 or 2 of 64 bf16 columns, 128B swizzle)
 // and later the Gram rows (boxes 0-1: each warp over its own state rows) and
@@ -75,6 +94,7 @@ struct WarpCfg {
   static_assert(kBlocks * (kDynSmem + 1024u) <= 228u * 1024u, "CTAs per SM");
   static_assert(8u * NPM * NPM <= kKQBytes, "x scratch of 2 NPM long paths");
   static_assert(2 * NPM <= kWThreads && NPM <= 64, "one operand row per thread");
+  static_assert(kWPathOff + kWSeg * kWPathStride <= kKQBytes, "fused commit staging");
 };
 
 // Fragment row g of a warp's tiles stands for state rows 16 w + 2 f(g) (row
@@ -108,9 +128,19 @@ __device__ __forceinline__ void put_op(unsigned char* oph, unsigned char* opl, i
   *reinterpret_cast<__nv_bfloat16*>(opl + off) = xl;
 }
 
-template <int NPM, bool SB>
+// FUSED: the previous round's commit first, S_a = gamma_a S0 +
+// sum_{j in path(a)} c_j u_j k_j^T with c_j = gamma_a / gamma_j (TreeWY paper
+// §3 "Reconstruct on commit"), applied to the state tile by update passes
+// (two warp MMAs per 8-column tile and 8 path entries: A = c_j u_j of the
+// warp's rows split into hi + lo bf16, B = the entries' key rows, the D
+// columns ordered so that each lane's update lands on the elements it holds),
+// written back to the pool once; the verification then runs from S_a.  Each
+// half runs exactly when its separate call would: a refused commit leaves the
+// state alone, a bad next tree still commits.
+template <int NPM, bool SB, bool FUSED>
 __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
-    verify_warp_kernel(const __grid_constant__ CUtensorMap map_s0, const treewy_batch b) {
+    verify_warp_kernel(const __grid_constant__ CUtensorMap map_s0, const treewy_batch b,
+                       const PrevRound prev) {
   using C = WarpCfg<NPM, SB>;
   constexpr int KT = C::kKT;
   extern __shared__ unsigned char smem_raw[];
@@ -119,6 +149,8 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
   unsigned char* s0 = base;
   unsigned char* kqs = base + C::kKQOff;
   WarpTree<NPM>& ts = *reinterpret_cast<WarpTree<NPM>*>(base + C::kTreeOff);
+  WarpPrev& pv = *reinterpret_cast<WarpPrev*>(kqs);  // FUSED only
+  unsigned char* pathk = kqs + kWPathOff;             // FUSED only
 
   const int H = b.H;
   const int r = blockIdx.x / H;
@@ -138,6 +170,26 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
   if (slot < 0 || static_cast<int64_t>(slot) >= b.num_slots) flags |= TREEWY_STATUS_BAD_SLOT;
   const int N = flags ? 0 : hi - lo;  // at most NPM (the launcher's max_nodes bound)
   const bool issued = N > 0;
+  const bool bad_slot = (flags & TREEWY_STATUS_BAD_SLOT) != 0;
+  // the previous round's request: its errors refuse the commit only
+  int cflags = 0, commit_a = -1, plo = 0, pn = 0;
+  if constexpr (FUSED) {
+    const int pa = __ldg(prev.accepted + r);
+    plo = __ldg(prev.node_offset + r);
+    const int phi = __ldg(prev.node_offset + r + 1);
+    pn = phi - plo;
+    if (pa != -1) {
+      if (pn < 0 || pn > prev.max_nodes) cflags |= TREEWY_STATUS_TOO_MANY_NODES;
+      else if (plo < 0 || static_cast<int64_t>(phi) > prev.T) cflags |= TREEWY_STATUS_BAD_TREE;
+      if (pa < -1 || pa >= pn) cflags |= TREEWY_STATUS_BAD_ACCEPTED;
+      if (cflags || bad_slot) cflags |= TREEWY_STATUS_COMMIT_REFUSED;
+    }
+    commit_a = cflags ? -1 : pa;
+  }
+  const bool have_s0 = issued || commit_a >= 0;
+  // a commit to apply keeps the K/Q region for its staging: the K/Q rows
+  // are stored there once the update is done
+  const bool kq_late = FUSED && commit_a >= 0;
   const int64_t rowstride = static_cast<int64_t>(H) * kWDim;
   const int64_t node0 = static_cast<int64_t>(lo) * H + h;  // (node 0, head h) row
 
@@ -164,6 +216,39 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
     al_t = __ldg(b.alpha + rw * H + h);
     be_t = __ldg(b.beta + rw * H + h);
   }
+  // node t of the previous tree
+  int pp = -1;
+  float pal = 0.f;
+  if (FUSED && commit_a >= 0 && t < pn) {
+    const int64_t rw = static_cast<int64_t>(plo) + t;
+    pp = __ldg(prev.parent + rw);
+    pal = __ldg(prev.alpha + rw * H + h);
+  }
+  // A previous tree of at most kWSeg nodes: every node's U values in this
+  // lane's two rows and (threads < 128) its key row are requested in the same
+  // round trip as the tree; the path walk then only weights them (c_j on the
+  // accepted path; nodes off it are skipped), so S_a waits for no further
+  // memory round trip.  cu = the update's A operand: u_j of entries
+  // j = 2q, 2q+1 in rows sr0 (cu[0], cu[1]) and sr0 + 1 (cu[2], cu[3]).
+  const bool spec = FUSED && commit_a >= 0 && prev.max_nodes <= kWSeg;
+  float cu[4] = {0.f, 0.f, 0.f, 0.f};
+  uint4 pkr = make_uint4(0u, 0u, 0u, 0u);
+  if (spec) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int j = 2 * q + e;
+      if (j < pn) {
+        const float2 u2 = __ldg(reinterpret_cast<const float2*>(
+            prev.U + ((static_cast<int64_t>(plo) + j) * H + h) * kWDim + sr0));
+        cu[e] = u2.x;
+        cu[2 + e] = u2.y;
+      }
+    }
+    if (t < kWSeg * 16 && (t >> 4) < pn) {
+      const uint4* kg4 = reinterpret_cast<const uint4*>(prev.k);
+      pkr = __ldg(kg4 + ((static_cast<int64_t>(plo) + (t >> 4)) * H + h) * (kWDim / 8) + (t & 15));
+    }
+  }
   // v_n at this lane's rows sr0, sr0 + 1 for the nodes n = 8 j + 2 q + e of
   // its accumulator columns, as bf16 pairs
   uint32_t vv[KT][2];
@@ -182,7 +267,7 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
   if (t == 0) {
     mbar_init(&ts.bar, 1);
     fence_mbarrier_init();
-    if (issued) {
+    if (have_s0) {
       const int y = (slot * H + h) * kWDim;
       mbar_arrive_expect_tx(&ts.bar, SB ? 2u * kWBox : 4u * kWBox);
 #pragma unroll
@@ -191,12 +276,16 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
     }
   }
   const int live_tiles = (N + 7) >> 3;  // n8-tiles of keys holding a node
+  auto store_kq = [&]() {
 #pragma unroll
-  for (int p = 0; p < kGroups; ++p) {
-    const int tile0 = 2 * p < KT ? 2 * p : 2 * p - KT;
-    if (tile0 < live_tiles)
-      *reinterpret_cast<uint4*>(kqs + (16 * p + (t >> 4)) * kWKQStride + (t & 15) * 16) = kraw[p];
-  }
+    for (int p = 0; p < kGroups; ++p) {
+      const int tile0 = 2 * p < KT ? 2 * p : 2 * p - KT;
+      if (tile0 < live_tiles)
+        *reinterpret_cast<uint4*>(kqs + (16 * p + (t >> 4)) * kWKQStride + (t & 15) * 16) = kraw[p];
+    }
+  };
+  if (!kq_late) store_kq();
+  if (spec && t < kWSeg * 16) *reinterpret_cast<uint4*>(pathk + (t >> 4) * kWPathStride + (t & 15) * 16) = pkr;
   bool bad = false;
   if (t < N) {
     bad = !(p_t >= -1 && p_t < t);
@@ -207,6 +296,41 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
   const bool bad_tree = __syncthreads_or(bad);
   const bool work = issued && !bad_tree;
 
+  // ---- the previous tree: parents checked, then (thread 0) the accepted
+  //      node's root path with the decay ratios c_j = gamma_a / gamma_j as
+  //      products of alpha (no division), published by the barrier after the
+  //      state tile's wait
+  bool bad_prev = false;
+  if constexpr (FUSED) {
+    if (commit_a >= 0) {
+      bool badp = false;
+      if (t < pn) {
+        badp = !(pp >= -1 && pp < t);
+        pv.parent[t] = pp;
+        pv.alpha[t] = pal;
+      }
+      bad_prev = __syncthreads_or(badp);
+      if (!bad_prev && t == 0) {
+        int len = 0, onpath = 0;
+        float c = 1.f;
+        for (int cur = commit_a; cur >= 0; cur = pv.parent[cur]) {
+          pv.path[len] = static_cast<uint8_t>(cur);
+          pv.c[len] = c;
+          if (spec) {
+            pv.w[cur] = c;
+            onpath |= 1 << cur;
+          }
+          c *= pv.alpha[cur];
+          ++len;
+        }
+        pv.len = len;
+        pv.onpath = onpath;
+        pv.gamma_a = c;
+      }
+    }
+  }
+  const bool commit_now = commit_a >= 0 && !bad_prev;
+
   // gamma_n: the product of alpha over node n's root path
   if (work && t < N) {
     float c = 1.f;
@@ -214,9 +338,129 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
     ts.coef[t] = make_float4(be_t, be_t * c, c, 0.f);
   }
   int fail = 0;
-  if (issued && t == 0 && !mbar_wait(&ts.bar, 0)) fail = 1;
+  if (have_s0 && t == 0 && !mbar_wait(&ts.bar, 0)) fail = 1;
   fail = __syncthreads_or(fail);
   const bool go = work && !fail;
+  const bool commit_go = commit_now && !fail;
+
+  // ---- the fused commit: update passes over this warp's rows of the tile,
+  //      per k-step of 16 state columns, then S_a back to the pool
+  bool stored = false;
+  if constexpr (FUSED) {
+    if (commit_go) {
+      const int len = pv.len;
+      const int nseg = spec ? 1 : (len + kWSeg - 1) / kWSeg;
+      const int swz = sr0 & 7;
+      for (int ps = 0; ps < nseg; ++ps) {
+        const int j0 = kWSeg * ps;
+        float ga = 1.f;
+        if (spec) {
+          // entries = the previous tree's nodes: those on the accepted path
+          // weighted by c_j, the others zero (their key rows cleared as well)
+          const int use = pv.onpath;
+          if (t < kWSeg * 16 && !((use >> (t >> 4)) & 1))
+            *reinterpret_cast<uint4*>(pathk + (t >> 4) * kWPathStride + (t & 15) * 16) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int j = 2 * q + e;
+            const bool on = (use >> j) & 1;
+            const float wj = on ? pv.w[j] : 0.f;
+            cu[e] = on ? cu[e] * wj : 0.f;
+            cu[2 + e] = on ? cu[2 + e] * wj : 0.f;
+          }
+          ga = pv.gamma_a;
+          __syncthreads();  // the cleared key rows
+        } else {
+          // c_j u_j of this lane's two rows for path entries j0 + 2q, j0 + 2q + 1,
+          // and (shared) the key rows of entries j0 .. j0 + kWSeg - 1 (zero past
+          // the path)
+          if (ps > 0) __syncthreads();  // the previous pass has read the key rows
+          if (t < kWSeg * 16) {
+            const int j = t >> 4;
+            uint4 kr = make_uint4(0u, 0u, 0u, 0u);
+            if (j0 + j < len) {
+              const uint4* kg4 = reinterpret_cast<const uint4*>(prev.k);
+              kr = __ldg(kg4 + ((static_cast<int64_t>(plo) + pv.path[j0 + j]) * H + h) * (kWDim / 8) +
+                         (t & 15));
+            }
+            *reinterpret_cast<uint4*>(pathk + j * kWPathStride + (t & 15) * 16) = kr;
+          }
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int j = j0 + 2 * q + e;
+            cu[e] = cu[2 + e] = 0.f;
+            if (j < len) {
+              const float2 u2 = __ldg(reinterpret_cast<const float2*>(
+                  prev.U + ((static_cast<int64_t>(plo) + pv.path[j]) * H + h) * kWDim + sr0));
+              cu[e] = pv.c[j] * u2.x;
+              cu[2 + e] = pv.c[j] * u2.y;
+            }
+          }
+          if (ps == 0) ga = pv.gamma_a;
+          __syncthreads();
+        }
+        uint32_t uh0, ul0, uh1, ul1;
+        split_pair(cu[0], cu[1], uh0, ul0);
+        split_pair(cu[2], cu[3], uh1, ul1);
+#pragma unroll 2
+        for (int ks = 0; ks < 8; ++ks) {
+          const int c0 = 16 * ks + 4 * q;
+          // D column n of tile tt stands for state column 16 ks + 4 (n / 2) +
+          // 2 tt + n % 2, so du[tt] lands on this lane's columns c0 + 2 tt,
+          // c0 + 2 tt + 1 (rows sr0: du[tt][0..1], sr0 + 1: du[tt][2..3])
+          float du[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+          for (int tt = 0; tt < 2; ++tt) {
+            const int pc = 16 * ks + 4 * (g >> 1) + 2 * tt + (g & 1);
+            const uint32_t k0 = *reinterpret_cast<const unsigned short*>(pathk + (2 * q) * kWPathStride + pc * 2);
+            const uint32_t k1 = *reinterpret_cast<const unsigned short*>(pathk + (2 * q + 1) * kWPathStride + pc * 2);
+            const uint32_t bk = k0 | (k1 << 16);
+            mma16816_bf16_nv(du[tt], uh0, uh1, 0u, 0u, bk, 0u);
+            mma16816_bf16_nv(du[tt], ul0, ul1, 0u, 0u, bk, 0u);
+          }
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int rr = sr0 + hr;
+            const int sr = swz ^ hr;
+            if constexpr (SB) {
+              unsigned char* ep = s0 + (c0 >> 6) * kWBox + rr * 128 + ((((c0 & 63) >> 3) ^ sr) << 4) + (c0 & 7) * 2;
+              const uint2 raw = wlds64(ep);
+              float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                            __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) x[i] = fmaf(ga, x[i], du[i >> 1][2 * hr + (i & 1)]);
+              const __nv_bfloat162 p0 = __floats2bfloat162_rn(x[0], x[1]);  // rounded once
+              const __nv_bfloat162 p1 = __floats2bfloat162_rn(x[2], x[3]);
+              *reinterpret_cast<uint2*>(ep) = make_uint2(*reinterpret_cast<const uint32_t*>(&p0),
+                                                         *reinterpret_cast<const uint32_t*>(&p1));
+            } else {
+              float4* ep = reinterpret_cast<float4*>(s0 + (c0 >> 5) * kWBox + rr * 128 +
+                                                     ((((c0 & 31) >> 2) ^ sr) << 4));
+              const float4 x = *ep;
+              *ep = make_float4(fmaf(ga, x.x, du[0][2 * hr]), fmaf(ga, x.y, du[0][2 * hr + 1]),
+                                fmaf(ga, x.z, du[1][2 * hr]), fmaf(ga, x.w, du[1][2 * hr + 1]));
+            }
+          }
+        }
+      }
+      // the committed state goes back to the pool once every row is updated
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (t == 0) {
+#pragma unroll
+        for (int c = 0; c < (SB ? 2 : 4); ++c)
+          tma_store_2d(&map_s0, s0 + c * kWBox, (SB ? 64 : 32) * c, (slot * H + h) * kWDim);
+        bulk_commit_group();
+      }
+      stored = true;
+    }
+    if (kq_late) {
+      // every read of the staging area is done (the barriers above): the K/Q
+      // rows go to their region now
+      if (go) store_kq();
+      __syncthreads();
+    }
+  }
 
   if (go) {
     // ---- MMA 1: acc[nt] = S0 [K;Q]^T, tile nt of slots 8 nt .. 8 nt + 7
@@ -313,7 +557,12 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
 
     // ---- Gram: slots 16 warp .. 16 warp + 15 (fragment rows g, g + 8) times
     //      the live key tiles, in passes of at most 4 tiles, written over the
-    //      warp's own rows of the state tile (all read above)
+    //      warp's own rows of the state tile (all read above; a fused commit's
+    //      store of S_a must have read the tile first)
+    if (stored) {
+      if (t == 0) bulk_wait_group_read0();
+      __syncthreads();
+    }
     __syncwarp();
     const int mt = warp < KT / 2 ? warp : warp - KT / 2;  // key tile pair of these slots
     if (warp < KT && 2 * mt < live_tiles) {
@@ -485,38 +734,51 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
 
   if (t == 0) {
     int bits = fail ? kStatusTimeout : 0;
-    if (h == 0) bits |= flags | (issued && bad_tree ? TREEWY_STATUS_BAD_TREE : 0);
+    if (h == 0) bits |= flags | cflags | (issued && bad_tree ? TREEWY_STATUS_BAD_TREE : 0);
+    // the previous tree failed its checks, or a wait gave up before S_a was
+    // stored: that request's commit did not happen
+    if (bad_prev && h == 0) bits |= TREEWY_STATUS_BAD_TREE | TREEWY_STATUS_COMMIT_REFUSED;
+    if (fail && commit_now && !stored) bits |= TREEWY_STATUS_COMMIT_REFUSED;
     if (bits) atomicOr(b.status + r, bits);
     // no copy may still target this CTA's memory at exit
     if (fail) mbar_wait(&ts.bar, 0);
+    if (stored) bulk_wait_group_read0();
   }
 }
 
-template <int NPM, bool SB>
-cudaError_t launch_warp(const treewy_batch& b, const CUtensorMap& map_s0, cudaStream_t stream) {
+template <int NPM, bool SB, bool FUSED>
+cudaError_t launch_warp(const treewy_batch& b, const CUtensorMap& map_s0, const PrevRound& prev,
+                        cudaStream_t stream) {
   using C = WarpCfg<NPM, SB>;
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t attr = once_per_device(attr_done, [] {
-    cudaError_t e = cudaFuncSetAttribute(verify_warp_kernel<NPM, SB>,
+    cudaError_t e = cudaFuncSetAttribute(verify_warp_kernel<NPM, SB, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kDynSmem));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(verify_warp_kernel<NPM, SB>, cudaFuncAttributePreferredSharedMemoryCarveout,
+      e = cudaFuncSetAttribute(verify_warp_kernel<NPM, SB, FUSED>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
     return e;
   });
   if (attr != cudaSuccess) return attr;
   const unsigned grid = static_cast<unsigned>(b.R) * static_cast<unsigned>(b.H);
-  verify_warp_kernel<NPM, SB><<<grid, kWThreads, C::kDynSmem, stream>>>(map_s0, b);
+  verify_warp_kernel<NPM, SB, FUSED><<<grid, kWThreads, C::kDynSmem, stream>>>(map_s0, b, prev);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_verify_warp(const treewy_batch& b, const CUtensorMap& map_s0, cudaStream_t stream) {
+cudaError_t launch_verify_warp(const treewy_batch& b, const CUtensorMap& map_s0, const PrevRound* prev,
+                               cudaStream_t stream) {
   static_assert(kWarpTreeNodes == 16, "launched for the 16-node capacity");
   const bool sb = (b.flags & TREEWY_FLAG_STATE_BF16) != 0;
-  return sb ? launch_warp<16, true>(b, map_s0, stream) : launch_warp<16, false>(b, map_s0, stream);
+  if (prev == nullptr) {
+    const PrevRound none{};
+    return sb ? launch_warp<16, true, false>(b, map_s0, none, stream)
+              : launch_warp<16, false, false>(b, map_s0, none, stream);
+  }
+  return sb ? launch_warp<16, true, true>(b, map_s0, *prev, stream)
+            : launch_warp<16, false, true>(b, map_s0, *prev, stream);
 }
 
 }  // namespace treewy

@@ -4,8 +4,10 @@ on the same seeded inputs: every size from 1 to 16 in chain, star, forest and
 random shapes (chains longer than 8 take the kernel's general root-path
 recurrence, shorter paths its register form), the smallest capacity routed
 to it (9), ragged batches with empty trees, gates at the ends of their range,
-a bf16 state pool, device-side errors, CUDA-graph replay, and agreement with
-the small-tree and tcgen05 kernels on the same inputs.  Tolerances as in
+a bf16 state pool, device-side errors, CUDA-graph replay, agreement with
+the small-tree and tcgen05 kernels on the same inputs, and the commit fused
+in front (paths of 1 to 64 entries, both pools, refusals, against the two
+separate calls, the binary workload at full size).  Tolerances as in
 gpu_helpers (o, U: 2e-3 of the largest reference value; committed state
 1e-3; gamma 1e-5 relative).
 """
@@ -20,7 +22,8 @@ from gdn_speculative_tree_gb300 import workloads as wl
 from oracle import gdn_tree_oracle as orc
 from tests.gpu_helpers import (CudaRun, FLT_MIN, G_TOL, O_TOL, U_TOL, assert_within, compare, np32,
                                oracle_request)
-from tests.test_gpu_small import custom, random_tree, shapes
+from tests.test_gpu_small import (check_two_rounds, custom, random_tree, run_commit_verify, shapes,
+                                  two_rounds)
 
 pytestmark = pytest.mark.gpu
 
@@ -210,3 +213,125 @@ def test_warp_graph_replay_matches_eager(cuda_lib):
     assert_within(compare(w, replay, range(w.R)), "binary graph replay")
     assert torch.equal(tv.o.cpu(), torch.from_numpy(run.o))
     assert torch.equal(w.state.cpu(), run.S_after.cpu())
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_warp_commit_verify_matches_oracle(cuda_lib, state_dtype):
+    """treewy_commit_verify whose next trees have 9 to 16 nodes: accepted paths
+    from the root only to 64 entries (eight update passes of the fused kernel
+    for an fp32 pool; a bf16 pool with previous trees above 8 nodes takes the
+    commit and the verification as two calls), no commit, empty next trees;
+    S_a and the next round's o and U against the oracle run as
+    commit-then-verify."""
+    rng = np.random.default_rng(23)
+    prev_trees = [random_tree(rng, n) for n in (40, 4, 64, 8, 1, 12, 9, 16)]
+    prev_trees[2] = wl.chain_parents(64)
+    prev_trees[6] = wl.chain_parents(9)     # a path of one pass + 1 entry
+    next_trees = [random_tree(rng, n) for n in (CAP, 2, 0, 1, CAP - 1, 3, 9, 12)]
+    next_trees[0] = wl.chain_parents(CAP)   # the longest next root path
+    accepted = [39, -1, 63, 5, 0, 11, 8, 15]
+    prev, nxt = two_rounds(prev_trees, next_trees, accepted, cap=CAP, state_dtype=state_dtype)
+    tn, S0_pool = run_commit_verify(prev, nxt)
+    assert not tn.status.any(), tn.status.tolist()
+    check_two_rounds(prev, nxt, tn, S0_pool, range(len(prev_trees)), bf16=state_dtype == "bf16")
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_warp_commit_verify_short_paths(cuda_lib, state_dtype):
+    """Previous trees of at most 8 nodes (one update pass with every node's U
+    and key row requested up front; a bf16 pool's S_a rounded once), next
+    trees of up to 16: chains, stars and random trees, accepted nodes from the
+    root to the deepest node."""
+    rng = np.random.default_rng(43)
+    prev_trees = [wl.chain_parents(8), np.array([-1] + [0] * 7, np.int32), random_tree(rng, 5),
+                  random_tree(rng, 8), wl.chain_parents(3), random_tree(rng, 1)]
+    next_trees = [random_tree(rng, n) for n in (CAP, 1, 11, 2, 0, CAP - 1)]
+    accepted = [7, 6, 4, 5, -1, 0]
+    prev, nxt = two_rounds(prev_trees, next_trees, accepted, cap=CAP, state_dtype=state_dtype, seed=11)
+    assert prev.max_nodes <= 8
+    tn, S0_pool = run_commit_verify(prev, nxt)
+    assert not tn.status.any(), tn.status.tolist()
+    check_two_rounds(prev, nxt, tn, S0_pool, range(len(prev_trees)), bf16=state_dtype == "bf16")
+
+
+def test_warp_commit_verify_refusals(cuda_lib):
+    """Each half runs exactly when its separate call would: an accepted index
+    outside the previous tree, a previous parent after its node and a state
+    slot outside the pool refuse the commit (state unchanged, COMMIT_REFUSED
+    beside the reason; the bad slot skips the verification too), while a bad
+    next tree (parent after its node, more nodes than the capacity) skips
+    only the verification and still commits."""
+    rng = np.random.default_rng(31)
+    prev_trees = [random_tree(rng, n) for n in (6, 7, 5, 12, 6, 4)]
+    prev_trees[2] = prev_trees[2].copy()
+    prev_trees[2][3] = 4                    # previous tree: parent after its node
+    next_trees = [random_tree(rng, n) for n in (12, 3, 9, 14, 16, 10)]
+    next_trees[3] = next_trees[3].copy()
+    next_trees[3][12] = 13                  # next tree: parent after its node
+    accepted = [5, 7, 2, 11, 3, 1]          # request 1: outside its 7-node tree
+    prev, nxt = two_rounds(prev_trees, next_trees, accepted, cap=CAP)
+    slots = prev.state_slot.clone()
+    slots[5] = prev.num_slots               # outside the pool
+    tp = binding.TreeVerifier(prev)
+    tp.verify()
+    torch.cuda.synchronize()
+    S0_pool = prev.state.cpu()
+    prev.state_slot.copy_(slots)
+    nxt.state_slot = prev.state_slot
+    tn = binding.TreeVerifier(nxt, max_nodes=15)   # request 4 (16 nodes) exceeds it
+    tn.o.fill_(float("nan"))
+    binding.treewy_commit_verify(tp.batch, prev.accepted, tn.batch)
+    torch.cuda.synchronize()
+    st = tn.status.cpu().tolist()
+    R_ = binding.STATUS_COMMIT_REFUSED
+    assert st[0] == 0, st
+    assert st[1] == binding.STATUS_BAD_ACCEPTED | R_, st
+    assert st[2] == binding.STATUS_BAD_TREE | R_, st
+    assert st[3] == binding.STATUS_BAD_TREE, st
+    assert st[4] == binding.STATUS_TOO_MANY_NODES, st
+    assert st[5] == binding.STATUS_BAD_SLOT | R_, st
+    nn = nxt.node_offset.cpu().tolist()
+    for r in (3, 4, 5):
+        assert torch.isnan(tn.o[nn[r]:nn[r + 1]]).all(), r
+    check_two_rounds(prev, nxt, tn, S0_pool, [0, 1, 2], refused=(1, 2))
+    # committed although not verified
+    check_two_rounds(prev, nxt, tn, S0_pool, [3, 4], verified=False)
+
+
+def test_warp_commit_verify_equals_separate_calls(cuda_lib):
+    """The binary-tree workload, two layers on one state pool: the fused call
+    against verify(prev), commit(prev), verify(next)."""
+    cfg = wl.CONFIGS["binary"]
+    pa = wl.generate(cfg, R=24).to("cuda")
+    na = wl.generate(cfg, R=24, layer=1).to("cuda")
+    pb = wl.generate(cfg, R=24).to("cuda")
+    nb = wl.generate(cfg, R=24, layer=1).to("cuda")
+    na.state, na.state_slot = pa.state, pa.state_slot
+    nb.state, nb.state_slot = pb.state, pb.state_slot
+    tn, _ = run_commit_verify(pa, na)
+    tpb = binding.TreeVerifier(pb)
+    tpb.verify()
+    tpb.commit()
+    tnb = binding.TreeVerifier(nb)
+    tnb.verify()
+    torch.cuda.synchronize()
+    assert not tn.status.any() and not tnb.status.any()
+    ds = (pa.state - pb.state).abs().max().item()
+    assert ds <= 1e-4 * pb.state.abs().max().item(), ds
+    do = (tn.o - tnb.o).abs().max().item()
+    assert do <= 1e-3 * tnb.o.abs().max().item(), do
+
+
+def test_warp_commit_verify_binary_full_size(cuda_lib):
+    """The binary-tree workload at full size (128 requests x 32 heads, the
+    launch configuration of the per-workload study): two layers on one state
+    pool, the fused call against the oracle run as commit-then-verify on
+    every request."""
+    cfg = wl.CONFIGS["binary"]
+    prev = wl.generate(cfg).to("cuda")
+    nxt = wl.generate(cfg, layer=1).to("cuda")
+    nxt.state, nxt.state_slot = prev.state, prev.state_slot
+    assert 8 < nxt.max_nodes <= CAP
+    tn, S0_pool = run_commit_verify(prev, nxt)
+    assert not tn.status.any(), tn.status.tolist()
+    check_two_rounds(prev, nxt, tn, S0_pool, range(prev.R))
