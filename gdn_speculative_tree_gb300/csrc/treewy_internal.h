@@ -75,8 +75,7 @@ constexpr int kWarpTreeNodes = 16;
 cudaError_t launch_verify_warp(const treewy_batch& b, const CUtensorMap& state_map,
                                const PrevRound* prev, cudaStream_t stream);
 
-// npm: padded tree capacity (16, 32 or 64).
-size_t verify_tc_smem(int npm);
+// npm: tree capacity bucket (32 or 64 nodes; launched for max_nodes > 16).
 cudaError_t launch_verify_tc(const treewy_batch& b, const VerifyMaps& maps, int npm,
                              cudaStream_t stream);
 cudaError_t launch_commit_verify_tc(const treewy_batch& next, const PrevRound& prev,

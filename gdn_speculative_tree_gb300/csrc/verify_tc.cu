@@ -5,12 +5,6 @@
 
 namespace treewy {
 
-size_t verify_tc_smem(int npm) {
-  if (npm <= 16) return TcCfg<16>::kDynSmem;
-  if (npm <= 32) return TcCfg<32>::kDynSmem;
-  return TcCfg<64>::kDynSmem;
-}
-
 cudaError_t launch_verify_tc(const treewy_batch& b, const VerifyMaps& maps, int npm,
                              cudaStream_t stream) {
   if (b.flags & TREEWY_FLAG_STATE_BF16) return launch_verify_tc_bf16state(b, maps, nullptr, npm, stream);

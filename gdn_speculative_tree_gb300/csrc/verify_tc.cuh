@@ -55,37 +55,29 @@ template <int NPM>
 struct TcCfg {
   // D1 = [S0k | S0q] in columns [0, 2NPM); the Gram, then [U | O], from 2NPM
   static constexpr uint32_t kCols = 4u * NPM;
-  static_assert(NPM == 16 || NPM == 32 || NPM == 64, "tree capacity bucket");
+  static_assert(NPM == 32 || NPM == 64, "tree capacity bucket (smaller trees have their own kernels)");
   static constexpr int kE = NPM * (NPM + 1) / 2;              // path-list entries, worst case
   static constexpr uint32_t kListBytes = 4u * kE;
   static constexpr uint32_t kPidxBytes = (kE + 15u) & ~15u;
   static constexpr uint32_t kR2Bytes = kPidxBytes + kListBytes;  // pidx + (pc | B scratch)
-  // K/Q: two 64-column chunks of 128 rows (the Gram's M = 128 operand).  A
-  // 16-node tree uses 32 rows, so its chunks are 32 rows and the region sits
-  // before the S0 tile: the Gram's reads of rows 32..127 stay inside the
-  // CTA's shared memory (their products land in TMEM lanes that are never
-  // read).  (16-node trees reach this kernel only with the commit fused in;
-  // plain verification of trees of up to 16 nodes has its own kernels.)
-  static constexpr uint32_t kKQRows = NPM == 16 ? 32u : 128u;
+  // K/Q: two 64-column chunks of 128 rows (the Gram's M = 128 operand), after
+  // the S0 tile.
+  static constexpr uint32_t kKQRows = 128u;
   static constexpr uint32_t kKQChunk = kKQRows * 128u;
   static constexpr uint32_t kKQ = 2u * kKQChunk;
-  static constexpr uint32_t kKQOff = NPM == 16 ? 0u : kS0Bytes;
-  static constexpr uint32_t kS0Off = NPM == 16 ? kKQ : 0u;
+  static constexpr uint32_t kKQOff = kS0Bytes;
+  static constexpr uint32_t kS0Off = 0u;
   static constexpr uint32_t kR2Off = kS0Bytes + kKQ;
   static constexpr uint32_t kDynSmem = kR2Off + kR2Bytes + 1024u;
   static_assert(3u * kListBytes <= kKQ, "A, M and T-scratch lists must fit the K/Q region");
 };
 
-// Dynamic shared memory of one kernel instance.  The fused fp32 instance for
-// 16-node trees adds a 16 KB tile for its commit's update operands after the
-// lists (its K/Q region, 8 KB, is too small to hold them; the larger buckets
-// use their K/Q region, and a bf16 state the free half of the state region).
+// Dynamic shared memory of one kernel instance (the fused commit's update
+// operands use the K/Q region of an fp32 instance, the free half of the state
+// region of a bf16 one).
 template <int NPM, bool FUSED, bool SB>
 struct TcSmem {
-  using C = TcCfg<NPM>;
-  static constexpr bool kExtraUpd = FUSED && !SB && NPM < 32;
-  static constexpr uint32_t kUpdOff = (C::kR2Off + C::kR2Bytes + 1023u) & ~1023u;
-  static constexpr uint32_t kBytes = kExtraUpd ? kUpdOff + 16384u + 1024u : C::kDynSmem;
+  static constexpr uint32_t kBytes = TcCfg<NPM>::kDynSmem;
 };
 
 // Per-CTA tree data for one (request, head), sized by the capacity bucket.
@@ -315,10 +307,9 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
   // TMEM columns 0..127 (before the first products need them), with its
   // operands in a 16 KB tile: the free upper half of the state region for a
   // bf16 state; for an fp32 one the K/Q region (whose K/Q boxes are then
-  // requested once the update has read it), or for 16-node trees, whose K/Q
-  // region is too small, a tile of its own after the lists.
-  constexpr bool kDeferKQ = FUSED && !SB && NPM >= 32;
-  constexpr uint32_t kTmemCols = (FUSED && C::kCols < 128u) ? 128u : C::kCols;
+  // requested once the update has read it).
+  constexpr bool kDeferKQ = FUSED && !SB;
+  constexpr uint32_t kTmemCols = C::kCols;
   extern __shared__ unsigned char smem_raw[];
   __shared__ TreeTC<NPM> ts;
   __shared__ PrevSmem<FUSED> pv;
@@ -634,8 +625,7 @@ __global__ void __launch_bounds__(kThreads, (SB || FUSED || NPM < 64) ? 2 : 0)
         // the _lo parts, slot 2 k_j[c]; thread (wg, lane) writes entries
         // 8wg..8wg+7 of row `lane` of each.  Then S_a = gamma_a S0 + D row by
         // row (rounded once for a bf16 state).
-        unsigned char* opt = SB ? s0 + 2 * kS0ChunkBytes
-                              : (NPM >= 32 ? kq : base + TcSmem<NPM, FUSED, SB>::kUpdOff);
+        unsigned char* opt = SB ? s0 + 2 * kS0ChunkBytes : kq;
         unsigned char* orow = opt + lane * 128;
         const int r7 = lane & 7;
         const int nseg = (len + 2 * kPrevSeg - 1) / (2 * kPrevSeg);
@@ -1092,14 +1082,13 @@ cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, const PrevRou
 template <bool SB>
 cudaError_t launch_tc(const treewy_batch& b, const VerifyMaps& m, const PrevRound* prev, int npm,
                       cudaStream_t stream) {
+  // trees of more than 16 nodes (smaller ones go to the small-tree and
+  // warp-MMA kernels, fused or not)
   if (prev == nullptr) {
-    // plain verification: trees of more than 16 nodes (smaller ones go to
-    // the small-tree and warp-MMA kernels)
     const PrevRound none{};
     if (npm <= 32) return launch_npm<32, false, SB>(b, m, none, stream);
     return launch_npm<64, false, SB>(b, m, none, stream);
   }
-  if (npm <= 16) return launch_npm<16, true, SB>(b, m, *prev, stream);
   if (npm <= 32) return launch_npm<32, true, SB>(b, m, *prev, stream);
   return launch_npm<64, true, SB>(b, m, *prev, stream);
 }

@@ -79,8 +79,8 @@ enum {
 /* Flags. */
 enum {
   /* Use the portable kernels (CUDA cores, no bulk tensor copies) even where
-     the tensor-core verification (dk = dv = 128, bf16 q/k/v: tcgen05, or
-     warp-level MMAs for batches of trees of at most 8 nodes) or the
+     the tensor-core verification (dk = dv = 128, bf16 q/k/v: warp-level
+     MMAs for batches of trees of at most 16 nodes, tcgen05 above) or the
      bulk-copy commit (dk = dv = 128) applies.  Same results within rounding. */
   TREEWY_FLAG_FORCE_GENERIC = 1u,
   /* The state pool holds bf16 instead of f32: the dtype in which the GDN
@@ -191,7 +191,8 @@ treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted,
  * results equal treewy_commit(prev, prev_accepted) followed by
  * treewy_verify(next), with one state read per head instead of two.  (Shapes
  * other than dk = dv = 128 with bf16 q/k/v in both rounds, and a bf16 pool
- * whose next trees have at most 8 nodes while the previous ones have more,
+ * whose next trees have at most 16 nodes while the previous ones have more
+ * than 8,
  * run as those two calls back to back on `stream`.)  A request with no node
  * in `next` still gets its commit.  prev and next must have the
  * same R, H, dk, dv, state pool pointer, num_slots, state_slot pointer and
