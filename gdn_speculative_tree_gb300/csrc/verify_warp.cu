@@ -30,7 +30,9 @@
 //
 // The kernel is written for a capacity NPM of up to 64 nodes, but launched
 // for NPM = 16 only: three CTAs per SM fit (76 KB of shared memory, 80
-// registers), and the tile count is small.  At 32 nodes it measured level
+// registers; a bf16 pool's instances four, 44 KB and 64 registers: its 32 KB
+// tile region also holds the Gram rows and the [T;B] halves), and the tile
+// count is small.  At 32 nodes it measured level
 // with the tcgen05 kernel, at 64 nodes ~35 % slower: the first products take
 // two warp MMAs per 8-node tile and state element pair (hi and lo), and warp
 // MMAs run at ~0.47 m16n8k16 per cycle per SM, about a quarter of the tcgen05
@@ -85,12 +87,15 @@ template <int NPM, bool SB>
 struct WarpCfg {
   static constexpr int kSlots = 2 * NPM;  // keys 0..NPM-1, queries NPM..2NPM-1
   static constexpr int kKT = NPM / 8;     // n8-tiles of keys (and of queries)
-  static constexpr uint32_t kKQOff = 4u * kWBox;
+  // a bf16 pool's 16-node instances: the 32 KB tile region also holds the
+  // Gram rows (box 0) and the [T;B] halves (box 1)
+  static constexpr bool kCompact = SB && NPM == 16;
+  static constexpr uint32_t kKQOff = (kCompact ? 2u : 4u) * kWBox;
   static constexpr uint32_t kKQBytes = kSlots * kWKQStride;
   static constexpr uint32_t kTreeOff = kKQOff + kKQBytes;
   static constexpr uint32_t kEnd = kTreeOff + static_cast<uint32_t>(sizeof(WarpTree<NPM>));
   static constexpr uint32_t kDynSmem = 1024u + kEnd;
-  static constexpr int kBlocks = NPM == 16 ? 3 : 2;  // CTAs per SM
+  static constexpr int kBlocks = kCompact ? 4 : (NPM == 16 ? 3 : 2);  // CTAs per SM
   static_assert(kBlocks * (kDynSmem + 1024u) <= 228u * 1024u, "CTAs per SM");
   static_assert(8u * NPM * NPM <= kKQBytes, "x scratch of 2 NPM long paths");
   static_assert(2 * NPM <= kWThreads && NPM <= 64, "one operand row per thread");
@@ -600,8 +605,8 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
 
     // ---- operand rows of [T;B]: thread t < NPM the T row of node t, thread
     //      NPM + n the B row of node n, over boxes 2 (hi) and 3 (lo)
-    unsigned char* oph = s0 + 2 * kWBox;
-    unsigned char* opl = s0 + 3 * kWBox;
+    unsigned char* oph = s0 + (C::kCompact ? kWBox : 2 * kWBox);
+    unsigned char* opl = s0 + (C::kCompact ? kWBox + 4096 : 3 * kWBox);
     if (t < 2 * NPM) {
       const bool isB = t >= NPM;
       const int n = isB ? t - NPM : t;
