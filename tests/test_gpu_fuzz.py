@@ -63,15 +63,25 @@ def check_state(S_gpu, S_ref, sd):
 
 
 SMALL_CAPS = (4, 8)  # the small-tree kernel's capacities (dk = dv = 128, bf16 q/k/v)
+MID_CAPS = (9, 12, 16)  # the warp-MMA kernel's range below the tcgen05 kernel's
 
 
-@pytest.mark.parametrize("seed", list(range(48)) + [f"small{i}" for i in range(24)])
-def test_fuzz_verify_commit(cuda_lib, seed):
+def seeded(seed, base_small, base_mid, base):
+    """Batch parameters for a seed: "small<i>" and "mid<i>" draw capacities of
+    the small-tree and warp-MMA kernels, integers the general mix."""
     if isinstance(seed, str):
-        _, p = draw_batch(3000 + int(seed[5:]), caps=SMALL_CAPS)
-        seed = 3000 + int(seed[5:])
-    else:
-        _, p = draw_batch(seed)
+        kind, i = ("small", int(seed[5:])) if seed.startswith("small") else ("mid", int(seed[3:]))
+        s2 = (base_small if kind == "small" else base_mid) + i
+        rng, p = draw_batch(s2, caps=SMALL_CAPS if kind == "small" else MID_CAPS)
+        return rng, p, s2
+    rng, p = draw_batch(base + seed)
+    return rng, p, seed
+
+
+@pytest.mark.parametrize("seed", list(range(48)) + [f"small{i}" for i in range(24)] +
+                         [f"mid{i}" for i in range(16)])
+def test_fuzz_verify_commit(cuda_lib, seed):
+    _, p, seed = seeded(seed, 3000, 5000, 0)
     w = assemble(p, p["trees"], p["acc"], seed)
     S0_pool = w.state.cpu()
     tv = binding.TreeVerifier(w)
@@ -99,13 +109,10 @@ def test_fuzz_verify_commit(cuda_lib, seed):
     assert u_err <= 2e-3 * max(u_max, 1e-30), (u_err, u_max)
 
 
-@pytest.mark.parametrize("seed", list(range(24)) + [f"small{i}" for i in range(16)])
+@pytest.mark.parametrize("seed", list(range(24)) + [f"small{i}" for i in range(16)] +
+                         [f"mid{i}" for i in range(12)])
 def test_fuzz_fused_two_rounds(cuda_lib, seed):
-    if isinstance(seed, str):
-        rng, p = draw_batch(4000 + int(seed[5:]), caps=SMALL_CAPS)
-        seed = 4000 + int(seed[5:])
-    else:
-        rng, p = draw_batch(100 + seed)
+    rng, p, seed = seeded(seed, 4000, 6000, 100)
     R = len(p["trees"])
     nxt_trees = [draw_tree(rng, p["cap"]) for _ in range(R)]
     prev = assemble(p, p["trees"], p["acc"], 2 * seed)
