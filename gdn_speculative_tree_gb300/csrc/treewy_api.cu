@@ -77,6 +77,8 @@ treewy_status validate(const treewy_batch* b, bool need_qv, bool need_outputs, b
   if (need_k && !aligned16(b->k)) return fail(TREEWY_ERR_INVALID_ARG, "k must be 16-byte aligned");
   if (need_qv && (!aligned16(b->q) || !aligned16(b->v)))
     return fail(TREEWY_ERR_INVALID_ARG, "q and v must be 16-byte aligned");
+  if (need_outputs && (!aligned16(b->o) || !aligned16(b->U)))
+    return fail(TREEWY_ERR_INVALID_ARG, "o and U must be 16-byte aligned");
   return TREEWY_OK;
 }
 
@@ -212,6 +214,7 @@ treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted, 
   treewy_status st = validate(batch, false, false, true);
   if (st != TREEWY_OK || batch->R == 0) return st;
   if (!batch->U && batch->T > 0) return fail(TREEWY_ERR_INVALID_ARG, "U is NULL");
+  if (!aligned16(batch->U)) return fail(TREEWY_ERR_INVALID_ARG, "U must be 16-byte aligned");
   if (!accepted) return fail(TREEWY_ERR_INVALID_ARG, "accepted is NULL");
   return launch_commit_any(batch, accepted, 0, stream, "treewy_commit launch");
 }
@@ -232,6 +235,7 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
     return fail(TREEWY_ERR_INVALID_ARG, "prev and next must agree on TREEWY_FLAG_STATE_BF16");
   if (next->R == 0) return TREEWY_OK;
   if (!prev->U && prev->T > 0) return fail(TREEWY_ERR_INVALID_ARG, "prev->U is NULL");
+  if (!aligned16(prev->U)) return fail(TREEWY_ERR_INVALID_ARG, "prev->U must be 16-byte aligned");
   if (!prev_accepted) return fail(TREEWY_ERR_INVALID_ARG, "prev_accepted is NULL");
   cudaError_t err;
   // The small-tree and warp-MMA kernels apply an accepted path 8 entries per

@@ -115,8 +115,9 @@ enum {
  *                                 head's state holds S0[d][0..dk-1]); 16-byte aligned;
  *                                 bf16, same shape, with TREEWY_FLAG_STATE_BF16
  *   state_slot   int32 [R]        pool slot of each request, in [0, num_slots)
- *   o            f32 [T][H][dv]   verify output o_n
- *   U            f32 [T][H][dv]   verify output u_n, commit input (keep it
+ *   o            f32 [T][H][dv]   verify output o_n (16-byte aligned base)
+ *   U            f32 [T][H][dv]   verify output u_n, commit input (16-byte
+ *                                 aligned base; keep it
  *                                 alive from verify to commit: it replaces
  *                                 the per-node snapshots)
  *   gamma        f32 [T][H]       optional verify output gamma_n (may be NULL)

@@ -77,6 +77,8 @@ def _valid_batch():
     ("status", None, binding.TREEWY_ERR_INVALID_ARG),
     ("state", 0x10004, binding.TREEWY_ERR_INVALID_ARG),
     ("k", 0x10008, binding.TREEWY_ERR_INVALID_ARG),
+    ("o", 0x10004, binding.TREEWY_ERR_INVALID_ARG),
+    ("U", 0x10008, binding.TREEWY_ERR_INVALID_ARG),
 ])
 def test_verify_rejects_bad_arguments(lib, field, value, code):
     b = _valid_batch()
@@ -119,6 +121,15 @@ def test_commit_verify_rejects_inconsistent_rounds(lib):
     assert lib.treewy_commit_verify(ctypes.byref(prev), 0x10000, ctypes.byref(nxt), None) == \
         binding.TREEWY_ERR_INVALID_ARG
     assert b"state pool" in lib.treewy_last_error()
+    prev = _valid_batch()
+    prev.U = 0x10004
+    assert lib.treewy_commit_verify(ctypes.byref(prev), 0x10000, ctypes.byref(nxt), None) == \
+        binding.TREEWY_ERR_INVALID_ARG
+    assert b"aligned" in lib.treewy_last_error()
+    b = _valid_batch()
+    b.U = 0x10004
+    assert lib.treewy_commit(ctypes.byref(b), 0x10000, None) == binding.TREEWY_ERR_INVALID_ARG
+    assert b"aligned" in lib.treewy_last_error()
     prev = _valid_batch()
     assert lib.treewy_commit_verify(ctypes.byref(prev), None, ctypes.byref(nxt), None) == \
         binding.TREEWY_ERR_INVALID_ARG
