@@ -67,12 +67,12 @@ struct WarpPrev {
   float alpha[kMaxNodes];
   float c[kMaxNodes];        // gamma_a / gamma_{path j} as products of alpha
   uint8_t path[kMaxNodes];   // accepted node, its parent, ... (root last)
-  float w[8];                // previous trees of at most 8 nodes: c_j by node
+  float w[16];               // previous trees of at most 16 nodes: c_j by node
   int onpath;                // ... and the nodes on the accepted path (bit j)
   int len;
   float gamma_a;
 };
-constexpr int kWSeg = 8;              // path entries applied per pass over the tile
+constexpr int kWSeg = 16;             // path entries applied per pass over the tile (the MMA's k)
 constexpr uint32_t kWPathStride = 272u;  // bf16 key row of the path: 256 + 16
 constexpr uint32_t kWPathOff = 1024u;    // key rows after WarpPrev in the K/Q region
 static_assert(sizeof(WarpPrev) <= kWPathOff, "previous tree before the key rows");
@@ -100,6 +100,7 @@ struct WarpCfg {
   static_assert(8u * NPM * NPM <= kKQBytes, "x scratch of 2 NPM long paths");
   static_assert(2 * NPM <= kWThreads && NPM <= 64, "one operand row per thread");
   static_assert(kWPathOff + kWSeg * kWPathStride <= kKQBytes, "fused commit staging");
+  static_assert(kWSeg == kWarpTreeNodes, "a bf16 pool's fused form needs one pass per path");
 };
 
 // Fragment row g of a warp's tiles stands for state rows 16 w + 2 f(g) (row
@@ -233,20 +234,24 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
   // lane's two rows and (threads < 128) its key row are requested in the same
   // round trip as the tree; the path walk then only weights them (c_j on the
   // accepted path; nodes off it are skipped), so S_a waits for no further
-  // memory round trip.  cu = the update's A operand: u_j of entries
-  // j = 2q, 2q+1 in rows sr0 (cu[0], cu[1]) and sr0 + 1 (cu[2], cu[3]).
+  // memory round trip.  cu = the update's A operand (the m16n8k16 fragment,
+  // path entries as k): u_j of entries j = 2q + e (cu[e], row sr0; cu[2 + e],
+  // row sr0 + 1) and j = 2q + 8 + e (cu[4 + e], cu[6 + e]).
   const bool spec = FUSED && commit_a >= 0 && prev.max_nodes <= kWSeg;
-  float cu[4] = {0.f, 0.f, 0.f, 0.f};
+  float cu[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   uint4 pkr = make_uint4(0u, 0u, 0u, 0u);
   if (spec) {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int j = 2 * q + e;
-      if (j < pn) {
-        const float2 u2 = __ldg(reinterpret_cast<const float2*>(
-            prev.U + ((static_cast<int64_t>(plo) + j) * H + h) * kWDim + sr0));
-        cu[e] = u2.x;
-        cu[2 + e] = u2.y;
+    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = 2 * q + 8 * hh + e;
+        if (j < pn) {
+          const float2 u2 = __ldg(reinterpret_cast<const float2*>(
+              prev.U + ((static_cast<int64_t>(plo) + j) * H + h) * kWDim + sr0));
+          cu[4 * hh + e] = u2.x;
+          cu[4 * hh + 2 + e] = u2.y;
+        }
       }
     }
     if (t < kWSeg * 16 && (t >> 4) < pn) {
@@ -366,19 +371,22 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
           if (t < kWSeg * 16 && !((use >> (t >> 4)) & 1))
             *reinterpret_cast<uint4*>(pathk + (t >> 4) * kWPathStride + (t & 15) * 16) = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int j = 2 * q + e;
-            const bool on = (use >> j) & 1;
-            const float wj = on ? pv.w[j] : 0.f;
-            cu[e] = on ? cu[e] * wj : 0.f;
-            cu[2 + e] = on ? cu[2 + e] * wj : 0.f;
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int j = 2 * q + 8 * hh + e;
+              const bool on = (use >> j) & 1;
+              const float wj = on ? pv.w[j] : 0.f;
+              cu[4 * hh + e] = on ? cu[4 * hh + e] * wj : 0.f;
+              cu[4 * hh + 2 + e] = on ? cu[4 * hh + 2 + e] * wj : 0.f;
+            }
           }
           ga = pv.gamma_a;
           __syncthreads();  // the cleared key rows
         } else {
-          // c_j u_j of this lane's two rows for path entries j0 + 2q, j0 + 2q + 1,
-          // and (shared) the key rows of entries j0 .. j0 + kWSeg - 1 (zero past
-          // the path)
+          // c_j u_j of this lane's two rows for path entries j0 + 2q + e and
+          // j0 + 2q + 8 + e, and (shared) the key rows of entries j0 ..
+          // j0 + kWSeg - 1 (zero past the path)
           if (ps > 0) __syncthreads();  // the previous pass has read the key rows
           if (t < kWSeg * 16) {
             const int j = t >> 4;
@@ -391,22 +399,25 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
             *reinterpret_cast<uint4*>(pathk + j * kWPathStride + (t & 15) * 16) = kr;
           }
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int j = j0 + 2 * q + e;
-            cu[e] = cu[2 + e] = 0.f;
-            if (j < len) {
-              const float2 u2 = __ldg(reinterpret_cast<const float2*>(
-                  prev.U + ((static_cast<int64_t>(plo) + pv.path[j]) * H + h) * kWDim + sr0));
-              cu[e] = pv.c[j] * u2.x;
-              cu[2 + e] = pv.c[j] * u2.y;
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int j = j0 + 2 * q + 8 * hh + e;
+              cu[4 * hh + e] = cu[4 * hh + 2 + e] = 0.f;
+              if (j < len) {
+                const float2 u2 = __ldg(reinterpret_cast<const float2*>(
+                    prev.U + ((static_cast<int64_t>(plo) + pv.path[j]) * H + h) * kWDim + sr0));
+                cu[4 * hh + e] = pv.c[j] * u2.x;
+                cu[4 * hh + 2 + e] = pv.c[j] * u2.y;
+              }
             }
           }
           if (ps == 0) ga = pv.gamma_a;
           __syncthreads();
         }
-        uint32_t uh0, ul0, uh1, ul1;
-        split_pair(cu[0], cu[1], uh0, ul0);
-        split_pair(cu[2], cu[3], uh1, ul1);
+        uint32_t uh[4], ul[4];  // A fragment a0..a3, hi and lo halves
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_pair(cu[2 * i], cu[2 * i + 1], uh[i], ul[i]);
 #pragma unroll 2
         for (int ks = 0; ks < 8; ++ks) {
           const int c0 = 16 * ks + 4 * q;
@@ -417,11 +428,14 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
 #pragma unroll
           for (int tt = 0; tt < 2; ++tt) {
             const int pc = 16 * ks + 4 * (g >> 1) + 2 * tt + (g & 1);
-            const uint32_t k0 = *reinterpret_cast<const unsigned short*>(pathk + (2 * q) * kWPathStride + pc * 2);
-            const uint32_t k1 = *reinterpret_cast<const unsigned short*>(pathk + (2 * q + 1) * kWPathStride + pc * 2);
-            const uint32_t bk = k0 | (k1 << 16);
-            mma16816_bf16_nv(du[tt], uh0, uh1, 0u, 0u, bk, 0u);
-            mma16816_bf16_nv(du[tt], ul0, ul1, 0u, 0u, bk, 0u);
+            // b0: key rows of entries 2q, 2q+1; b1: of entries 2q+8, 2q+9
+            const unsigned char* kc = pathk + pc * 2;
+            const uint32_t b0 = static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(kc + (2 * q) * kWPathStride)) |
+                                (static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(kc + (2 * q + 1) * kWPathStride)) << 16);
+            const uint32_t b1 = static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(kc + (2 * q + 8) * kWPathStride)) |
+                                (static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(kc + (2 * q + 9) * kWPathStride)) << 16);
+            mma16816_bf16_nv(du[tt], uh[0], uh[1], uh[2], uh[3], b0, b1);
+            mma16816_bf16_nv(du[tt], ul[0], ul[1], ul[2], ul[3], b0, b1);
           }
 #pragma unroll
           for (int hr = 0; hr < 2; ++hr) {
