@@ -242,9 +242,9 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
   // entries per pass over the state tile; a bf16 pool is rounded at the end of
   // each pass, so it takes their fused form only while every path fits one
   // pass (S_a rounded once, as the separate commit does).
-  const bool small = next->max_nodes <= treewy::kWarpTreeNodes;
+  const bool small = next->max_nodes <= treewy::kWarpFusedNodes;
   const int seg = next->max_nodes <= treewy::kSmallTreeNodes ? treewy::kSmallTreeNodes
-                                                              : treewy::kWarpTreeNodes;
+                                                              : treewy::kWarpFusedNodes;
   const bool small_fused_ok = !(next->flags & TREEWY_FLAG_STATE_BF16) || prev->max_nodes <= seg;
   if (use_tensor_cores(next) && next->T > 0 && prev->qkv_dtype == TREEWY_DTYPE_BF16 &&
       (!small || small_fused_ok)) {

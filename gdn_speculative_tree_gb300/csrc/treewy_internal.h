@@ -67,11 +67,13 @@ struct PrevRound;
 cudaError_t launch_verify_small(const treewy_batch& b, const CUtensorMap& state_map,
                                 const PrevRound* prev, cudaStream_t stream);
 
-// Batches of at most this many nodes per tree (and more than
+// Batches of at most kWarpTreeNodes nodes per tree (and more than
 // kSmallTreeNodes) are verified by warp-level MMAs over the whole method
-// (verify_warp.cu); larger trees by the tcgen05 kernel, whose state products
+// (verify_warp.cu), with the previous round's commit fused in front up to
+// kWarpFusedNodes; larger trees by the tcgen05 kernel, whose state products
 // run at several times the rate of warp-level MMAs.
-constexpr int kWarpTreeNodes = 16;
+constexpr int kWarpTreeNodes = 32;
+constexpr int kWarpFusedNodes = 16;
 cudaError_t launch_verify_warp(const treewy_batch& b, const CUtensorMap& state_map,
                                const PrevRound* prev, cudaStream_t stream);
 

@@ -1082,13 +1082,9 @@ cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, const PrevRou
 template <bool SB>
 cudaError_t launch_tc(const treewy_batch& b, const VerifyMaps& m, const PrevRound* prev, int npm,
                       cudaStream_t stream) {
-  // trees of more than 16 nodes (smaller ones go to the small-tree and
-  // warp-MMA kernels, fused or not)
-  if (prev == nullptr) {
-    const PrevRound none{};
-    if (npm <= 32) return launch_npm<32, false, SB>(b, m, none, stream);
-    return launch_npm<64, false, SB>(b, m, none, stream);
-  }
+  // plain verification of trees of more than 32 nodes, the fused form above
+  // 16 nodes (smaller trees go to the small-tree and warp-MMA kernels)
+  if (prev == nullptr) return launch_npm<64, false, SB>(b, m, PrevRound{}, stream);
   if (npm <= 32) return launch_npm<32, true, SB>(b, m, *prev, stream);
   return launch_npm<64, true, SB>(b, m, *prev, stream);
 }

@@ -1,4 +1,4 @@
-// verify_warp.cu -- TreeWY verification of trees of 9 to 16 nodes with
+// verify_warp.cu -- TreeWY verification of trees of 9 to 32 nodes with
 // warp-level MMAs, dk = dv = 128, bf16 q/k/v, fp32 or bf16 committed state.
 //
 // One CTA of 256 threads per (request, head).  The state tile lands in
@@ -28,15 +28,16 @@
 //           children) are multiplied.
 //  store    each lane writes its two adjacent value rows of U[n] and o_n.
 //
-// The kernel is written for a capacity NPM of up to 64 nodes, but launched
-// for NPM = 16 only: three CTAs per SM fit (76 KB of shared memory, 80
-// registers; a bf16 pool's instances four, 44 KB and 64 registers: its 32 KB
-// tile region also holds the Gram rows and the [T;B] halves), and the tile
-// count is small.  At 32 nodes it measured level
-// with the tcgen05 kernel, at 64 nodes ~35 % slower: the first products take
-// two warp MMAs per 8-node tile and state element pair (hi and lo), and warp
-// MMAs run at ~0.47 m16n8k16 per cycle per SM, about a quarter of the tcgen05
-// rate, so two resident 64-node CTAs keep the MMA pipe saturated.
+// The kernel is written for a capacity NPM of up to 64 nodes, and launched
+// for NPM = 16 (plain and fused) and 32 (plain): three CTAs per SM fit (76 KB
+// of shared memory at 16 nodes, 68 KB at 32 with the fp32 state streamed
+// through a ring of three of its four boxes, 80 registers; a bf16 pool's
+// 16-node instances four CTAs, 44 KB and 64 registers: its 32 KB tile region
+// also holds the Gram rows and the [T;B] halves).  At 64 nodes it measured
+// ~35 % slower than the tcgen05 kernel: the first products take two warp
+// MMAs per 8-node tile and state element pair (hi and lo), and warp MMAs run
+// at ~0.47 m16n8k16 per cycle per SM, about a quarter of the tcgen05 rate,
+// so two resident 64-node CTAs keep the MMA pipe saturated.
 #include "treewy_device.cuh"
 #include "treewy_internal.h"
 
@@ -51,7 +52,8 @@ constexpr int kWRegPath = 8;             // root paths up to this long stay in r
 
 template <int NPM>
 struct WarpTree {
-  uint64_t bar;  // state tile landed
+  uint64_t bar;   // state tile landed (ring: boxes 0-2)
+  uint64_t bar3;  // ring: box 3 landed in box 0's slot
   int par[NPM];
   float alpha[NPM];
   float beta[NPM];
@@ -87,20 +89,25 @@ template <int NPM, bool SB>
 struct WarpCfg {
   static constexpr int kSlots = 2 * NPM;  // keys 0..NPM-1, queries NPM..2NPM-1
   static constexpr int kKT = NPM / 8;     // n8-tiles of keys (and of queries)
-  // a bf16 pool's 16-node instances: the 32 KB tile region also holds the
-  // Gram rows (box 0) and the [T;B] halves (box 1)
-  static constexpr bool kCompact = SB && NPM == 16;
-  static constexpr uint32_t kKQOff = (kCompact ? 2u : 4u) * kWBox;
+  // A bf16 pool's instances: the 32 KB tile region also holds the Gram rows
+  // (box 0) and the [T;B] halves (box 1).  32-node instances on an fp32 pool
+  // keep three of the four 16 KB state boxes at a time: box 3 lands in box
+  // 0's slot once every warp has multiplied box 0 (a ring of 48 KB), the
+  // Gram rows go over slot 0, the [T;B] halves into slots 1 and 2.  Both
+  // leave room for three CTAs per SM.
+  static constexpr bool kCompact = SB;
+  static constexpr bool kRing = !SB && NPM == 32;
+  static constexpr uint32_t kKQOff = (kCompact ? 2u : (kRing ? 3u : 4u)) * kWBox;
   static constexpr uint32_t kKQBytes = kSlots * kWKQStride;
   static constexpr uint32_t kTreeOff = kKQOff + kKQBytes;
   static constexpr uint32_t kEnd = kTreeOff + static_cast<uint32_t>(sizeof(WarpTree<NPM>));
   static constexpr uint32_t kDynSmem = 1024u + kEnd;
-  static constexpr int kBlocks = kCompact ? 4 : (NPM == 16 ? 3 : 2);  // CTAs per SM
+  static constexpr int kBlocks = (SB && NPM == 16) ? 4 : (NPM <= 32 ? 3 : 2);  // CTAs per SM
   static_assert(kBlocks * (kDynSmem + 1024u) <= 228u * 1024u, "CTAs per SM");
   static_assert(8u * NPM * NPM <= kKQBytes, "x scratch of 2 NPM long paths");
   static_assert(2 * NPM <= kWThreads && NPM <= 64, "one operand row per thread");
   static_assert(kWPathOff + kWSeg * kWPathStride <= kKQBytes, "fused commit staging");
-  static_assert(kWSeg == kWarpTreeNodes, "a bf16 pool's fused form needs one pass per path");
+  static_assert(kWSeg == kWarpFusedNodes, "a bf16 pool's fused form needs one pass per path");
 };
 
 // Fragment row g of a warp's tiles stands for state rows 16 w + 2 f(g) (row
@@ -276,12 +283,14 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
   // the state tile, requested once this thread's own loads are on their way
   if (t == 0) {
     mbar_init(&ts.bar, 1);
+    if constexpr (C::kRing) mbar_init(&ts.bar3, 1);
     fence_mbarrier_init();
     if (have_s0) {
       const int y = (slot * H + h) * kWDim;
-      mbar_arrive_expect_tx(&ts.bar, SB ? 2u * kWBox : 4u * kWBox);
+      constexpr int kFirst = SB ? 2 : (C::kRing ? 3 : 4);  // boxes requested now
+      mbar_arrive_expect_tx(&ts.bar, kFirst * kWBox);
 #pragma unroll
-      for (int c = 0; c < (SB ? 2 : 4); ++c)
+      for (int c = 0; c < kFirst; ++c)
         tma_load_2d(s0 + c * kWBox, &map_s0, &ts.bar, (SB ? 64 : 32) * c, y);
     }
   }
@@ -481,6 +490,7 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
     }
   }
 
+  int ring_fail = 0;  // ring: the wait for box 3 gave up (uniform)
   if (go) {
     // ---- MMA 1: acc[nt] = S0 [K;Q]^T, tile nt of slots 8 nt .. 8 nt + 7
     //      (keys: nt < KT; queries: nt >= KT).  Within a k-step of 16 state
@@ -493,6 +503,21 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
 #pragma unroll 2
     for (int ks = 0; ks < 8; ++ks) {
       const int c0 = 16 * ks + 4 * q;
+      if constexpr (C::kRing) {
+        if (ks == 2) {
+          // every warp is done with box 0: box 3 into its slot
+          __syncthreads();
+          if (t == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&ts.bar3, kWBox);
+            tma_load_2d(s0, &map_s0, &ts.bar3, 96, (slot * H + h) * kWDim);
+          }
+        } else if (ks == 6) {
+          int f3 = 0;
+          if (t == 0 && !mbar_wait(&ts.bar3, 0)) f3 = 1;
+          ring_fail = __syncthreads_or(f3);
+        }
+      }
       uint32_t ah[4], al4[4];
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
@@ -504,8 +529,9 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
           ah[hr] = raw.x;
           ah[2 + hr] = raw.y;
         } else {
-          const float4 x = *reinterpret_cast<const float4*>(s0 + (c0 >> 5) * kWBox + rr * 128 +
-                                                            ((((c0 & 31) >> 2) ^ sr) << 4));
+          const int box = c0 >> 5;  // its slot: box 3 reuses box 0's (ring)
+          const float4 x = *reinterpret_cast<const float4*>(s0 + ((C::kRing && box == 3) ? 0 : box) * kWBox +
+                                                            rr * 128 + ((((c0 & 31) >> 2) ^ sr) << 4));
           split_pair(x.x, x.y, ah[hr], al4[hr]);
           split_pair(x.z, x.w, ah[2 + hr], al4[2 + hr]);
         }
@@ -537,6 +563,7 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
         }
       }
     }
+    if (!ring_fail) {
 
     // ---- W in the key tiles, gamma_n S0 q_n in the query tiles (zero for
     //      nodes past N), then W as MMA 2's A fragments in hi + lo bf16:
@@ -619,8 +646,8 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
 
     // ---- operand rows of [T;B]: thread t < NPM the T row of node t, thread
     //      NPM + n the B row of node n, over boxes 2 (hi) and 3 (lo)
-    unsigned char* oph = s0 + (C::kCompact ? kWBox : 2 * kWBox);
-    unsigned char* opl = s0 + (C::kCompact ? kWBox + 4096 : 3 * kWBox);
+    unsigned char* oph = s0 + (C::kCompact || C::kRing ? kWBox : 2 * kWBox);
+    unsigned char* opl = C::kCompact ? oph + 2 * NPM * 128 : s0 + (C::kRing ? 2 : 3) * kWBox;
     if (t < 2 * NPM) {
       const bool isB = t >= NPM;
       const int n = isB ? t - NPM : t;
@@ -749,10 +776,11 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
         }
       }
     }
+    }  // !ring_fail
   }
 
   if (t == 0) {
-    int bits = fail ? kStatusTimeout : 0;
+    int bits = (fail || ring_fail) ? kStatusTimeout : 0;
     if (h == 0) bits |= flags | cflags | (issued && bad_tree ? TREEWY_STATUS_BAD_TREE : 0);
     // the previous tree failed its checks, or a wait gave up before S_a was
     // stored: that request's commit did not happen
@@ -761,6 +789,7 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
     if (bits) atomicOr(b.status + r, bits);
     // no copy may still target this CTA's memory at exit
     if (fail) mbar_wait(&ts.bar, 0);
+    if (C::kRing && ring_fail) mbar_wait(&ts.bar3, 0);
     if (stored) bulk_wait_group_read0();
   }
 }
@@ -789,10 +818,13 @@ cudaError_t launch_warp(const treewy_batch& b, const CUtensorMap& map_s0, const 
 
 cudaError_t launch_verify_warp(const treewy_batch& b, const CUtensorMap& map_s0, const PrevRound* prev,
                                cudaStream_t stream) {
-  static_assert(kWarpTreeNodes == 16, "launched for the 16-node capacity");
+  static_assert(kWarpTreeNodes == 32 && kWarpFusedNodes == 16, "launched capacities");
   const bool sb = (b.flags & TREEWY_FLAG_STATE_BF16) != 0;
   if (prev == nullptr) {
     const PrevRound none{};
+    if (b.max_nodes > 16)
+      return sb ? launch_warp<32, true, false>(b, map_s0, none, stream)
+                : launch_warp<32, false, false>(b, map_s0, none, stream);
     return sb ? launch_warp<16, true, false>(b, map_s0, none, stream)
               : launch_warp<16, false, false>(b, map_s0, none, stream);
   }

@@ -80,7 +80,7 @@ enum {
 enum {
   /* Use the portable kernels (CUDA cores, no bulk tensor copies) even where
      the tensor-core verification (dk = dv = 128, bf16 q/k/v: warp-level
-     MMAs for batches of trees of at most 16 nodes, tcgen05 above) or the
+     MMAs for batches of trees of at most 32 nodes, tcgen05 above) or the
      bulk-copy commit (dk = dv = 128) applies.  Same results within rounding. */
   TREEWY_FLAG_FORCE_GENERIC = 1u,
   /* The state pool holds bf16 instead of f32: the dtype in which the GDN

@@ -91,13 +91,13 @@ def test_small_gate_edges(cuda_lib, alpha, beta, cap):
 
 def test_small_agrees_with_tensor_cores(cuda_lib):
     """The same batch through the small-tree kernel (max_nodes 8) and the
-    tcgen05 kernel (max_nodes 32): both within tolerance of the oracle, and of
+    tcgen05 kernel (max_nodes 64): both within tolerance of the oracle, and of
     each other."""
     trees, acc = shapes()
     w_small = custom(trees, acc, seed=5)
     w_tc = custom(trees, acc, seed=5)
     small = CudaRun(w_small)
-    tc = CudaRun(w_tc, max_nodes=32)
+    tc = CudaRun(w_tc, max_nodes=64)
     assert not small.status.any() and not tc.status.any()
     assert_within(compare(w_small, small, range(w_small.R)), "small kernel")
     assert_within(compare(w_tc, tc, range(w_tc.R)), "tensor-core kernel")

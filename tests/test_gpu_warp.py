@@ -1,9 +1,11 @@
-"""GPU parity of the warp-MMA verification (batches whose trees have at most
-16 nodes and more than 8: dk = dv = 128 with bf16 q/k/v) against the oracle
-on the same seeded inputs: every size from 1 to 16 in chain, star, forest and
-random shapes (chains longer than 8 take the kernel's general root-path
-recurrence, shorter paths its register form), the smallest capacity routed
-to it (9), ragged batches with empty trees, gates at the ends of their range,
+"""GPU parity of the warp-MMA verification (batches whose trees have 9 to 32
+nodes: dk = dv = 128 with bf16 q/k/v; capacities 16 and 32, the latter with
+an fp32 state streamed through a ring of three of its four boxes) against the
+oracle on the same seeded inputs: every size from 1 to 16 (and 32) in chain,
+star, forest and random shapes (chains longer than 8 take the kernel's general
+root-path recurrence, shorter paths its register form), the smallest
+capacities routed to it (9, 17), ragged batches with empty trees, gates at the
+ends of their range,
 a bf16 state pool, device-side errors, CUDA-graph replay, agreement with
 the small-tree and tcgen05 kernels on the same inputs, and the commit fused
 in front (paths of 1 to 64 entries, both pools, refusals, against the two
@@ -27,25 +29,29 @@ from tests.test_gpu_small import (check_two_rounds, custom, random_tree, run_com
 
 pytestmark = pytest.mark.gpu
 
-CAP = 16  # node capacity of the warp-MMA kernel
+CAP = 16   # node capacity of the warp-MMA kernel's fused form
+CAP2 = 32  # ... and of its plain verification
 
 
-def test_warp_every_size_and_shape(cuda_lib):
-    trees, acc = shapes(CAP)
-    w = custom(trees, acc)
-    assert w.max_nodes == CAP
+@pytest.mark.parametrize("cap", [CAP, CAP2])
+def test_warp_every_size_and_shape(cuda_lib, cap):
+    trees, acc = shapes(cap)
+    w = custom(trees, acc, H=2 if cap > CAP else 3)
+    assert w.max_nodes == cap
     run = CudaRun(w)
     assert not run.status.any()
-    assert_within(compare(w, run, range(w.R)), "warp kernel shapes")
+    assert_within(compare(w, run, range(w.R)), f"warp kernel shapes, capacity {cap}")
 
 
-@pytest.mark.parametrize("max_nodes,sizes", [(9, [9, 1, 9, 0, 4]), (16, [16]), (12, [12, 11, 3])])
+@pytest.mark.parametrize("max_nodes,sizes", [(9, [9, 1, 9, 0, 4]), (16, [16]), (12, [12, 11, 3]),
+                                             (17, [17, 1, 17, 0, 9]), (32, [32]), (24, [24, 20, 18])])
 def test_warp_capacities(cuda_lib, max_nodes, sizes):
-    """The smallest capacity routed to the kernel (9) and full trees at it."""
+    """The smallest capacities routed to the kernel's two instances (9, 17)
+    and full trees at them."""
     rng = np.random.default_rng(max_nodes + len(sizes))
     trees = [random_tree(rng, n) for n in sizes]
-    if sizes[0] == 16:
-        trees = [wl.chain_parents(16)]  # the longest root path
+    if len(sizes) == 1:
+        trees = [wl.chain_parents(sizes[0])]  # the longest root path
     acc = [len(t) - 1 for t in trees]
     w = custom(trees, acc, H=2, max_nodes=max_nodes)
     run = CudaRun(w)
@@ -53,12 +59,13 @@ def test_warp_capacities(cuda_lib, max_nodes, sizes):
     assert_within(compare(w, run, range(w.R)), f"capacity {max_nodes}, sizes {sizes}")
 
 
-@pytest.mark.parametrize("sizes,H", [([0, 13, 0, 16, 1, 0, 9], 5), ([15] * 7 + [0], 1), ([10, 2, 14, 0], 7)])
+@pytest.mark.parametrize("sizes,H", [([0, 13, 0, 16, 1, 0, 9], 5), ([15] * 7 + [0], 1), ([10, 2, 14, 0], 7),
+                                     ([0, 29, 0, 32, 1, 0, 17], 5), ([31] * 5 + [0], 1)])
 def test_warp_ragged_with_empty_trees(cuda_lib, sizes, H):
     rng = np.random.default_rng(sum(sizes) + H)
     trees = [random_tree(rng, n) for n in sizes]
     acc = [len(t) - 1 for t in trees]
-    w = custom(trees, acc, H=H, max_nodes=CAP)
+    w = custom(trees, acc, H=H, max_nodes=CAP if max(sizes) <= CAP else CAP2)
     run = CudaRun(w)
     assert not run.status.any()
     assert_within(compare(w, run, range(w.R)), f"ragged {sizes}")
@@ -68,8 +75,9 @@ def test_warp_ragged_with_empty_trees(cuda_lib, sizes, H):
                                         ((0.9, 0.999), ("const", 0.0)),
                                         ((0.01, 0.05), ("uniform", 0.05, 0.95)),
                                         ((0.999999, 0.9999999), ("uniform", 0.9999, 0.99999))])
-def test_warp_gate_edges(cuda_lib, alpha, beta):
-    trees, acc = shapes(CAP)
+@pytest.mark.parametrize("cap", [CAP, CAP2])
+def test_warp_gate_edges(cuda_lib, alpha, beta, cap):
+    trees, acc = shapes(cap)
     w = custom(trees, acc, alpha=alpha, beta=beta, seed=41)
     run = CudaRun(w)
     assert not run.status.any()
@@ -77,14 +85,14 @@ def test_warp_gate_edges(cuda_lib, alpha, beta):
 
 
 def test_warp_agrees_with_other_kernels(cuda_lib):
-    """The same batch through the warp-MMA kernel (max_nodes 16) and the
-    tcgen05 kernel (max_nodes 32), and its trees of at most 8 nodes through
-    the small-tree kernel as well: all within tolerance of the oracle and of
-    each other, with identical decays (the same products of alpha in the same
-    order)."""
+    """The same batch through the warp-MMA kernel (max_nodes 16 and 32) and
+    the tcgen05 kernel (max_nodes 64), and its trees of at most 8 nodes
+    through the small-tree kernel as well: all within tolerance of the oracle
+    and of each other, with identical decays (the same products of alpha in
+    the same order)."""
     trees, acc = shapes(CAP)
     runs = {}
-    for name, mn in (("warp", 16), ("tcgen05", 32)):
+    for name, mn in (("warp", 16), ("warp32", 32), ("tcgen05", 64)):
         w = custom(trees, acc, seed=5)
         runs[name] = (w, CudaRun(w, max_nodes=mn))
     for name, (w, run) in runs.items():
@@ -94,6 +102,9 @@ def test_warp_agrees_with_other_kernels(cuda_lib):
     assert float(np.abs(warp.o - tc.o).max()) <= 2 * O_TOL * float(np.abs(tc.o).max())
     assert float(np.abs(warp.U - tc.U).max()) <= 2 * U_TOL * float(np.abs(tc.U).max())
     assert np.array_equal(warp.gamma, tc.gamma)
+    w32 = runs["warp32"][1]
+    assert float(np.abs(w32.o - tc.o).max()) <= 2 * O_TOL * float(np.abs(tc.o).max())
+    assert np.array_equal(w32.gamma, tc.gamma)
     small_trees = [t for t in trees if len(t) <= 8]
     small_acc = [a for t, a in zip(trees, acc) if len(t) <= 8]
     ws, ww = custom(small_trees, small_acc, seed=9), custom(small_trees, small_acc, seed=9)
@@ -115,11 +126,12 @@ def test_warp_deterministic(cuda_lib):
     assert torch.equal(o1, tv.o) and torch.equal(u1, tv.U)
 
 
-def test_warp_bf16_state(cuda_lib):
+@pytest.mark.parametrize("cap", [CAP, CAP2])
+def test_warp_bf16_state(cuda_lib, cap):
     """A bf16 state pool: verification reads the bf16 S0 exactly (o and U to
     the fp32 tolerances), the commit rounds S_a once to bf16:
     |S_gpu - S_ref| <= 2^-8 |S_ref| + 1e-3 max|S_ref|."""
-    trees, acc = shapes(CAP)
+    trees, acc = shapes(cap)
     w = custom(trees, acc, seed=73, state_dtype="bf16")
     run = CudaRun(w, flags=binding.FLAG_STATE_BF16)
     assert not run.status.any()
@@ -142,17 +154,19 @@ def test_warp_bf16_state(cuda_lib):
     assert g_err <= G_TOL, g_err
 
 
-def test_warp_bad_inputs_set_status_and_spare_others(cuda_lib):
-    rng = np.random.default_rng(29)
-    trees = [random_tree(rng, n) for n in (12, 15, 16, 10, 9, 14)]
-    trees[1][11] = 13                      # parent after child
+@pytest.mark.parametrize("cap", [CAP, CAP2])
+def test_warp_bad_inputs_set_status_and_spare_others(cuda_lib, cap):
+    rng = np.random.default_rng(29 + cap)
+    k = cap - CAP                          # sizes shifted into the capacity tested
+    trees = [random_tree(rng, n + k) for n in (12, 15, 16, 10, 9, 14)]
+    trees[1][11] = 13 + k                  # parent after child
     trees[5][13] = 13                      # parent is the node itself
-    acc = [3, 2, 1, 10, 0, 1]              # request 3: accepted outside its 10-node tree
-    w = custom(trees, acc, max_nodes=CAP, extra_slots=2)
+    acc = [3, 2, 1, 10 + k, 0, 1]          # request 3: accepted outside its tree
+    w = custom(trees, acc, max_nodes=cap, extra_slots=2)
     slots = w.state_slot.clone()
     slots[4] = -1                          # outside the pool
     w.state_slot.copy_(slots)
-    tv = binding.TreeVerifier(w, max_nodes=15)  # request 2 (16 nodes) exceeds it
+    tv = binding.TreeVerifier(w, max_nodes=cap - 1)  # request 2 (cap nodes) exceeds it
     tv.o.fill_(float("nan"))
     tv.U.fill_(float("nan"))
     S_before = w.state.clone()
