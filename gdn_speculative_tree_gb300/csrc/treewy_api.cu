@@ -238,14 +238,20 @@ treewy_status treewy_commit_verify(const treewy_batch* prev, const int32_t* prev
   if (!aligned16(prev->U)) return fail(TREEWY_ERR_INVALID_ARG, "prev->U must be 16-byte aligned");
   if (!prev_accepted) return fail(TREEWY_ERR_INVALID_ARG, "prev_accepted is NULL");
   cudaError_t err;
-  // The small-tree and warp-MMA kernels apply an accepted path 8 or 16
-  // entries per pass over the state tile; a bf16 pool is rounded at the end of
-  // each pass, so it takes their fused form only while every path fits one
-  // pass (S_a rounded once, as the separate commit does).
-  const bool small = next->max_nodes <= treewy::kWarpFusedNodes;
+  // Kernel for the next round: the small-tree kernel up to 8 nodes, the
+  // warp-MMA kernel up to 16 (up to 32 for a bf16 pool, whose fused or
+  // two-call form there beats the tcgen05 kernel's), the tcgen05 kernel
+  // above.  The warp-MMA kernels apply an accepted path 8 or 16 entries per
+  // pass over the state tile; a bf16 pool is rounded at the end of each pass,
+  // so it takes their fused form only while every path fits one pass (S_a
+  // rounded once, as the separate commit does), and otherwise the commit and
+  // the verification run as two calls.
+  const bool bf16_pool = (next->flags & TREEWY_FLAG_STATE_BF16) != 0;
+  const bool small = next->max_nodes <= treewy::kFusedWarpNodes ||
+                     (bf16_pool && next->max_nodes <= treewy::kWarpTreeNodes);
   const int seg = next->max_nodes <= treewy::kSmallTreeNodes ? treewy::kSmallTreeNodes
-                                                              : treewy::kWarpFusedNodes;
-  const bool small_fused_ok = !(next->flags & TREEWY_FLAG_STATE_BF16) || prev->max_nodes <= seg;
+                                                              : treewy::kWarpSegEntries;
+  const bool small_fused_ok = !bf16_pool || prev->max_nodes <= seg;
   if (use_tensor_cores(next) && next->T > 0 && prev->qkv_dtype == TREEWY_DTYPE_BF16 &&
       (!small || small_fused_ok)) {
     treewy::PrevRound pr;

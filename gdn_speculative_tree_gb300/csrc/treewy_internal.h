@@ -70,10 +70,14 @@ cudaError_t launch_verify_small(const treewy_batch& b, const CUtensorMap& state_
 // Batches of at most kWarpTreeNodes nodes per tree (and more than
 // kSmallTreeNodes) are verified by warp-level MMAs over the whole method
 // (verify_warp.cu), with the previous round's commit fused in front up to
-// kWarpFusedNodes; larger trees by the tcgen05 kernel, whose state products
-// run at several times the rate of warp-level MMAs.
+// kFusedWarpNodes (fp32 pool) or kWarpTreeNodes (bf16 pool); larger trees by
+// the tcgen05 kernel, whose state products run at several times the rate of
+// warp-level MMAs.
 constexpr int kWarpTreeNodes = 32;
-constexpr int kWarpFusedNodes = 16;
+constexpr int kFusedWarpNodes = 16;
+// Path entries the warp-MMA kernel applies per update pass of its fused
+// commit (a bf16 pool takes the fused form when every path fits one pass).
+constexpr int kWarpSegEntries = 16;
 cudaError_t launch_verify_warp(const treewy_batch& b, const CUtensorMap& state_map,
                                const PrevRound* prev, cudaStream_t stream);
 

@@ -1082,10 +1082,13 @@ cudaError_t launch_npm(const treewy_batch& b, const VerifyMaps& m, const PrevRou
 template <bool SB>
 cudaError_t launch_tc(const treewy_batch& b, const VerifyMaps& m, const PrevRound* prev, int npm,
                       cudaStream_t stream) {
-  // plain verification of trees of more than 32 nodes, the fused form above
-  // 16 nodes (smaller trees go to the small-tree and warp-MMA kernels)
+  // plain verification of trees of more than 32 nodes; the fused form above
+  // 16 nodes for an fp32 pool, above 32 for a bf16 one (smaller trees go to
+  // the small-tree and warp-MMA kernels)
   if (prev == nullptr) return launch_npm<64, false, SB>(b, m, PrevRound{}, stream);
-  if (npm <= 32) return launch_npm<32, true, SB>(b, m, *prev, stream);
+  if constexpr (!SB) {
+    if (npm <= 32) return launch_npm<32, true, false>(b, m, *prev, stream);
+  }
   return launch_npm<64, true, SB>(b, m, *prev, stream);
 }
 

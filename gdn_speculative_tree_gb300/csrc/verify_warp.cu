@@ -85,7 +85,7 @@ static_assert(sizeof(WarpPrev) <= kWPathOff, "previous tree before the key rows"
 // the hi and lo halves of the [T;B] operand (boxes 2 and 3), the 2 NPM K/Q
 // slot rows (later the x scratch of root paths longer than kWRegPath), the
 // tree.
-template <int NPM, bool SB>
+template <int NPM, bool SB, bool FUSED>
 struct WarpCfg {
   static constexpr int kSlots = 2 * NPM;  // keys 0..NPM-1, queries NPM..2NPM-1
   static constexpr int kKT = NPM / 8;     // n8-tiles of keys (and of queries)
@@ -96,18 +96,19 @@ struct WarpCfg {
   // Gram rows go over slot 0, the [T;B] halves into slots 1 and 2.  Both
   // leave room for three CTAs per SM.
   static constexpr bool kCompact = SB;
-  static constexpr bool kRing = !SB && NPM == 32;
+  static constexpr bool kRing = !SB && NPM == 32 && !FUSED;
   static constexpr uint32_t kKQOff = (kCompact ? 2u : (kRing ? 3u : 4u)) * kWBox;
   static constexpr uint32_t kKQBytes = kSlots * kWKQStride;
   static constexpr uint32_t kTreeOff = kKQOff + kKQBytes;
   static constexpr uint32_t kEnd = kTreeOff + static_cast<uint32_t>(sizeof(WarpTree<NPM>));
   static constexpr uint32_t kDynSmem = 1024u + kEnd;
-  static constexpr int kBlocks = (SB && NPM == 16) ? 4 : (NPM <= 32 ? 3 : 2);  // CTAs per SM
+  // CTAs per SM (a fused fp32 32-node instance keeps the whole tile: two)
+  static constexpr int kBlocks = (SB && NPM == 16) ? 4 : ((NPM == 16 || SB || kRing) ? 3 : 2);
   static_assert(kBlocks * (kDynSmem + 1024u) <= 228u * 1024u, "CTAs per SM");
   static_assert(8u * NPM * NPM <= kKQBytes, "x scratch of 2 NPM long paths");
   static_assert(2 * NPM <= kWThreads && NPM <= 64, "one operand row per thread");
   static_assert(kWPathOff + kWSeg * kWPathStride <= kKQBytes, "fused commit staging");
-  static_assert(kWSeg == kWarpFusedNodes, "a bf16 pool's fused form needs one pass per path");
+  static_assert(kWSeg == kWarpSegEntries, "entries per update pass");
 };
 
 // Fragment row g of a warp's tiles stands for state rows 16 w + 2 f(g) (row
@@ -151,10 +152,10 @@ __device__ __forceinline__ void put_op(unsigned char* oph, unsigned char* opl, i
 // half runs exactly when its separate call would: a refused commit leaves the
 // state alone, a bad next tree still commits.
 template <int NPM, bool SB, bool FUSED>
-__global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
+__global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB, FUSED>::kBlocks)
     verify_warp_kernel(const __grid_constant__ CUtensorMap map_s0, const treewy_batch b,
                        const PrevRound prev) {
-  using C = WarpCfg<NPM, SB>;
+  using C = WarpCfg<NPM, SB, FUSED>;
   constexpr int KT = C::kKT;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -797,7 +798,7 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB>::kBlocks)
 template <int NPM, bool SB, bool FUSED>
 cudaError_t launch_warp(const treewy_batch& b, const CUtensorMap& map_s0, const PrevRound& prev,
                         cudaStream_t stream) {
-  using C = WarpCfg<NPM, SB>;
+  using C = WarpCfg<NPM, SB, FUSED>;
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t attr = once_per_device(attr_done, [] {
     cudaError_t e = cudaFuncSetAttribute(verify_warp_kernel<NPM, SB, FUSED>,
@@ -818,7 +819,7 @@ cudaError_t launch_warp(const treewy_batch& b, const CUtensorMap& map_s0, const 
 
 cudaError_t launch_verify_warp(const treewy_batch& b, const CUtensorMap& map_s0, const PrevRound* prev,
                                cudaStream_t stream) {
-  static_assert(kWarpTreeNodes == 32 && kWarpFusedNodes == 16, "launched capacities");
+  static_assert(kWarpTreeNodes == 32 && kFusedWarpNodes == 16, "launched capacities");
   const bool sb = (b.flags & TREEWY_FLAG_STATE_BF16) != 0;
   if (prev == nullptr) {
     const PrevRound none{};
@@ -828,6 +829,10 @@ cudaError_t launch_verify_warp(const treewy_batch& b, const CUtensorMap& map_s0,
     return sb ? launch_warp<16, true, false>(b, map_s0, none, stream)
               : launch_warp<16, false, false>(b, map_s0, none, stream);
   }
+  // the fused 32-node form is launched for a bf16 pool only (an fp32 pool's
+  // runs on the tcgen05 kernel)
+  if (b.max_nodes > 16)
+    return sb ? launch_warp<32, true, true>(b, map_s0, *prev, stream) : cudaErrorInvalidValue;
   return sb ? launch_warp<16, true, true>(b, map_s0, *prev, stream)
             : launch_warp<16, false, true>(b, map_s0, *prev, stream);
 }

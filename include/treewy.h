@@ -192,8 +192,8 @@ treewy_status treewy_commit(const treewy_batch* batch, const int32_t* accepted,
  * results equal treewy_commit(prev, prev_accepted) followed by
  * treewy_verify(next), with one state read per head instead of two.  (Shapes
  * other than dk = dv = 128 with bf16 q/k/v in both rounds, and a bf16 pool
- * whose next trees have at most 8 (16) nodes while the previous ones have
- * more than 8 (16),
+ * whose next trees have at most 8 nodes while the previous ones have more
+ * than 8, or 9 to 32 nodes while the previous ones have more than 16,
  * run as those two calls back to back on `stream`.)  A request with no node
  * in `next` still gets its commit.  prev and next must have the
  * same R, H, dk, dv, state pool pointer, num_slots, state_slot pointer and

@@ -229,8 +229,9 @@ def test_warp_graph_replay_matches_eager(cuda_lib):
     assert torch.equal(w.state.cpu(), run.S_after.cpu())
 
 
+@pytest.mark.parametrize("cap", [CAP, CAP2])
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
-def test_warp_commit_verify_matches_oracle(cuda_lib, state_dtype):
+def test_warp_commit_verify_matches_oracle(cuda_lib, state_dtype, cap):
     """treewy_commit_verify whose next trees have 9 to 16 nodes: accepted paths
     from the root only to 64 entries (four update passes of 16 entries for an
     fp32 pool; a bf16 pool with previous trees above 16 nodes takes the commit
@@ -241,17 +242,18 @@ def test_warp_commit_verify_matches_oracle(cuda_lib, state_dtype):
     prev_trees = [random_tree(rng, n) for n in (40, 4, 64, 8, 1, 12, 9, 16)]
     prev_trees[2] = wl.chain_parents(64)
     prev_trees[6] = wl.chain_parents(17)    # a path of one pass + 1 entry
-    next_trees = [random_tree(rng, n) for n in (CAP, 2, 0, 1, CAP - 1, 3, 9, 12)]
-    next_trees[0] = wl.chain_parents(CAP)   # the longest next root path
+    next_trees = [random_tree(rng, n) for n in (cap, 2, 0, 1, cap - 1, 3, 9, 12)]
+    next_trees[0] = wl.chain_parents(cap)   # the longest next root path
     accepted = [39, -1, 63, 5, 0, 11, 16, 15]
-    prev, nxt = two_rounds(prev_trees, next_trees, accepted, cap=CAP, state_dtype=state_dtype)
+    prev, nxt = two_rounds(prev_trees, next_trees, accepted, cap=cap, state_dtype=state_dtype)
     tn, S0_pool = run_commit_verify(prev, nxt)
     assert not tn.status.any(), tn.status.tolist()
     check_two_rounds(prev, nxt, tn, S0_pool, range(len(prev_trees)), bf16=state_dtype == "bf16")
 
 
+@pytest.mark.parametrize("cap", [CAP, CAP2])
 @pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
-def test_warp_commit_verify_short_paths(cuda_lib, state_dtype):
+def test_warp_commit_verify_short_paths(cuda_lib, state_dtype, cap):
     """Previous trees of at most 16 nodes (one update pass with every node's U
     and key row requested up front; a bf16 pool's S_a rounded once), next
     trees of up to 16: chains, stars, binary and random trees, accepted nodes
@@ -260,9 +262,9 @@ def test_warp_commit_verify_short_paths(cuda_lib, state_dtype):
     prev_trees = [wl.chain_parents(16), np.array([-1] + [0] * 15, np.int32), random_tree(rng, 5),
                   random_tree(rng, 12), wl.chain_parents(3), random_tree(rng, 1),
                   wl.complete_binary_parents(4), wl.chain_parents(8)]
-    next_trees = [random_tree(rng, n) for n in (CAP, 1, 11, 2, 0, CAP - 1, 15, 9)]
+    next_trees = [random_tree(rng, n) for n in (cap, 1, 11, 2, 0, cap - 1, 15, 9)]
     accepted = [15, 9, 4, 11, -1, 0, 14, 7]
-    prev, nxt = two_rounds(prev_trees, next_trees, accepted, cap=CAP, state_dtype=state_dtype, seed=11)
+    prev, nxt = two_rounds(prev_trees, next_trees, accepted, cap=cap, state_dtype=state_dtype, seed=11)
     assert prev.max_nodes <= 16
     tn, S0_pool = run_commit_verify(prev, nxt)
     assert not tn.status.any(), tn.status.tolist()
