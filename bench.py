@@ -711,9 +711,9 @@ def study_graph(args, local):
 def study_bf16state(args, local):
     """A bf16 state pool (32 KiB per head instead of 64 KiB), the serving
     dtype: 30 layers of verify + commit, and the fused commit-into-verify
-    step, on the wide ragged workload (the benchmark) and on the chain
-    workload (multi-token-prediction chains, the pages' serving shape); one
-    JSON line each.  Each step cycles through 30 layers of distinct inputs,
+    step, on the wide ragged workload (the benchmark), on the chain workload
+    (multi-token-prediction chains, the pages' serving shape) and on the
+    binary-tree workload; one JSON line each.  Each step cycles through 30 layers of distinct inputs,
     more than the 129 MB L2 holds."""
     from gdn_speculative_tree_gb300 import binding
     dev = torch.device("cuda", local)
@@ -722,7 +722,8 @@ def study_bf16state(args, local):
     layers = args.layers
     g = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
     for name, label in ((CONFIG_NAME, "wide ragged trees, 256 req x 32 heads"),
-                        ("chain", "MTP chains of 4, 64 req x 32 heads")):
+                        ("chain", "MTP chains of 4, 64 req x 32 heads"),
+                        ("binary", "complete binary trees of 15 nodes, 128 req x 32 heads")):
         cfg = wl.CONFIGS[name]
         work = [binding.TreeVerifier(wl.generate(cfg, layer=l, device=dev, state_dtype="bf16"))
                 for l in range(layers)]
