@@ -14,7 +14,8 @@
 //           beta_n gamma_n (S0 k_n)[d], and the read-out's first term
 //           gamma_n (S0 q_n)[d]; the accumulator layout of MMA 1 is already
 //           the A-operand layout of MMA 2.
-//  Gram     warp w: slots 16w..16w+15 of [K;Q] times K^T, written over the
+//  Gram     slots 16m..16m+15 of [K;Q] times K^T, the key columns split in
+//           halves between warps m and m + NPM/8, each half written over its
 //           warp's own (already read) rows of the state tile.
 //  rows     thread t builds operand row t of [T;B], T = (I + A)^-1 and
 //           B = M T restricted to node n's root path (both non-zero only
@@ -28,12 +29,13 @@
 //           children) are multiplied.
 //  store    each lane writes its two adjacent value rows of U[n] and o_n.
 //
-// The kernel is written for a capacity NPM of up to 64 nodes, and launched
-// for NPM = 16 (plain and fused) and 32 (plain): three CTAs per SM fit (76 KB
-// of shared memory at 16 nodes, 68 KB at 32 with the fp32 state streamed
-// through a ring of three of its four boxes, 80 registers; a bf16 pool's
-// 16-node instances four CTAs, 44 KB and 64 registers: its 32 KB tile region
-// also holds the Gram rows and the [T;B] halves).  At 64 nodes it measured
+// The kernel is written for a capacity NPM of up to 32 nodes, and launched
+// for NPM = 16 (plain and fused) and 32 (plain; fused on a bf16 pool): three
+// CTAs per SM fit (76 KB of shared memory at 16 nodes, 68 KB at 32 with the
+// fp32 state streamed through a ring of three of its four boxes, 80
+// registers; a bf16 pool's 16-node instances four CTAs, 44 KB and 64
+// registers: its 32 KB tile region also holds the Gram rows and the [T;B]
+// halves).  A 64-node version measured
 // ~35 % slower than the tcgen05 kernel: the first products take two warp
 // MMAs per 8-node tile and state element pair (hi and lo), and warp MMAs run
 // at ~0.47 m16n8k16 per cycle per SM, about a quarter of the tcgen05 rate,
@@ -81,7 +83,7 @@ static_assert(sizeof(WarpPrev) <= kWPathOff, "previous tree before the key rows"
 
 // Dynamic shared memory: alignment slack, a 64 KB region that first holds
 // the state tile (4 boxes of 32 fp32 or 2 of 64 bf16 columns, 128B swizzle)
-// and later the Gram rows (boxes 0-1: each warp over its own state rows) and
+// and later the Gram rows (box 0: each warp over its own state rows) and
 // the hi and lo halves of the [T;B] operand (boxes 2 and 3), the 2 NPM K/Q
 // slot rows (later the x scratch of root paths longer than kWRegPath), the
 // tree.
@@ -106,7 +108,7 @@ struct WarpCfg {
   static constexpr int kBlocks = (SB && NPM == 16) ? 4 : ((NPM == 16 || SB || kRing) ? 3 : 2);
   static_assert(kBlocks * (kDynSmem + 1024u) <= 228u * 1024u, "CTAs per SM");
   static_assert(8u * NPM * NPM <= kKQBytes, "x scratch of 2 NPM long paths");
-  static_assert(2 * NPM <= kWThreads && NPM <= 64, "one operand row per thread");
+  static_assert(2 * NPM <= kWThreads && NPM <= 32, "one operand row per thread; Gram halves in box 0");
   static_assert(kWPathOff + kWSeg * kWPathStride <= kKQBytes, "fused commit staging");
   static_assert(kWSeg == kWarpSegEntries, "entries per update pass");
 };
@@ -123,12 +125,15 @@ __device__ __forceinline__ uint2 wlds64(const unsigned char* p) {
   return *reinterpret_cast<const uint2*>(p);
 }
 
-// Gram entry slot_m . key_i (fp32), row m of the Gram region: key columns
-// 0-31 in box 0, 32-63 in box 1 of the state region, at state row m (warp
-// m / 16 writes it over its own rows), words XOR-ed by (m mod 4) * 8 so that
-// the dump's 8-byte stores meet distinct banks.
+// Gram entry slot_m . key_i (fp32) in the Gram region of box 0.  The key
+// columns come in two halves computed by different warps (warp w: slots of
+// tile w mod KT, half w / KT); half h of slot m sits at state row m + 2 NPM h,
+// i.e. over the computing warp's own rows, its words XOR-ed by (m mod 4) * 8
+// so that the dump's 8-byte stores meet distinct banks.
+template <int NPM>
 __device__ __forceinline__ uint32_t gram_off(int m, int i) {
-  return static_cast<uint32_t>((i >> 5) * kWBox + m * 128 + (((i & 31) ^ ((m & 3) << 3)) << 2));
+  const int hh = i / (NPM / 2);
+  return static_cast<uint32_t>((m + 2 * NPM * hh) * 128 + (((i & 31) ^ ((m & 3) << 3)) << 2));
 }
 
 // [T;B] operand halves: row o = output column (T rows 0..NPM-1, B rows
@@ -602,44 +607,43 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB, FUSED>::kBlocks)
 #pragma unroll
       for (int i = 0; i < 4; ++i) oi[j][i] = acc[KT + j][i];
 
-    // ---- Gram: slots 16 warp .. 16 warp + 15 (fragment rows g, g + 8) times
-    //      the live key tiles, in passes of at most 4 tiles, written over the
-    //      warp's own rows of the state tile (all read above; a fused commit's
-    //      store of S_a must have read the tile first)
+    // ---- Gram: warps w and w + KT take the two halves of the live key
+    //      tiles against slots 16 (w mod KT) .. + 15 (fragment rows g, g + 8)
+    //      and write them over their own rows of the state tile (all read
+    //      above; a fused commit's store of S_a must have read the tile first)
     if (stored) {
       if (t == 0) bulk_wait_group_read0();
       __syncthreads();
     }
     __syncwarp();
-    const int mt = warp < KT / 2 ? warp : warp - KT / 2;  // key tile pair of these slots
-    if (warp < KT && 2 * mt < live_tiles) {
-      constexpr int kGP = KT < 4 ? KT : 4;
+    if (warp < 2 * KT) {
+      const int gmt = warp % KT, hh = warp / KT;
+      const int mtp = gmt < KT / 2 ? gmt : gmt - KT / 2;  // key tile pair of these slots
+      constexpr int kNH = KT / 2;                         // key tiles per half
+      const int nt0 = hh * kNH;
+      if (2 * mtp < live_tiles && nt0 < live_tiles) {
+        float gd[kNH][4];
 #pragma unroll
-      for (int gp = 0; gp < KT / kGP; ++gp) {
-        if (kGP * gp < live_tiles) {
-          float gd[kGP][4];
-#pragma unroll
-          for (int i = 0; i < kGP; ++i) gd[i][0] = gd[i][1] = gd[i][2] = gd[i][3] = 0.f;
+        for (int i = 0; i < kNH; ++i) gd[i][0] = gd[i][1] = gd[i][2] = gd[i][3] = 0.f;
 #pragma unroll 2
-          for (int ks = 0; ks < 8; ++ks) {
-            const int cb = (16 * ks + 4 * q) * 2;
-            const uint2 x0 = wlds64(kqs + (16 * warp + g) * kWKQStride + cb);
-            const uint2 x1 = wlds64(kqs + (16 * warp + g + 8) * kWKQStride + cb);
+        for (int ks = 0; ks < 8; ++ks) {
+          const int cb = (16 * ks + 4 * q) * 2;
+          const uint2 x0 = wlds64(kqs + (16 * gmt + g) * kWKQStride + cb);
+          const uint2 x1 = wlds64(kqs + (16 * gmt + g + 8) * kWKQStride + cb);
 #pragma unroll
-            for (int i = 0; i < kGP; ++i) {
-              if (kGP * gp + i < live_tiles) {
-                const uint2 bk = wlds64(kqs + (8 * (kGP * gp + i) + g) * kWKQStride + cb);
-                mma16816_bf16_nv(gd[i], x0.x, x1.x, x0.y, x1.y, bk.x, bk.y);
-              }
+          for (int i = 0; i < kNH; ++i) {
+            if (nt0 + i < live_tiles) {
+              const uint2 bk = wlds64(kqs + (8 * (nt0 + i) + g) * kWKQStride + cb);
+              mma16816_bf16_nv(gd[i], x0.x, x1.x, x0.y, x1.y, bk.x, bk.y);
             }
           }
+        }
 #pragma unroll
-          for (int i = 0; i < kGP; ++i) {
-            const int col = 8 * (kGP * gp + i) + 2 * q;
-            const int m0 = 16 * warp + g;
-            *reinterpret_cast<float2*>(s0 + gram_off(m0, col)) = make_float2(gd[i][0], gd[i][1]);
-            *reinterpret_cast<float2*>(s0 + gram_off(m0 + 8, col)) = make_float2(gd[i][2], gd[i][3]);
-          }
+        for (int i = 0; i < kNH; ++i) {
+          const int col = 8 * (nt0 + i) + 2 * q;
+          const int m0 = 16 * gmt + g;
+          *reinterpret_cast<float2*>(s0 + gram_off<NPM>(m0, col)) = make_float2(gd[i][0], gd[i][1]);
+          *reinterpret_cast<float2*>(s0 + gram_off<NPM>(m0 + 8, col)) = make_float2(gd[i][2], gd[i][3]);
         }
       }
     }
@@ -660,7 +664,7 @@ __global__ void __launch_bounds__(kWThreads, WarpCfg<NPM, SB, FUSED>::kBlocks)
           *reinterpret_cast<uint4*>(opl + off) = make_uint4(0u, 0u, 0u, 0u);
         }
         const unsigned char* gq = s0;  // Gram rows: key slot m = node m, query slot NPM + n
-        auto G = [&](int m, int i) { return *reinterpret_cast<const float*>(gq + gram_off(m, i)); };
+        auto G = [&](int m, int i) { return *reinterpret_cast<const float*>(gq + gram_off<NPM>(m, i)); };
         int pn[kWRegPath];
         float al[kWRegPath], be[kWRegPath], x[kWRegPath];
         int L = 0, cur = n;
